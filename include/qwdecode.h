@@ -1,0 +1,197 @@
+/*
+ * qwdecode — forward pass of a Qwen3-0.6B-shaped decoder (prefill and KV-cached
+ * decode) with its sampler, as hand-written CUDA for GB300 (sm_103a).
+ *
+ * The operations are those of "Inside an LLM: Pure Python Inference for
+ * Qwen3-0.6B on MLX":
+ *   Step 2  embedding lookup              x = E[ids]
+ *   Step 3  RMSNorm                       x / sqrt(mean(x^2) + eps) * w
+ *   Step 4  RoPE (half-split pairs)       angle = pos * theta^(-i/64)
+ *   Step 5  attention with grouped query heads, QK-Norm, the KV cache and the
+ *           causal mask
+ *   Step 6  SwiGLU feed-forward           (silu(x Wg^T) * x Wu^T) Wd^T
+ *   Step 7  pre-norm block with residuals
+ *   Step 8  final norm, LM head (tied to E here) and sample()
+ *   Step 9  the generation loop: one prefill, then one decode step per token
+ *
+ * Conventions for every call
+ *   - Array arguments marked DEVICE are device pointers owned by the caller;
+ *     HOST marks host pointers.  Work is enqueued on `stream` (a cudaStream_t
+ *     passed as void*, NULL = legacy default stream); calls return once the work
+ *     is enqueued, except where noted.
+ *   - bf16 values cross the boundary as uint16_t bit patterns.
+ *   - Return value: QW_OK (0) or a negative QW_E* code; the reason is available
+ *     from qw_last_error_message() on the calling thread.  Nothing throws and no
+ *     kernel traps: bad device-side inputs (token id out of range, position past
+ *     the block table, page id outside the pool) are skipped by the kernels and
+ *     recorded in a device error word that qw_check() reports.
+ *   - A context is not thread-safe: serialise calls on one qw_ctx.
+ */
+#ifndef QWDECODE_H
+#define QWDECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QW_OK 0
+#define QW_EINVAL (-1)    /* bad argument (null pointer, size out of range, unsupported shape) */
+#define QW_ERANGE (-2)    /* token id, position or page id out of range (reported by qw_check) */
+#define QW_ENOMEM (-3)    /* device allocation failed */
+#define QW_EKVFULL (-4)   /* a KV pool request larger than the device can hold */
+#define QW_ECUDA (-5)     /* a CUDA runtime or driver call failed */
+#define QW_ETIMEOUT (-6)  /* a bounded device-side wait gave up (reported by qw_check) */
+
+#define QW_PAGE_SIZE 16   /* tokens per KV page */
+#define QW_HEAD_DIM 128   /* the only head size the kernels implement */
+#define QW_MAX_TOP_K 1024 /* largest top_k qw_sample accepts */
+
+typedef struct qw_ctx qw_ctx;
+typedef struct qw_kv qw_kv;
+
+/* Model sizes and workspace limits.  qw_config_default() fills Qwen3-0.6B:
+ * 28 layers, hidden 1024, 16 query / 8 KV heads of 128, SwiGLU 3072,
+ * vocab 151936, eps 1e-6 (Step 3), RoPE base theta 1e6 (Step 4 gives one million
+ * as the Qwen3 value). */
+typedef struct qw_config {
+    int32_t n_layers;
+    int32_t hidden;        /* multiple of 256, at most 4096 */
+    int32_t n_heads;       /* query heads; n_heads * head_dim is a multiple of 256 */
+    int32_t n_kv_heads;    /* divides n_heads */
+    int32_t head_dim;      /* must be QW_HEAD_DIM */
+    int32_t intermediate;  /* multiple of 128 */
+    int32_t vocab;         /* multiple of 32 */
+    int32_t max_batch;     /* most rows in one qw_decode_step or qw_sample call (<= 256) */
+    int32_t max_tokens;    /* most tokens in one qw_prefill call (sizes the workspaces) */
+    int32_t debug_hidden;  /* nonzero: keep the residual after every layer for qw_debug_hidden */
+    float rms_eps;
+    double rope_theta;
+} qw_config;
+
+/* Weights as the checkpoint names them (Step 5-8 code): bf16 bit patterns,
+ * row-major [out_features][in_features].  Per-layer members point to arrays of
+ * n_layers pointers.  `on_device` = 1: every tensor pointer is a device pointer;
+ * 0: host pointers.  qw_init copies everything; the caller may free its copies
+ * afterwards.  The LM head is tied to embed_tokens (no lm_head tensor). */
+typedef struct qw_weights {
+    const uint16_t* embed_tokens;              /* model.embed_tokens.weight   [vocab][hidden] */
+    const uint16_t* norm;                      /* model.norm.weight           [hidden] */
+    const uint16_t* const* input_layernorm;    /* .input_layernorm.weight     [hidden] */
+    const uint16_t* const* q_proj;             /* .self_attn.q_proj.weight    [n_heads*head_dim][hidden] */
+    const uint16_t* const* k_proj;             /* .self_attn.k_proj.weight    [n_kv_heads*head_dim][hidden] */
+    const uint16_t* const* v_proj;             /* .self_attn.v_proj.weight    [n_kv_heads*head_dim][hidden] */
+    const uint16_t* const* q_norm;             /* .self_attn.q_norm.weight    [head_dim] */
+    const uint16_t* const* k_norm;             /* .self_attn.k_norm.weight    [head_dim] */
+    const uint16_t* const* o_proj;             /* .self_attn.o_proj.weight    [hidden][n_heads*head_dim] */
+    const uint16_t* const* post_attention_layernorm; /* [hidden] */
+    const uint16_t* const* gate_proj;          /* .mlp.gate_proj.weight       [intermediate][hidden] */
+    const uint16_t* const* up_proj;            /* .mlp.up_proj.weight         [intermediate][hidden] */
+    const uint16_t* const* down_proj;          /* .mlp.down_proj.weight       [hidden][intermediate] */
+    int32_t on_device;
+} qw_weights;
+
+/* Per-row sampling parameters (Step 8 sample(), plus a top-k cap). */
+typedef struct qw_sample_params {
+    float temperature;  /* 0: greedy argmax (lowest id wins a tie); > 0: sample */
+    int32_t top_k;      /* 1 .. QW_MAX_TOP_K: at most this many candidates (used when temperature > 0) */
+    float top_p;        /* (0, 1]: keep the smallest prefix of the sorted distribution whose mass reaches top_p */
+    uint32_t reserved;  /* set to 0 */
+    uint64_t seed;      /* Philox4x32-10 key of this row (e.g. the sequence id) */
+} qw_sample_params;
+
+/* Fill `cfg` with the Qwen3-0.6B sizes, max_batch 64, max_tokens 16384. */
+void qw_config_default(qw_config* cfg);
+
+/* Validate `cfg`, upload and repack the weights, allocate workspaces.
+ * On success *out owns all device memory it allocated; free with qw_destroy.
+ * Synchronous.  Errors: QW_EINVAL (sizes), QW_ENOMEM, QW_ECUDA. */
+int qw_init(const qw_config* cfg, const qw_weights* weights, qw_ctx** out);
+int qw_destroy(qw_ctx* ctx);
+
+/* Allocate a paged KV pool of `n_pages` pages for every layer.
+ * Layout (bf16): [n_layers][n_pages][2 (K, V)][n_kv_heads][QW_PAGE_SIZE][head_dim];
+ * one page holds QW_PAGE_SIZE consecutive positions of one sequence.  Keys are
+ * stored after QK-Norm and RoPE (Step 5: the cache holds the rotated keys).
+ * Errors: QW_EINVAL, QW_EKVFULL (more than the free device memory). */
+int qw_kv_create(qw_ctx* ctx, int32_t n_pages, qw_kv** out);
+int qw_kv_destroy(qw_kv* kv);
+/* Base device address and byte strides of the pool (for injecting or reading caches). */
+int qw_kv_layout(const qw_kv* kv, void** base, int64_t* layer_stride, int64_t* page_stride, int32_t* n_pages);
+
+/* Prefill (Step 9): all prompt tokens of every sequence in one pass.
+ *   ids, positions   DEVICE int32[n_tok], n_tok = cu_seqlens[n_seqs]: the tokens of
+ *                    sequence s are rows cu_seqlens[s] .. cu_seqlens[s+1]-1, with
+ *                    consecutive positions.  Every position below a sequence's first
+ *                    position must already be in the cache (chunked prefill), so a
+ *                    fresh sequence starts at position 0.
+ *   cu_seqlens       HOST int32[n_seqs+1], cu_seqlens[0] = 0, nondecreasing, n_tok <= max_tokens.
+ *   block_tables     DEVICE int32[n_seqs][bt_stride]: page ids; position p of sequence s
+ *                    lives in page block_tables[s][p / QW_PAGE_SIZE], slot p % QW_PAGE_SIZE.
+ *   last_logits      DEVICE float[n_seqs][vocab] or NULL: logits of each sequence's last token.
+ * Writes K/V of every token into the pool.  Attention of a token at position p sees
+ * the cached positions 0 .. p of its sequence (the causal mask of Step 5). */
+int qw_prefill(qw_ctx* ctx, const int32_t* ids, const int32_t* positions, const int32_t* cu_seqlens,
+               int32_t n_seqs, qw_kv* kv, const int32_t* block_tables, int32_t bt_stride,
+               float* last_logits, void* stream);
+
+/* One decode step for `batch` sequences, one token each (Step 9 loop body).
+ *   tokens, positions  DEVICE int32[batch]; row b is at position positions[b] and sees
+ *                      positions 0 .. positions[b] of its cache (its own K/V included).
+ *   block_tables       DEVICE int32[batch][bt_stride].
+ *   logits             DEVICE float[batch][vocab], or NULL to keep them in the context
+ *                      (qw_sample with logits == NULL then reads them).
+ * 1 <= batch <= max_batch. */
+int qw_decode_step(qw_ctx* ctx, const int32_t* tokens, const int32_t* positions, int32_t batch,
+                   qw_kv* kv, const int32_t* block_tables, int32_t bt_stride, float* logits,
+                   void* stream);
+
+/* Sample one id per row (Step 8 sample()).
+ *   logits   DEVICE float[batch][vocab], or NULL for the context's logits from the last
+ *            qw_decode_step / qw_prefill call that returned them in the context.
+ *   params   DEVICE qw_sample_params[batch].
+ *   rng_counter  Philox counter of this step: row b draws u from Philox4x32-10 with
+ *            key = params[b].seed and counter = (rng_counter, 0, 0) as four 32-bit
+ *            words (low word first); u = (word0 >> 8) * 2^-24.
+ *   out_ids  DEVICE int32[batch].
+ * Greedy rows take the argmax.  Sampling rows take softmax(logits / temperature) over
+ * the whole vocabulary, sort it descending (ties: lower id first), keep
+ * cutoff = min(top_k, 1 + #(cumsum < top_p)) entries, and return the first kept
+ * entry whose cumulative kept mass exceeds u * (kept mass). */
+int qw_sample(qw_ctx* ctx, const float* logits, int32_t batch, const qw_sample_params* params,
+              uint64_t rng_counter, int32_t* out_ids, void* stream);
+
+/* Wait for `stream`, then return and clear the first error the kernels recorded
+ * since the last check (QW_OK if none). */
+int qw_check(qw_ctx* ctx, void* stream);
+
+/* Reason for the last non-zero return on this thread ("" if none). */
+const char* qw_last_error_message(void);
+
+/* Copy the residual stream after layer `layer` (0 .. n_layers-1) of the last
+ * qw_prefill or qw_decode_step into DEVICE float[n_rows][hidden] (n_rows = tokens of
+ * that call).  Needs debug_hidden; for checking, not for speed. */
+int qw_debug_hidden(qw_ctx* ctx, int32_t layer, float* out, int32_t n_rows, void* stream);
+
+/* Test hook for the tensor-core projection kernel alone: C = A . B^T with
+ *   A DEVICE bf16[M][K], B DEVICE bf16[N][K] (the layout of every weight), K % 64 == 0,
+ *   N % 32 == 0, bn = 128 or 256 (output tile width) and the epilogue
+ *   epi = 0: C is float[M][N], C = A B^T;  1: C += A B^T (residual add);
+ *   epi = 2: C is bf16[M][N/2], C[m][j] = silu(Y[m][2j]) * Y[m][2j+1] with Y = A B^T
+ *   (the SwiGLU of Step 6 on gate/up rows interleaved). */
+int qw_debug_gemm(const uint16_t* A, const uint16_t* B, void* C, int32_t M, int32_t N, int32_t K, int32_t epi,
+                  int32_t bn, void* stream);
+
+/* Number of kernels this library has launched in the process so far (all contexts). */
+uint64_t qw_kernel_launches(void);
+
+/* Select the decode implementation: 0 = automatic, 1 = per-op kernels,
+ * 2 = the fused persistent small-batch kernel (batch <= 8).  For tests. */
+int qw_set_decode_path(qw_ctx* ctx, int32_t path);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QWDECODE_H */

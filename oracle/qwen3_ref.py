@@ -38,9 +38,8 @@ M32 = 0xFFFFFFFF
 def bf16_to_f64(t) -> np.ndarray:
     """Exact widening of bf16 values (torch.bfloat16 tensor or uint16 bit array) to float64."""
     if isinstance(t, torch.Tensor):
-        bits = t.contiguous().view(torch.int16).numpy().view(np.uint16)
-    else:
-        bits = np.asarray(t, dtype=np.uint16)
+        return t.detach().to("cpu").contiguous().view(torch.bfloat16).to(torch.float64).numpy()
+    bits = np.asarray(t, dtype=np.uint16)
     return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 

@@ -1,0 +1,51 @@
+"""The tensor-core projection kernel (tcgen05 + TMA + TMEM) against a plain
+PyTorch fp32 reference of the same contraction, through the C ABI hook."""
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bd():
+    from transformer_decode_qwen3_gb300 import binding
+    binding.load()
+    return binding
+
+
+def _operands(M, N, K, seed):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    A = (torch.randn(M, K, generator=g) * 0.5).to(torch.bfloat16).cuda()
+    B = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16).cuda()
+    return A, B, A.float() @ B.float().T
+
+
+@pytest.mark.parametrize("M,N,K,bn", [(128, 256, 64, 256), (1, 4096, 1024, 256), (5, 1024, 2048, 128),
+                                      (300, 6144, 1024, 256), (64, 1024, 3072, 128), (257, 384, 1024, 256),
+                                      (130, 151936, 1024, 256)])
+def test_gemm_store(bd, M, N, K, bn):
+    A, B, ref = _operands(M, N, K, M * 7 + N)
+    C = torch.full((M, N), float("nan"), device="cuda")
+    bd.debug_gemm(A, B, C, epi=0, bn=bn)
+    torch.cuda.synchronize()
+    err = (C - ref).norm() / ref.norm()
+    assert torch.isfinite(C).all() and err < 1e-5, f"rel err {err:.3e}"
+
+
+def test_gemm_residual_add(bd):
+    A, B, ref = _operands(200, 1024, 2048, 3)
+    X = torch.randn(200, 1024, device="cuda")
+    C = X.clone()
+    bd.debug_gemm(A, B, C, epi=1, bn=128)
+    torch.cuda.synchronize()
+    torch.testing.assert_close(C, X + ref, rtol=1e-4, atol=1e-4)
+
+
+def test_gemm_swiglu_pairs(bd):
+    A, B, ref = _operands(130, 768, 256, 4)
+    C = torch.zeros(130, 384, dtype=torch.bfloat16, device="cuda")
+    bd.debug_gemm(A, B, C, epi=2, bn=256)
+    torch.cuda.synchronize()
+    g, u = ref[:, 0::2], ref[:, 1::2]
+    expect = g * torch.sigmoid(g) * u
+    torch.testing.assert_close(C.float(), expect, rtol=1e-2, atol=1e-3)

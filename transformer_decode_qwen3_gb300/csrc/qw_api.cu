@@ -1,0 +1,508 @@
+// Host runtime behind the C ABI of include/qwdecode.h: configuration checks,
+// weight upload and repacking, workspaces, the paged KV pool, and the launch
+// sequences of prefill, decode and sampling.
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+#include <string>
+#include <vector>
+
+#include "qw_common.cuh"
+#include "qw_fused.h"
+#include "qw_internal.h"
+
+using namespace qw;
+namespace qw {
+unsigned long long launches_so_far();
+}
+
+namespace {
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+    g_last_error = msg;
+    return code;
+}
+}  // namespace
+
+#define QW_CUDA(call)                                                                              \
+    do {                                                                                           \
+        cudaError_t e_ = (call);                                                                   \
+        if (e_ != cudaSuccess) return fail(QW_ECUDA, std::string(#call) + ": " + cudaGetErrorString(e_)); \
+    } while (0)
+#define QW_TRY(call, what)                                  \
+    do {                                                    \
+        int rc_ = (call);                                   \
+        if (rc_ != QW_OK) return fail(rc_, what);           \
+    } while (0)
+
+struct LayerW {
+    uint16_t *wqkv, *wo, *wgu, *wd;  // [qkv_dim][D], [D][Hq*d], [2I][D] (gate, up rows interleaved), [D][I]
+    float *in_norm, *post_norm, *q_norm, *k_norm;
+    CUtensorMap tm_qkv, tm_o, tm_gu, tm_d;
+};
+
+struct qw_ctx {
+    qw_config cfg;
+    int dev = 0, n_sm = 0;
+    int qkv_dim = 0, attn_dim = 0;
+    uint8_t* wbuf = nullptr;
+    uint16_t* E = nullptr;
+    float* final_norm = nullptr;
+    float* inv_freq = nullptr;
+    std::vector<LayerW> L;
+    CUtensorMap tm_E;
+    // workspaces
+    uint8_t* wsbuf = nullptr;
+    float *x = nullptr, *qkv = nullptr, *q = nullptr, *logits = nullptr, *part = nullptr, *hidden = nullptr;
+    uint16_t *h = nullptr, *attn = nullptr, *act = nullptr;
+    int *tok_seq = nullptr, *iota = nullptr, *rows_last = nullptr, *err = nullptr;
+    int4* tiles = nullptr;
+    int max_rows = 0, max_splits = 128, max_tiles = 0;
+    int last_rows = 0, logits_rows = 0;
+    int decode_path = 0;
+    FusedDecode* fused = nullptr;
+};
+
+struct qw_kv {
+    qw_ctx* ctx;
+    uint16_t* base;
+    int32_t n_pages;
+    int64_t page_elems;   // elements per page (2 * n_kv * 16 * 128)
+    int64_t layer_elems;  // elements per layer (n_pages * page_elems)
+};
+
+extern "C" {
+
+void qw_config_default(qw_config* c) {
+    if (!c) return;
+    c->n_layers = 28;
+    c->hidden = 1024;
+    c->n_heads = 16;
+    c->n_kv_heads = 8;
+    c->head_dim = QW_HEAD_DIM;
+    c->intermediate = 3072;
+    c->vocab = 151936;
+    c->max_batch = 64;
+    c->max_tokens = 16384;
+    c->debug_hidden = 0;
+    c->rms_eps = 1e-6f;
+    c->rope_theta = 1e6;
+}
+
+const char* qw_last_error_message(void) { return g_last_error.c_str(); }
+
+static int validate_config(const qw_config* c) {
+    if (c->n_layers < 1 || c->n_layers > 256) return fail(QW_EINVAL, "n_layers must be in [1, 256]");
+    if (c->hidden < 256 || c->hidden % 256 || c->hidden > 4096)
+        return fail(QW_EINVAL, "hidden must be a multiple of 256 in [256, 4096]");
+    if (c->head_dim != QW_HEAD_DIM) return fail(QW_EINVAL, "head_dim must be 128");
+    if (c->n_kv_heads < 1 || c->n_heads != 2 * c->n_kv_heads)
+        return fail(QW_EINVAL, "the attention kernels implement n_heads == 2 * n_kv_heads");
+    if ((c->n_heads * c->head_dim) % 256) return fail(QW_EINVAL, "n_heads * head_dim must be a multiple of 256");
+    if (c->intermediate < 128 || c->intermediate % 128) return fail(QW_EINVAL, "intermediate must be a multiple of 128");
+    if (c->vocab < 32 || c->vocab % 32) return fail(QW_EINVAL, "vocab must be a positive multiple of 32");
+    if (c->max_batch < 1 || c->max_batch > 256) return fail(QW_EINVAL, "max_batch must be in [1, 256]");
+    if (c->max_tokens < 1 || c->max_tokens > (1 << 20)) return fail(QW_EINVAL, "max_tokens must be in [1, 2^20]");
+    if (!(c->rms_eps > 0.f) || !(c->rope_theta > 1.0)) return fail(QW_EINVAL, "rms_eps > 0 and rope_theta > 1 required");
+    return QW_OK;
+}
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+static int upload_norm(float* dst, const uint16_t* src, int n, int on_device) {
+    if (on_device) {
+        QW_TRY(launch_bf16_to_f32(src, dst, n, 0), "bf16_to_f32 launch");
+        return QW_OK;
+    }
+    std::vector<float> tmp(n);
+    for (int i = 0; i < n; ++i) {
+        uint32_t b = (uint32_t)src[i] << 16;
+        memcpy(&tmp[i], &b, 4);
+    }
+    QW_CUDA(cudaMemcpy(dst, tmp.data(), n * sizeof(float), cudaMemcpyHostToDevice));
+    return QW_OK;
+}
+
+static void free_ctx(qw_ctx* c) {
+    if (!c) return;
+    if (c->fused) fused_destroy(c->fused);
+    if (c->wbuf) cudaFree(c->wbuf);
+    if (c->wsbuf) cudaFree(c->wsbuf);
+    delete c;
+}
+
+int qw_init(const qw_config* cfg, const qw_weights* w, qw_ctx** out) {
+    if (!cfg || !w || !out) return fail(QW_EINVAL, "null argument");
+    *out = nullptr;
+    int rc = validate_config(cfg);
+    if (rc) return rc;
+    const qw_config& c = *cfg;
+    if (!w->embed_tokens || !w->norm || !w->input_layernorm || !w->q_proj || !w->k_proj || !w->v_proj ||
+        !w->q_norm || !w->k_norm || !w->o_proj || !w->post_attention_layernorm || !w->gate_proj || !w->up_proj ||
+        !w->down_proj)
+        return fail(QW_EINVAL, "null weight pointer");
+    for (int l = 0; l < c.n_layers; ++l)
+        if (!w->input_layernorm[l] || !w->q_proj[l] || !w->k_proj[l] || !w->v_proj[l] || !w->q_norm[l] ||
+            !w->k_norm[l] || !w->o_proj[l] || !w->post_attention_layernorm[l] || !w->gate_proj[l] ||
+            !w->up_proj[l] || !w->down_proj[l])
+            return fail(QW_EINVAL, "null per-layer weight pointer");
+
+    qw_ctx* ctx = new qw_ctx();
+    ctx->cfg = c;
+    cudaGetDevice(&ctx->dev);
+    cudaDeviceGetAttribute(&ctx->n_sm, cudaDevAttrMultiProcessorCount, ctx->dev);
+    const int D = c.hidden, Hq = c.n_heads, Hkv = c.n_kv_heads, d = c.head_dim, I = c.intermediate, V = c.vocab;
+    ctx->qkv_dim = (Hq + 2 * Hkv) * d;
+    ctx->attn_dim = Hq * d;
+
+    // ---- weights: one allocation, 1 KiB-aligned pieces
+    const size_t A = 1024;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off = align_up(off + bytes, A);
+        return o;
+    };
+    const size_t oE = take((size_t)V * D * 2);
+    const size_t oFinal = take((size_t)D * 4);
+    const size_t oFreq = take(64 * 4);
+    struct Offs { size_t qkv, o, gu, dn, inn, post, qn, kn; };
+    std::vector<Offs> lo(c.n_layers);
+    for (int l = 0; l < c.n_layers; ++l) {
+        lo[l].qkv = take((size_t)ctx->qkv_dim * D * 2);
+        lo[l].o = take((size_t)D * ctx->attn_dim * 2);
+        lo[l].gu = take((size_t)2 * I * D * 2);
+        lo[l].dn = take((size_t)D * I * 2);
+        lo[l].inn = take((size_t)D * 4);
+        lo[l].post = take((size_t)D * 4);
+        lo[l].qn = take((size_t)d * 4);
+        lo[l].kn = take((size_t)d * 4);
+    }
+    if (cudaMalloc(&ctx->wbuf, off) != cudaSuccess) {
+        free_ctx(ctx);
+        return fail(QW_ENOMEM, "weight allocation failed");
+    }
+    const cudaMemcpyKind kind = w->on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice;
+    uint8_t* B = ctx->wbuf;
+    ctx->E = (uint16_t*)(B + oE);
+    ctx->final_norm = (float*)(B + oFinal);
+    ctx->inv_freq = (float*)(B + oFreq);
+#define QW_INIT_CUDA(call)                                                                          \
+    do {                                                                                            \
+        cudaError_t e_ = (call);                                                                    \
+        if (e_ != cudaSuccess) {                                                                    \
+            free_ctx(ctx);                                                                          \
+            return fail(QW_ECUDA, std::string(#call) + ": " + cudaGetErrorString(e_));              \
+        }                                                                                           \
+    } while (0)
+    QW_INIT_CUDA(cudaMemcpy(ctx->E, w->embed_tokens, (size_t)V * D * 2, kind));
+    if ((rc = upload_norm(ctx->final_norm, w->norm, D, w->on_device))) {
+        free_ctx(ctx);
+        return rc;
+    }
+    {
+        // RoPE inverse frequencies (Step 4): float32(theta^(-i/half)), evaluated in double
+        float f[64];
+        for (int i = 0; i < d / 2; ++i) f[i] = (float)(1.0 / pow(c.rope_theta, (double)i / (double)(d / 2)));
+        QW_INIT_CUDA(cudaMemcpy(ctx->inv_freq, f, sizeof(float) * (d / 2), cudaMemcpyHostToDevice));
+    }
+    ctx->L.resize(c.n_layers);
+    for (int l = 0; l < c.n_layers; ++l) {
+        LayerW& Lw = ctx->L[l];
+        Lw.wqkv = (uint16_t*)(B + lo[l].qkv);
+        Lw.wo = (uint16_t*)(B + lo[l].o);
+        Lw.wgu = (uint16_t*)(B + lo[l].gu);
+        Lw.wd = (uint16_t*)(B + lo[l].dn);
+        Lw.in_norm = (float*)(B + lo[l].inn);
+        Lw.post_norm = (float*)(B + lo[l].post);
+        Lw.q_norm = (float*)(B + lo[l].qn);
+        Lw.k_norm = (float*)(B + lo[l].kn);
+        const size_t rowb = (size_t)D * 2;
+        QW_INIT_CUDA(cudaMemcpy(Lw.wqkv, w->q_proj[l], (size_t)Hq * d * rowb, kind));
+        QW_INIT_CUDA(cudaMemcpy(Lw.wqkv + (size_t)Hq * d * D, w->k_proj[l], (size_t)Hkv * d * rowb, kind));
+        QW_INIT_CUDA(cudaMemcpy(Lw.wqkv + (size_t)(Hq + Hkv) * d * D, w->v_proj[l], (size_t)Hkv * d * rowb, kind));
+        QW_INIT_CUDA(cudaMemcpy(Lw.wo, w->o_proj[l], (size_t)D * ctx->attn_dim * 2, kind));
+        // gate row j -> packed row 2j, up row j -> packed row 2j+1
+        QW_INIT_CUDA(cudaMemcpy2D(Lw.wgu, 2 * rowb, w->gate_proj[l], rowb, rowb, I, kind));
+        QW_INIT_CUDA(cudaMemcpy2D(Lw.wgu + D, 2 * rowb, w->up_proj[l], rowb, rowb, I, kind));
+        QW_INIT_CUDA(cudaMemcpy(Lw.wd, w->down_proj[l], (size_t)D * I * 2, kind));
+        if ((rc = upload_norm(Lw.in_norm, w->input_layernorm[l], D, w->on_device)) ||
+            (rc = upload_norm(Lw.post_norm, w->post_attention_layernorm[l], D, w->on_device)) ||
+            (rc = upload_norm(Lw.q_norm, w->q_norm[l], d, w->on_device)) ||
+            (rc = upload_norm(Lw.k_norm, w->k_norm[l], d, w->on_device))) {
+            free_ctx(ctx);
+            return rc;
+        }
+        if (make_tmap_bf16(&Lw.tm_qkv, Lw.wqkv, D, ctx->qkv_dim, rowb, 64, 256) ||
+            make_tmap_bf16(&Lw.tm_o, Lw.wo, ctx->attn_dim, D, (size_t)ctx->attn_dim * 2, 64, 128) ||
+            make_tmap_bf16(&Lw.tm_gu, Lw.wgu, D, 2 * I, rowb, 64, 256) ||
+            make_tmap_bf16(&Lw.tm_d, Lw.wd, I, D, (size_t)I * 2, 64, 128)) {
+            free_ctx(ctx);
+            return fail(QW_ECUDA, "cuTensorMapEncodeTiled failed for a weight");
+        }
+    }
+    if (make_tmap_bf16(&ctx->tm_E, ctx->E, D, V, (size_t)D * 2, 64, 256)) {
+        free_ctx(ctx);
+        return fail(QW_ECUDA, "cuTensorMapEncodeTiled failed for the embedding");
+    }
+
+    // ---- workspaces
+    const int T = std::max(c.max_tokens, c.max_batch);
+    ctx->max_rows = T;
+    ctx->max_tiles = c.max_tokens / 64 + c.max_tokens + 1;
+    off = 0;
+    const size_t ox = take((size_t)T * D * 4);
+    const size_t oqkv = take((size_t)T * ctx->qkv_dim * 4);
+    const size_t oq = take((size_t)T * ctx->attn_dim * 4);
+    const size_t ologits = take((size_t)c.max_batch * V * 4);
+    const size_t opart = take((size_t)c.max_batch * Hq * ctx->max_splits * (d + 2) * 4);
+    const size_t oh = take((size_t)T * D * 2);
+    const size_t oattn = take((size_t)T * ctx->attn_dim * 2);
+    const size_t oact = take((size_t)T * I * 2);
+    const size_t otok = take((size_t)T * 4);
+    const size_t oiota = take((size_t)c.max_batch * 4);
+    const size_t orows = take((size_t)T * 4);
+    const size_t oerr = take(64);
+    const size_t otiles = take((size_t)ctx->max_tiles * 16);
+    const size_t ohid = c.debug_hidden ? take((size_t)c.n_layers * T * D * 4) : 0;
+    if (cudaMalloc(&ctx->wsbuf, off) != cudaSuccess) {
+        free_ctx(ctx);
+        return fail(QW_ENOMEM, "workspace allocation failed");
+    }
+    uint8_t* W = ctx->wsbuf;
+    ctx->x = (float*)(W + ox);
+    ctx->qkv = (float*)(W + oqkv);
+    ctx->q = (float*)(W + oq);
+    ctx->logits = (float*)(W + ologits);
+    ctx->part = (float*)(W + opart);
+    ctx->h = (uint16_t*)(W + oh);
+    ctx->attn = (uint16_t*)(W + oattn);
+    ctx->act = (uint16_t*)(W + oact);
+    ctx->tok_seq = (int*)(W + otok);
+    ctx->iota = (int*)(W + oiota);
+    ctx->rows_last = (int*)(W + orows);
+    ctx->err = (int*)(W + oerr);
+    ctx->tiles = (int4*)(W + otiles);
+    ctx->hidden = c.debug_hidden ? (float*)(W + ohid) : nullptr;
+    {
+        std::vector<int> iota(c.max_batch);
+        for (int i = 0; i < c.max_batch; ++i) iota[i] = i;
+        QW_INIT_CUDA(cudaMemcpy(ctx->iota, iota.data(), iota.size() * 4, cudaMemcpyHostToDevice));
+        QW_INIT_CUDA(cudaMemset(ctx->err, 0, 64));
+    }
+    QW_INIT_CUDA(cudaDeviceSynchronize());
+#undef QW_INIT_CUDA
+    *out = ctx;
+    return QW_OK;
+}
+
+int qw_destroy(qw_ctx* ctx) {
+    if (!ctx) return fail(QW_EINVAL, "null context");
+    cudaDeviceSynchronize();
+    free_ctx(ctx);
+    return QW_OK;
+}
+
+int qw_kv_create(qw_ctx* ctx, int32_t n_pages, qw_kv** out) {
+    if (!ctx || !out || n_pages < 1) return fail(QW_EINVAL, "qw_kv_create: bad argument");
+    *out = nullptr;
+    const int64_t page_elems = (int64_t)2 * ctx->cfg.n_kv_heads * QW_PAGE_SIZE * QW_HEAD_DIM;
+    const size_t bytes = (size_t)ctx->cfg.n_layers * n_pages * page_elems * 2;
+    size_t free_b = 0, total_b = 0;
+    QW_CUDA(cudaMemGetInfo(&free_b, &total_b));
+    if (bytes + ((size_t)256 << 20) > free_b) return fail(QW_EKVFULL, "KV pool larger than free device memory");
+    void* p = nullptr;
+    if (cudaMalloc(&p, bytes) != cudaSuccess) return fail(QW_ENOMEM, "KV pool allocation failed");
+    qw_kv* kv = new qw_kv{ctx, (uint16_t*)p, n_pages, page_elems, (int64_t)n_pages * page_elems};
+    *out = kv;
+    return QW_OK;
+}
+
+int qw_kv_destroy(qw_kv* kv) {
+    if (!kv) return fail(QW_EINVAL, "null kv");
+    cudaDeviceSynchronize();
+    cudaFree(kv->base);
+    delete kv;
+    return QW_OK;
+}
+
+int qw_kv_layout(const qw_kv* kv, void** base, int64_t* layer_stride, int64_t* page_stride, int32_t* n_pages) {
+    if (!kv) return fail(QW_EINVAL, "null kv");
+    if (base) *base = kv->base;
+    if (layer_stride) *layer_stride = kv->layer_elems * 2;
+    if (page_stride) *page_stride = kv->page_elems * 2;
+    if (n_pages) *n_pages = kv->n_pages;
+    return QW_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- the layer stack
+// mode 0: prefill attention over `tiles`; mode 1: split-KV decode attention.
+static int run_layers(qw_ctx* ctx, int n, const int* ids, const int* positions, const int* tok_seq, qw_kv* kv,
+                      const int* bt, int bt_stride, int mode, int n_tiles, cudaStream_t st) {
+    const qw_config& c = ctx->cfg;
+    const int D = c.hidden, Hq = c.n_heads, Hkv = c.n_kv_heads, I = c.intermediate;
+    QW_TRY(launch_embed(ids, n, ctx->E, c.vocab, D, ctx->x, ctx->err, st), "embed launch");
+    for (int l = 0; l < c.n_layers; ++l) {
+        const LayerW& Lw = ctx->L[l];
+        KvView kvv{kv->base + (int64_t)l * kv->layer_elems, kv->page_elems, kv->n_pages, bt, bt_stride};
+        QW_TRY(launch_rmsnorm_bf16(ctx->x, nullptr, n, D, Lw.in_norm, c.rms_eps, ctx->h, st), "rmsnorm launch");
+        GemmEpilogue e{ctx->qkv, nullptr, ctx->qkv_dim, ctx->err};
+        QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_qkv, 256, n, ctx->qkv_dim, D, EPI_STORE_F32, e, st), "qkv gemm");
+        QW_TRY(launch_qkv_post(ctx->qkv, n, positions, tok_seq, Hq, Hkv, Lw.q_norm, Lw.k_norm, ctx->inv_freq,
+                               c.rms_eps, ctx->q, kvv, ctx->err, st),
+               "qk-norm/rope/kv-write launch");
+        if (mode == 0)
+            QW_TRY(launch_attn_prefill(ctx->q, positions, ctx->tiles, n_tiles, Hq, Hkv, kvv, ctx->attn, ctx->err, st),
+                   "prefill attention launch");
+        else
+            QW_TRY(launch_attn_decode(ctx->q, positions, n, Hq, Hkv, kvv, ctx->part, ctx->max_splits, ctx->attn,
+                                      ctx->err, ctx->n_sm, st),
+                   "decode attention launch");
+        e = GemmEpilogue{ctx->x, nullptr, D, ctx->err};
+        QW_TRY(gemm_bf16(ctx->attn, ctx->attn_dim, Lw.tm_o, 128, n, D, ctx->attn_dim, EPI_RESID_ADD, e, st), "o_proj gemm");
+        QW_TRY(launch_rmsnorm_bf16(ctx->x, nullptr, n, D, Lw.post_norm, c.rms_eps, ctx->h, st), "rmsnorm launch");
+        e = GemmEpilogue{nullptr, ctx->act, I, ctx->err};
+        QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_gu, 256, n, 2 * I, D, EPI_SWIGLU, e, st), "gate/up gemm");
+        e = GemmEpilogue{ctx->x, nullptr, D, ctx->err};
+        QW_TRY(gemm_bf16(ctx->act, I, Lw.tm_d, 128, n, D, I, EPI_RESID_ADD, e, st), "down gemm");
+        if (ctx->hidden)
+            QW_CUDA(cudaMemcpyAsync(ctx->hidden + (size_t)l * ctx->max_rows * D, ctx->x, (size_t)n * D * 4,
+                                    cudaMemcpyDeviceToDevice, st));
+    }
+    return QW_OK;
+}
+
+// final RMSNorm of the selected rows and the tied LM head (Step 8)
+static int lm_head(qw_ctx* ctx, const int* rows, int n, float* out, cudaStream_t st) {
+    const qw_config& c = ctx->cfg;
+    QW_TRY(launch_rmsnorm_bf16(ctx->x, rows, n, c.hidden, ctx->final_norm, c.rms_eps, ctx->h, st), "final norm");
+    GemmEpilogue e{out, nullptr, c.vocab, ctx->err};
+    QW_TRY(gemm_bf16(ctx->h, c.hidden, ctx->tm_E, 256, n, c.vocab, c.hidden, EPI_STORE_F32, e, st), "lm head gemm");
+    return QW_OK;
+}
+
+extern "C" {
+
+int qw_prefill(qw_ctx* ctx, const int32_t* ids, const int32_t* positions, const int32_t* cu, int32_t n_seqs,
+               qw_kv* kv, const int32_t* bt, int32_t bt_stride, float* last_logits, void* stream) {
+    if (!ctx || !ids || !positions || !cu || !kv || !bt) return fail(QW_EINVAL, "qw_prefill: null argument");
+    if (kv->ctx != ctx) return fail(QW_EINVAL, "qw_prefill: kv pool belongs to another context");
+    if (n_seqs < 1 || bt_stride < 1) return fail(QW_EINVAL, "qw_prefill: n_seqs and bt_stride must be >= 1");
+    if (cu[0] != 0) return fail(QW_EINVAL, "qw_prefill: cu_seqlens[0] must be 0");
+    for (int s = 0; s < n_seqs; ++s)
+        if (cu[s + 1] <= cu[s]) return fail(QW_EINVAL, "qw_prefill: every sequence needs at least one token");
+    const int n = cu[n_seqs];
+    if (n > ctx->cfg.max_tokens) return fail(QW_EINVAL, "qw_prefill: more tokens than max_tokens");
+    if (!last_logits && n_seqs > ctx->cfg.max_batch)
+        return fail(QW_EINVAL, "qw_prefill: more than max_batch sequences need a caller logits buffer");
+    cudaStream_t st = (cudaStream_t)stream;
+    std::vector<int> tok_seq(n), last(n_seqs);
+    std::vector<int4> tiles;
+    for (int s = 0; s < n_seqs; ++s) {
+        const int len = cu[s + 1] - cu[s];
+        for (int t = cu[s]; t < cu[s + 1]; ++t) tok_seq[t] = s;
+        last[s] = cu[s + 1] - 1;
+        for (int q0 = 0; q0 < len; q0 += 64) tiles.push_back(make_int4(s, cu[s] + q0, std::min(64, len - q0), q0));
+    }
+    // longest causal rows first, so the heaviest tiles start in the first wave
+    std::stable_sort(tiles.begin(), tiles.end(), [](const int4& a, const int4& b) { return a.w > b.w; });
+    if ((int)tiles.size() > ctx->max_tiles) return fail(QW_EINVAL, "qw_prefill: too many query tiles");
+    QW_CUDA(cudaMemcpyAsync(ctx->tok_seq, tok_seq.data(), n * 4, cudaMemcpyHostToDevice, st));
+    QW_CUDA(cudaMemcpyAsync(ctx->rows_last, last.data(), n_seqs * 4, cudaMemcpyHostToDevice, st));
+    QW_CUDA(cudaMemcpyAsync(ctx->tiles, tiles.data(), tiles.size() * 16, cudaMemcpyHostToDevice, st));
+    int rc = run_layers(ctx, n, ids, positions, ctx->tok_seq, kv, bt, bt_stride, 0, (int)tiles.size(), st);
+    if (rc) return rc;
+    ctx->last_rows = n;
+    float* out = last_logits ? last_logits : ctx->logits;
+    if ((rc = lm_head(ctx, ctx->rows_last, n_seqs, out, st))) return rc;
+    ctx->logits_rows = last_logits ? 0 : n_seqs;
+    return QW_OK;
+}
+
+int qw_decode_step(qw_ctx* ctx, const int32_t* tokens, const int32_t* positions, int32_t batch, qw_kv* kv,
+                   const int32_t* bt, int32_t bt_stride, float* logits, void* stream) {
+    if (!ctx || !tokens || !positions || !kv || !bt) return fail(QW_EINVAL, "qw_decode_step: null argument");
+    if (kv->ctx != ctx) return fail(QW_EINVAL, "qw_decode_step: kv pool belongs to another context");
+    if (batch < 1 || batch > ctx->cfg.max_batch) return fail(QW_EINVAL, "qw_decode_step: batch out of [1, max_batch]");
+    if (bt_stride < 1) return fail(QW_EINVAL, "qw_decode_step: bt_stride must be >= 1");
+    cudaStream_t st = (cudaStream_t)stream;
+    float* out = logits ? logits : ctx->logits;
+    const bool fused = ctx->decode_path == 2 || (ctx->decode_path == 0 && fused_supported(ctx->fused, batch));
+    int rc;
+    if (fused && ctx->fused) {
+        rc = fused_decode(ctx->fused, tokens, positions, batch, kv->base, kv->layer_elems, kv->page_elems,
+                          kv->n_pages, bt, bt_stride, out, ctx->err, st);
+        if (rc) return fail(rc, "fused decode launch failed");
+        ctx->last_rows = batch;
+    } else {
+        if ((rc = run_layers(ctx, batch, tokens, positions, ctx->iota, kv, bt, bt_stride, 1, 0, st))) return rc;
+        ctx->last_rows = batch;
+        if ((rc = lm_head(ctx, nullptr, batch, out, st))) return rc;
+    }
+    ctx->logits_rows = logits ? 0 : batch;
+    return QW_OK;
+}
+
+int qw_sample(qw_ctx* ctx, const float* logits, int32_t batch, const qw_sample_params* params, uint64_t rng_counter,
+              int32_t* out_ids, void* stream) {
+    if (!ctx || !params || !out_ids) return fail(QW_EINVAL, "qw_sample: null argument");
+    if (batch < 1 || batch > ctx->cfg.max_batch) return fail(QW_EINVAL, "qw_sample: batch out of [1, max_batch]");
+    if (!logits) {
+        if (ctx->logits_rows < batch) return fail(QW_EINVAL, "qw_sample: the context holds fewer logits rows than batch");
+        logits = ctx->logits;
+    }
+    QW_TRY(launch_sample(logits, batch, ctx->cfg.vocab, params, rng_counter, out_ids, ctx->err, (cudaStream_t)stream),
+           "sample launch");
+    return QW_OK;
+}
+
+int qw_check(qw_ctx* ctx, void* stream) {
+    if (!ctx) return fail(QW_EINVAL, "null context");
+    QW_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+    int h = 0;
+    QW_CUDA(cudaMemcpy(&h, ctx->err, 4, cudaMemcpyDeviceToHost));
+    if (h) {
+        QW_CUDA(cudaMemset(ctx->err, 0, 4));
+        return fail(h, h == QW_ERANGE ? "device: token id, position or page id out of range"
+                       : h == QW_ETIMEOUT ? "device: a bounded wait timed out"
+                                          : "device: invalid sampling parameters or too many tied logits");
+    }
+    return QW_OK;
+}
+
+int qw_debug_hidden(qw_ctx* ctx, int32_t layer, float* out, int32_t n_rows, void* stream) {
+    if (!ctx || !out) return fail(QW_EINVAL, "null argument");
+    if (!ctx->hidden) return fail(QW_EINVAL, "context was created without debug_hidden");
+    if (layer < 0 || layer >= ctx->cfg.n_layers) return fail(QW_EINVAL, "layer out of range");
+    if (n_rows < 1 || n_rows > ctx->last_rows) return fail(QW_EINVAL, "n_rows exceeds the rows of the last call");
+    QW_CUDA(cudaMemcpyAsync(out, ctx->hidden + (size_t)layer * ctx->max_rows * ctx->cfg.hidden,
+                            (size_t)n_rows * ctx->cfg.hidden * 4, cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
+    return QW_OK;
+}
+
+int qw_debug_gemm(const uint16_t* A, const uint16_t* B, void* C, int32_t M, int32_t N, int32_t K, int32_t epi,
+                  int32_t bn, void* stream) {
+    if (!A || !B || !C || M < 1 || N < 32 || K < 64 || K % 64 || N % 32 || epi < 0 || epi > 2 ||
+        (bn != 128 && bn != 256))
+        return fail(QW_EINVAL, "qw_debug_gemm: bad argument");
+    CUtensorMap tb;
+    QW_TRY(make_tmap_bf16(&tb, B, (uint64_t)K, (uint64_t)N, (uint64_t)K * 2, 64, (uint32_t)bn), "tensor map for B");
+    GemmEpilogue e{epi == 2 ? nullptr : (float*)C, epi == 2 ? (uint16_t*)C : nullptr, epi == 2 ? N / 2 : N, nullptr};
+    QW_TRY(gemm_bf16(A, K, tb, bn, M, N, K, epi, e, (cudaStream_t)stream), "gemm launch");
+    return QW_OK;
+}
+
+uint64_t qw_kernel_launches(void) { return (uint64_t)launches_so_far(); }
+
+int qw_set_decode_path(qw_ctx* ctx, int32_t path) {
+    if (!ctx || path < 0 || path > 2) return fail(QW_EINVAL, "qw_set_decode_path: bad argument");
+    if (path == 2 && !ctx->fused) return fail(QW_EINVAL, "the fused decode path is not available for this configuration");
+    ctx->decode_path = path;
+    return QW_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,55 @@
+// Declarations shared by the translation units of libqwdecode (not part of the C ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qwdecode.h"
+
+namespace qw {
+
+// Counts every kernel launch the library makes (read by qw_kernel_launches).
+void count_launches(int n);
+
+enum { EPI_STORE_F32 = 0, EPI_RESID_ADD = 1, EPI_SWIGLU = 2 };
+
+struct GemmEpilogue {
+    float* out;      // EPI_STORE_F32: out[m][n]; EPI_RESID_ADD: out[m][n] += acc
+    uint16_t* act;   // EPI_SWIGLU: act[m][n/2] = bf16(silu(acc[2j]) * acc[2j+1])
+    int ldo;         // row stride (elements) of out / act
+    int* err;        // device error word
+};
+
+// Tensor map of a row-major bf16 matrix [rows][inner] with a (box_rows x box_inner)
+// box and 128-byte swizzling (box_inner * 2 must be 128).
+int make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_bytes,
+                   uint32_t box_inner, uint32_t box_rows);
+
+// C[M][N] (epilogue) = A[M][K] . B[N][K]^T; tmB must have box {64, bn}.
+int gemm_bf16(const void* A, int lda_elems, const CUtensorMap& tmB, int bn, int M, int N, int K, int epi,
+              const GemmEpilogue& ep, cudaStream_t st);
+
+// ---------------------------------------------------------------- per-op kernels
+struct KvView {
+    uint16_t* base;        // this layer's pages: [n_pages][2][n_kv][16][128]
+    int64_t page_stride;   // elements per page (2 * n_kv * 16 * 128)
+    int n_pages;
+    const int* block_tables;
+    int bt_stride;
+};
+
+int launch_embed(const int* ids, int n, const uint16_t* E, int vocab, int D, float* x, int* err, cudaStream_t st);
+int launch_rmsnorm_bf16(const float* x, const int* rows /*nullable*/, int n, int D, const float* w, float eps,
+                        uint16_t* out, cudaStream_t st);
+int launch_qkv_post(const float* qkv, int n_tok, const int* positions, const int* tok_seq, int Hq, int Hkv,
+                    const float* q_norm, const float* k_norm, const float* inv_freq, float eps, float* q_out,
+                    const KvView& kv, int* err, cudaStream_t st);
+int launch_attn_prefill(const float* q, const int* positions, const int4* tiles, int n_tiles, int Hq, int Hkv,
+                        const KvView& kv, uint16_t* out, int* err, cudaStream_t st);
+int launch_attn_decode(const float* q, const int* positions, int batch, int Hq, int Hkv, const KvView& kv,
+                       float* part, int max_splits, uint16_t* out, int* err, int n_sm, cudaStream_t st);
+int launch_sample(const float* logits, int batch, int vocab, const qw_sample_params* params, uint64_t rng_counter,
+                  int32_t* out_ids, int* err, cudaStream_t st);
+int launch_bf16_to_f32(const uint16_t* src, float* dst, int n, cudaStream_t st);
+
+}  // namespace qw

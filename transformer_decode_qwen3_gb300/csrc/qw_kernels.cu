@@ -1,0 +1,762 @@
+// Per-op kernels of the decoder pass (everything except the tensor-core GEMM).
+// Step numbers refer to "Inside an LLM: Pure Python Inference for Qwen3-0.6B on MLX".
+#include <float.h>
+
+#include "qw_common.cuh"
+#include "qw_internal.h"
+
+namespace qw {
+
+static unsigned long long g_launches = 0;
+void count_launches(int n) { __atomic_fetch_add(&g_launches, (unsigned long long)n, __ATOMIC_RELAXED); }
+unsigned long long launches_so_far() { return __atomic_load_n(&g_launches, __ATOMIC_RELAXED); }
+
+static inline int check_launch() {
+    count_launches(1);
+    return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ECUDA;
+}
+
+// ---------------------------------------------------------------- Step 2: embedding
+// x[t][:] = E[ids[t]][:] widened to fp32.  An id outside [0, vocab) gives a zero row
+// and QW_ERANGE in the error word.
+__global__ void embed_kernel(const int* __restrict__ ids, const uint16_t* __restrict__ E, int vocab, int D,
+                             float* __restrict__ x, int* err) {
+    const int t = blockIdx.x;
+    const int id = ids[t];
+    const bool bad = id < 0 || id >= vocab;
+    if (bad && threadIdx.x == 0) set_error(err, QW_ERANGE);
+    float* xr = x + (size_t)t * D;
+    for (int c = threadIdx.x * 8; c < D; c += blockDim.x * 8) {
+        uint4 v = bad ? make_uint4(0, 0, 0, 0) : *(const uint4*)(E + (size_t)id * D + c);
+        float4 lo = make_float4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y));
+        float4 hi = make_float4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w));
+        *(float4*)(xr + c) = lo;
+        *(float4*)(xr + c + 4) = hi;
+    }
+}
+
+int launch_embed(const int* ids, int n, const uint16_t* E, int vocab, int D, float* x, int* err, cudaStream_t st) {
+    if (n <= 0) return QW_OK;
+    embed_kernel<<<n, 128, 0, st>>>(ids, E, vocab, D, x, err);
+    return check_launch();
+}
+
+// ---------------------------------------------------------------- Step 3: RMSNorm
+// out[r] = bf16(x[src] / sqrt(mean(x[src]^2) + eps) * w), one warp per row.
+__global__ void rmsnorm_bf16_kernel(const float* __restrict__ x, const int* __restrict__ rows, int n, int D,
+                                    const float* __restrict__ w, float eps, uint16_t* __restrict__ out) {
+    const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (r >= n) return;
+    const int src = rows ? rows[r] : r;
+    const float* xr = x + (size_t)src * D;
+    float ss = 0.f;
+    for (int c = lane * 4; c < D; c += 128) {
+        float4 v = *(const float4*)(xr + c);
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+    ss = warp_sum(ss);
+    const float s = 1.0f / sqrtf(ss / (float)D + eps);
+    for (int c = lane * 4; c < D; c += 128) {
+        float4 v = *(const float4*)(xr + c);
+        float4 wv = *(const float4*)(w + c);
+        uint2 o = make_uint2(pack_bf16x2(v.x * s * wv.x, v.y * s * wv.y), pack_bf16x2(v.z * s * wv.z, v.w * s * wv.w));
+        *(uint2*)(out + (size_t)r * D + c) = o;
+    }
+}
+
+int launch_rmsnorm_bf16(const float* x, const int* rows, int n, int D, const float* w, float eps, uint16_t* out,
+                        cudaStream_t st) {
+    if (n <= 0) return QW_OK;
+    rmsnorm_bf16_kernel<<<(n + 7) / 8, 256, 0, st>>>(x, rows, n, D, w, eps, out);
+    return check_launch();
+}
+
+// ------------------------------------- Step 5: QK-Norm, Step 4: RoPE, KV cache append
+// One warp per (token, head) of the fused q|k|v projection output.  Lane l holds
+// dims l, l+32, l+64, l+96, so both halves of every RoPE pair (i, i+64) sit in one
+// lane.  q goes to q_out (fp32); k and v go, as bf16, to slot pos % 16 of page
+// block_tables[seq][pos / 16].
+__global__ void qkv_post_kernel(const float* __restrict__ qkv, const int* __restrict__ positions,
+                                const int* __restrict__ tok_seq, int Hq, int Hkv, const float* __restrict__ q_norm,
+                                const float* __restrict__ k_norm, const float* __restrict__ inv_freq, float eps,
+                                float* __restrict__ q_out, KvView kv, int* err) {
+    const int t = blockIdx.x;
+    const int hh = blockIdx.y * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    const int nh = Hq + 2 * Hkv;
+    if (hh >= nh) return;
+    const float* row = qkv + ((size_t)t * nh + hh) * QW_HEAD_DIM;
+    float y[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) y[i] = row[lane + 32 * i];
+    const int pos = positions[t];
+    if (hh < Hq + Hkv) {
+        float ss = warp_sum(y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3]);
+        const float s = 1.0f / sqrtf(ss / (float)QW_HEAD_DIM + eps);
+        const float* w = hh < Hq ? q_norm : k_norm;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) y[i] = y[i] * s * w[lane + 32 * i];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {  // pairs (lane + 32j, lane + 32j + 64)
+            const float ang = __fmul_rn((float)pos, inv_freq[lane + 32 * j]);
+            float sn, cs;
+            sincosf(ang, &sn, &cs);
+            const float a = y[j], b = y[j + 2];
+            y[j] = a * cs - b * sn;
+            y[j + 2] = a * sn + b * cs;
+        }
+    }
+    if (hh < Hq) {
+        float* dst = q_out + ((size_t)t * Hq + hh) * QW_HEAD_DIM;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = y[i];
+        return;
+    }
+    const int seq = tok_seq[t];
+    if (pos < 0 || pos >= kv.bt_stride * QW_PAGE_SIZE) {
+        if (lane == 0) set_error(err, QW_ERANGE);
+        return;
+    }
+    const int page = kv.block_tables[(size_t)seq * kv.bt_stride + pos / QW_PAGE_SIZE];
+    if (page < 0 || page >= kv.n_pages) {
+        if (lane == 0) set_error(err, QW_ERANGE);
+        return;
+    }
+    const int which = hh < Hq + Hkv ? 0 : 1;
+    const int g = (hh - Hq) - which * Hkv;
+    uint16_t* dst = kv.base + (size_t)page * kv.page_stride + ((size_t)(which * Hkv + g) * QW_PAGE_SIZE +
+                                                               (pos % QW_PAGE_SIZE)) * QW_HEAD_DIM;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = f2bf(y[i]);
+}
+
+int launch_qkv_post(const float* qkv, int n_tok, const int* positions, const int* tok_seq, int Hq, int Hkv,
+                    const float* q_norm, const float* k_norm, const float* inv_freq, float eps, float* q_out,
+                    const KvView& kv, int* err, cudaStream_t st) {
+    if (n_tok <= 0) return QW_OK;
+    dim3 grid(n_tok, (Hq + 2 * Hkv + 3) / 4);
+    qkv_post_kernel<<<grid, 128, 0, st>>>(qkv, positions, tok_seq, Hq, Hkv, q_norm, k_norm, inv_freq, eps, q_out, kv,
+                                          err);
+    return check_launch();
+}
+
+// ---------------------------------------------------------------- mma.sync helpers
+QW_DEV void ldsm_x4(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+QW_DEV void ldsm_x4_t(uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3, uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+QW_DEV void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+QW_DEV void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+QW_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+QW_DEV void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---------------------------------------------- Step 5: causal attention over the cache
+// Flash-style prefill attention.  A CTA takes one tile of up to 64 query rows of
+// one sequence and one KV head; warps 0-3 serve query head 2g, warps 4-7 query
+// head 2g+1 (the grouped-query sharing of Step 5), 16 rows each.  Keys and values
+// stream from the paged cache in tiles of 64 positions (double-buffered cp.async,
+// XOR-swizzled rows), S = QK^T and PV run on mma.sync m16n8k16 with an online
+// softmax in fp32.  Key position j is visible to a query at position p iff j <= p.
+constexpr int AP_ROWS = 64;
+constexpr int AP_KEYS = 64;
+constexpr int AP_SMEM = 2 * 2 * AP_KEYS * QW_HEAD_DIM * 2;  // 2 buffers x (K, V) x 64 x 128 bf16
+
+__global__ void __launch_bounds__(256) attn_prefill_kernel(const float* __restrict__ q,
+                                                           const int* __restrict__ positions,
+                                                           const int4* __restrict__ tiles, int Hq, int Hkv,
+                                                           KvView kv, uint16_t* __restrict__ out, float scale_log2,
+                                                           int* err) {
+    extern __shared__ __align__(128) uint8_t sm[];
+    const int4 tile = tiles[blockIdx.x];
+    const int seq = tile.x, row0 = tile.y, nrows = tile.z;
+    const int g = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gq = lane >> 2, tq = lane & 3;
+    const int h = g * 2 + (warp >> 2);
+    const int r0 = (warp & 3) * 16;
+    const int ra = r0 + gq, rb = ra + 8;
+    const int pa = ra < nrows ? positions[row0 + ra] : -1;
+    const int pb = rb < nrows ? positions[row0 + rb] : -1;
+    const int pmax = positions[row0 + nrows - 1];
+
+    uint32_t qf[8][4];
+    {
+        const float* qa = q + ((size_t)(row0 + ra) * Hq + h) * QW_HEAD_DIM;
+        const float* qb = q + ((size_t)(row0 + rb) * Hq + h) * QW_HEAD_DIM;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const int d0 = kk * 16 + 2 * tq;
+            qf[kk][0] = pa >= 0 ? pack_bf16x2(qa[d0], qa[d0 + 1]) : 0u;
+            qf[kk][1] = pb >= 0 ? pack_bf16x2(qb[d0], qb[d0 + 1]) : 0u;
+            qf[kk][2] = pa >= 0 ? pack_bf16x2(qa[d0 + 8], qa[d0 + 9]) : 0u;
+            qf[kk][3] = pb >= 0 ? pack_bf16x2(qb[d0 + 8], qb[d0 + 9]) : 0u;
+        }
+    }
+    float o[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+
+    const int nkt = pmax / AP_KEYS + 1;
+    const int64_t head_off = (int64_t)g * QW_PAGE_SIZE * QW_HEAD_DIM;
+    const int64_t v_off = (int64_t)Hkv * QW_PAGE_SIZE * QW_HEAD_DIM;
+    const int* bt = kv.block_tables + (size_t)seq * kv.bt_stride;
+
+    auto load_tile = [&](int kt, int buf) {
+        uint8_t* sK = sm + buf * (2 * AP_KEYS * 256);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int idx = threadIdx.x + i * 256;
+            const int which = idx >> 10, r = (idx >> 4) & 63, c = idx & 15;
+            const int pos = kt * AP_KEYS + r;
+            const uint16_t* src = kv.base;
+            int bytes = 0;
+            if (pos <= pmax) {
+                const int pidx = pos / QW_PAGE_SIZE;
+                const int page = pidx < kv.bt_stride ? bt[pidx] : -1;
+                if (page >= 0 && page < kv.n_pages) {
+                    src = kv.base + (int64_t)page * kv.page_stride + which * v_off + head_off +
+                          (pos % QW_PAGE_SIZE) * QW_HEAD_DIM + c * 8;
+                    bytes = 16;
+                } else if (c == 0) {
+                    set_error(err, QW_ERANGE);
+                }
+            }
+            uint8_t* dst = sK + which * (AP_KEYS * 256) + r * 256 + ((c ^ (r & 7)) << 4);
+            cp_async16(smem_u32(dst), src, bytes);
+        }
+        cp_async_commit();
+    };
+
+    load_tile(0, 0);
+    for (int kt = 0; kt < nkt; ++kt) {
+        if (kt + 1 < nkt)
+            load_tile(kt + 1, (kt + 1) & 1);
+        else
+            cp_async_commit();
+        cp_async_wait<1>();
+        __syncthreads();
+        const uint8_t* sK = sm + (kt & 1) * (2 * AP_KEYS * 256);
+        const uint8_t* sV = sK + AP_KEYS * 256;
+
+        float s[8][4];
+#pragma unroll
+        for (int nb = 0; nb < 8; ++nb) {
+            s[nb][0] = s[nb][1] = s[nb][2] = s[nb][3] = 0.f;
+#pragma unroll
+            for (int kk2 = 0; kk2 < 4; ++kk2) {
+                const int key = nb * 8 + (lane & 7);
+                const int ch = kk2 * 4 + (lane >> 3);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(b0, b1, b2, b3, smem_u32(sK + key * 256 + ((ch ^ (key & 7)) << 4)));
+                mma16816(s[nb], qf[2 * kk2], b0, b1);
+                mma16816(s[nb], qf[2 * kk2 + 1], b2, b3);
+            }
+        }
+        const int kv0 = kt * AP_KEYS;
+        float mx_a = -INFINITY, mx_b = -INFINITY;
+#pragma unroll
+        for (int nb = 0; nb < 8; ++nb) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int kp = kv0 + nb * 8 + 2 * tq + j;
+                s[nb][j] = kp <= pa ? s[nb][j] * scale_log2 : -INFINITY;
+                s[nb][2 + j] = kp <= pb ? s[nb][2 + j] * scale_log2 : -INFINITY;
+                mx_a = fmaxf(mx_a, s[nb][j]);
+                mx_b = fmaxf(mx_b, s[nb][2 + j]);
+            }
+        }
+        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+        const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+        const float al_a = mn_a == -INFINITY ? 1.f : exp2f(m_a - mn_a);
+        const float al_b = mn_b == -INFINITY ? 1.f : exp2f(m_b - mn_b);
+        m_a = mn_a;
+        m_b = mn_b;
+        float sum_a = 0.f, sum_b = 0.f;
+#pragma unroll
+        for (int nb = 0; nb < 8; ++nb) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                s[nb][j] = mn_a == -INFINITY ? 0.f : exp2f(s[nb][j] - mn_a);
+                s[nb][2 + j] = mn_b == -INFINITY ? 0.f : exp2f(s[nb][2 + j] - mn_b);
+                sum_a += s[nb][j];
+                sum_b += s[nb][2 + j];
+            }
+        }
+        l_a = l_a * al_a + sum_a;
+        l_b = l_b * al_b + sum_b;
+#pragma unroll
+        for (int nd = 0; nd < 16; ++nd) {
+            o[nd][0] *= al_a;
+            o[nd][1] *= al_a;
+            o[nd][2] *= al_b;
+            o[nd][3] *= al_b;
+        }
+#pragma unroll
+        for (int kk2 = 0; kk2 < 4; ++kk2) {
+            uint32_t a[4];
+            a[0] = pack_bf16x2(s[2 * kk2][0], s[2 * kk2][1]);
+            a[1] = pack_bf16x2(s[2 * kk2][2], s[2 * kk2][3]);
+            a[2] = pack_bf16x2(s[2 * kk2 + 1][0], s[2 * kk2 + 1][1]);
+            a[3] = pack_bf16x2(s[2 * kk2 + 1][2], s[2 * kk2 + 1][3]);
+#pragma unroll
+            for (int nd = 0; nd < 16; nd += 2) {
+                const int mi = lane >> 3;
+                const int key = kk2 * 16 + (mi & 1) * 8 + (lane & 7);
+                const int ch = nd + (mi >> 1);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(b0, b1, b2, b3, smem_u32(sV + key * 256 + ((ch ^ (key & 7)) << 4)));
+                mma16816(o[nd], a, b0, b1);
+                mma16816(o[nd + 1], a, b2, b3);
+            }
+        }
+        __syncthreads();
+    }
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+    const float ia = l_a > 0.f ? 1.f / l_a : 0.f, ib = l_b > 0.f ? 1.f / l_b : 0.f;
+    const size_t ld = (size_t)Hq * QW_HEAD_DIM;
+#pragma unroll
+    for (int nd = 0; nd < 16; ++nd) {
+        const int d = h * QW_HEAD_DIM + nd * 8 + 2 * tq;
+        if (ra < nrows) *(uint32_t*)(out + (size_t)(row0 + ra) * ld + d) = pack_bf16x2(o[nd][0] * ia, o[nd][1] * ia);
+        if (rb < nrows) *(uint32_t*)(out + (size_t)(row0 + rb) * ld + d) = pack_bf16x2(o[nd][2] * ib, o[nd][3] * ib);
+    }
+}
+
+int launch_attn_prefill(const float* q, const int* positions, const int4* tiles, int n_tiles, int Hq, int Hkv,
+                        const KvView& kv, uint16_t* out, int* err, cudaStream_t st) {
+    if (n_tiles <= 0) return QW_OK;
+    if (Hq != 2 * Hkv) return QW_EINVAL;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(attn_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, AP_SMEM) !=
+            cudaSuccess)
+            return QW_ECUDA;
+        attr = true;
+    }
+    const float scale_log2 = 1.4426950408889634f / sqrtf((float)QW_HEAD_DIM);
+    attn_prefill_kernel<<<dim3(n_tiles, Hkv), 256, AP_SMEM, st>>>(q, positions, tiles, Hq, Hkv, kv, out,
+                                                                  scale_log2, err);
+    return check_launch();
+}
+
+// ---------------------------------------------- Step 5: decode attention, split over the cache
+// One CTA per (split of the cached positions, KV head, sequence): both query heads
+// of the group against up to chunk_pages pages.  Each warp walks pages; lane l
+// covers keys (l >> 4) + 2i of the page and dims 8 (l & 15) .. +8.  The CTA writes
+// an unnormalised partial (o[128], running max m in log2 units, sum l) per query
+// head; attn_combine_kernel merges the splits.
+constexpr int AD_WARPS = 4;
+constexpr int AD_PART = QW_HEAD_DIM + 2;
+
+QW_DEV uint4 ldg_stream(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+QW_DEV float dot8(const float (&q)[8], uint4 k) {
+    return q[0] * bf16_lo(k.x) + q[1] * bf16_hi(k.x) + q[2] * bf16_lo(k.y) + q[3] * bf16_hi(k.y) +
+           q[4] * bf16_lo(k.z) + q[5] * bf16_hi(k.z) + q[6] * bf16_lo(k.w) + q[7] * bf16_hi(k.w);
+}
+
+__global__ void __launch_bounds__(AD_WARPS * 32) attn_decode_kernel(const float* __restrict__ q,
+                                                                    const int* __restrict__ positions, int Hq,
+                                                                    int Hkv, KvView kv, int chunk_pages,
+                                                                    int n_splits, float* __restrict__ part,
+                                                                    float scale_log2, int* err) {
+    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int half = lane >> 4, dc = lane & 15;
+    const int pos = positions[b];
+    int L = pos + 1;
+    if (pos < 0 || pos >= kv.bt_stride * QW_PAGE_SIZE) {
+        if (threadIdx.x == 0 && split == 0 && g == 0) set_error(err, QW_ERANGE);
+        L = 0;
+    }
+    const int np = (L + QW_PAGE_SIZE - 1) / QW_PAGE_SIZE;
+    const int p_lo = split * chunk_pages, p_hi = min(np, p_lo + chunk_pages);
+    float* pa = part + (((size_t)b * Hq + 2 * g) * n_splits + split) * AD_PART;
+    float* pb = pa + (size_t)n_splits * AD_PART;
+    if (p_lo >= p_hi) {
+        if (threadIdx.x == 0) {
+            pa[QW_HEAD_DIM] = -INFINITY;
+            pa[QW_HEAD_DIM + 1] = 0.f;
+            pb[QW_HEAD_DIM] = -INFINITY;
+            pb[QW_HEAD_DIM + 1] = 0.f;
+        }
+        return;
+    }
+    float qa[8], qb[8];
+    {
+        const float* q0 = q + ((size_t)b * Hq + 2 * g) * QW_HEAD_DIM + dc * 8;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            qa[i] = q0[i] * scale_log2;
+            qb[i] = q0[QW_HEAD_DIM + i] * scale_log2;
+        }
+    }
+    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
+    float oa[8], ob[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) oa[i] = ob[i] = 0.f;
+    const int* bt = kv.block_tables + (size_t)b * kv.bt_stride;
+    const int64_t v_off = (int64_t)Hkv * QW_PAGE_SIZE * QW_HEAD_DIM;
+
+    for (int pi = p_lo + warp; pi < p_hi; pi += AD_WARPS) {
+        const int page = bt[pi];
+        if (page < 0 || page >= kv.n_pages) {
+            if (lane == 0) set_error(err, QW_ERANGE);
+            continue;
+        }
+        const uint16_t* kp = kv.base + (int64_t)page * kv.page_stride + (int64_t)g * QW_PAGE_SIZE * QW_HEAD_DIM +
+                             half * QW_HEAD_DIM + dc * 8;
+        uint4 kr[8], vr[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) kr[i] = ldg_stream(kp + i * 2 * QW_HEAD_DIM);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) vr[i] = ldg_stream(kp + v_off + i * 2 * QW_HEAD_DIM);
+        float sa[8], sb[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            sa[i] = dot8(qa, kr[i]);
+            sb[i] = dot8(qb, kr[i]);
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                sa[i] += __shfl_xor_sync(0xffffffffu, sa[i], o);
+                sb[i] += __shfl_xor_sync(0xffffffffu, sb[i], o);
+            }
+        }
+        float mxa = -INFINITY, mxb = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int kpos = pi * QW_PAGE_SIZE + half + 2 * i;
+            if (kpos >= L) sa[i] = sb[i] = -INFINITY;
+            mxa = fmaxf(mxa, sa[i]);
+            mxb = fmaxf(mxb, sb[i]);
+        }
+        mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 16));
+        mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 16));
+        const float na = fmaxf(m_a, mxa), nb = fmaxf(m_b, mxb);  // finite: key pi*16 is always visible
+        const float ala = exp2f(m_a - na), alb = exp2f(m_b - nb);
+        m_a = na;
+        m_b = nb;
+        l_a *= ala;
+        l_b *= alb;
+#pragma unroll
+        for (int d = 0; d < 8; ++d) {
+            oa[d] *= ala;
+            ob[d] *= alb;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float ea = exp2f(sa[i] - na), eb = exp2f(sb[i] - nb);
+            l_a += ea;
+            l_b += eb;
+            const float v[8] = {bf16_lo(vr[i].x), bf16_hi(vr[i].x), bf16_lo(vr[i].y), bf16_hi(vr[i].y),
+                                bf16_lo(vr[i].z), bf16_hi(vr[i].z), bf16_lo(vr[i].w), bf16_hi(vr[i].w)};
+#pragma unroll
+            for (int d = 0; d < 8; ++d) {
+                oa[d] += ea * v[d];
+                ob[d] += eb * v[d];
+            }
+        }
+    }
+    // the two key halves of a warp share m: add them
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 16);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 16);
+#pragma unroll
+    for (int d = 0; d < 8; ++d) {
+        oa[d] += __shfl_xor_sync(0xffffffffu, oa[d], 16);
+        ob[d] += __shfl_xor_sync(0xffffffffu, ob[d], 16);
+    }
+    __shared__ float s_o[AD_WARPS][2][QW_HEAD_DIM];
+    __shared__ float s_m[AD_WARPS][2], s_l[AD_WARPS][2];
+    if (half == 0) {
+#pragma unroll
+        for (int d = 0; d < 8; ++d) {
+            s_o[warp][0][dc * 8 + d] = oa[d];
+            s_o[warp][1][dc * 8 + d] = ob[d];
+        }
+    }
+    if (lane == 0) {
+        s_m[warp][0] = m_a;
+        s_m[warp][1] = m_b;
+        s_l[warp][0] = l_a;
+        s_l[warp][1] = l_b;
+    }
+    __syncthreads();
+    const int d = threadIdx.x;  // 128 threads = head_dim
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        float M = -INFINITY;
+        for (int w = 0; w < AD_WARPS; ++w)
+            if (s_l[w][hh] > 0.f) M = fmaxf(M, s_m[w][hh]);
+        float Ls = 0.f, O = 0.f;
+        for (int w = 0; w < AD_WARPS; ++w) {
+            if (s_l[w][hh] > 0.f) {
+                const float sc = exp2f(s_m[w][hh] - M);
+                Ls += s_l[w][hh] * sc;
+                O += s_o[w][hh][d] * sc;
+            }
+        }
+        float* dst = hh ? pb : pa;
+        dst[d] = O;
+        if (d == 0) {
+            dst[QW_HEAD_DIM] = M;
+            dst[QW_HEAD_DIM + 1] = Ls;
+        }
+    }
+}
+
+__global__ void attn_combine_kernel(const float* __restrict__ part, int n_splits, int Hq,
+                                    uint16_t* __restrict__ out) {
+    const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+    const float* base = part + ((size_t)b * Hq + h) * n_splits * AD_PART;
+    float M = -INFINITY;
+    for (int s = 0; s < n_splits; ++s)
+        if (base[s * AD_PART + QW_HEAD_DIM + 1] > 0.f) M = fmaxf(M, base[s * AD_PART + QW_HEAD_DIM]);
+    float Ls = 0.f, O = 0.f;
+    for (int s = 0; s < n_splits; ++s) {
+        const float l = base[s * AD_PART + QW_HEAD_DIM + 1];
+        if (l > 0.f) {
+            const float sc = exp2f(base[s * AD_PART + QW_HEAD_DIM] - M);
+            Ls += l * sc;
+            O += base[s * AD_PART + d] * sc;
+        }
+    }
+    out[((size_t)b * Hq + h) * QW_HEAD_DIM + d] = f2bf(Ls > 0.f ? O / Ls : 0.f);
+}
+
+int launch_attn_decode(const float* q, const int* positions, int batch, int Hq, int Hkv, const KvView& kv,
+                       float* part, int max_splits, uint16_t* out, int* err, int n_sm, cudaStream_t st) {
+    if (batch <= 0) return QW_OK;
+    if (Hq != 2 * Hkv) return QW_EINVAL;
+    // pages per split: aim for ~8 CTAs per SM when every sequence is at full capacity
+    long want = ((long)kv.bt_stride * batch * Hkv + 8L * n_sm - 1) / (8L * n_sm);
+    int chunk = 2;
+    while (chunk < want && chunk < 32) chunk <<= 1;
+    int n_splits = (kv.bt_stride + chunk - 1) / chunk;
+    while (n_splits > max_splits) {
+        chunk <<= 1;
+        n_splits = (kv.bt_stride + chunk - 1) / chunk;
+    }
+    const float scale_log2 = 1.4426950408889634f / sqrtf((float)QW_HEAD_DIM);
+    attn_decode_kernel<<<dim3(n_splits, Hkv, batch), AD_WARPS * 32, 0, st>>>(q, positions, Hq, Hkv, kv, chunk,
+                                                                             n_splits, part, scale_log2, err);
+    if (check_launch()) return QW_ECUDA;
+    attn_combine_kernel<<<dim3(Hq, batch), QW_HEAD_DIM, 0, st>>>(part, n_splits, Hq, out);
+    return check_launch();
+}
+
+// ---------------------------------------------------------------- Step 8: sample()
+// One 1024-thread CTA per row.  Greedy rows: argmax (lowest id on ties).  Sampling
+// rows: m = max, Z = sum exp((l - m) / T); a 4-pass radix select finds the top_k
+// largest logits, which are sorted (value descending, id ascending); their
+// probabilities are prefix-summed, the cutoff min(top_k, 1 + #(cumsum < top_p))
+// applied, and the first kept entry with cumsum > u * (kept mass) returned, u from
+// Philox4x32-10 (key = seed, counter = (rng_counter, 0, 0)).
+constexpr int SMP_THREADS = 1024;
+constexpr int SMP_CAND = 2048;
+
+QW_DEV uint32_t order_key(float v) {
+    const uint32_t u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+template <typename T, typename Op>
+QW_DEV T block_reduce(T v, Op op, T* scratch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
+    __syncthreads();
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    v = scratch[lane < (int)(blockDim.x >> 5) ? lane : 0];
+    if (warp == 0) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if (lane == 0) scratch[0] = v;
+    }
+    __syncthreads();
+    v = scratch[0];
+    __syncthreads();
+    return v;
+}
+
+__global__ void __launch_bounds__(SMP_THREADS) sample_kernel(const float* __restrict__ logits, int vocab,
+                                                             const qw_sample_params* __restrict__ params,
+                                                             uint64_t rng_counter, int32_t* __restrict__ out,
+                                                             int* err) {
+    const int row = blockIdx.x, tid = threadIdx.x;
+    const float* lg = logits + (size_t)row * vocab;
+    const qw_sample_params P = params[row];
+    __shared__ float s_f[32];
+    __shared__ unsigned long long s_u[32];
+    __shared__ int s_i[32];
+    __shared__ unsigned long long cand[SMP_CAND];
+    __shared__ uint32_t hist[256];
+    __shared__ uint32_t s_sel, s_rem, s_ncand;
+    __shared__ float cum[SMP_THREADS];
+
+    if (!(P.temperature > 0.f)) {
+        // greedy: pack (order key, ~index) so one max reduction picks the lowest id among equal maxima
+        unsigned long long best = 0ull;
+        for (int j = tid; j < vocab; j += SMP_THREADS) {
+            const unsigned long long k =
+                ((unsigned long long)order_key(lg[j]) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)j);
+            best = k > best ? k : best;
+        }
+        best = block_reduce(best, [](unsigned long long a, unsigned long long b) { return a > b ? a : b; }, s_u);
+        if (tid == 0) out[row] = (int32_t)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
+        return;
+    }
+    int k = P.top_k;
+    float top_p = P.top_p;
+    if (k < 1 || k > QW_MAX_TOP_K || !(top_p > 0.f) || top_p > 1.f) {
+        if (tid == 0) set_error(err, QW_EINVAL);
+        k = min(max(k, 1), QW_MAX_TOP_K);
+        top_p = fminf(fmaxf(top_p, 1e-6f), 1.f);
+    }
+    k = min(k, vocab);
+    const float invT = 1.0f / P.temperature;
+    float mx = -INFINITY;
+    for (int j = tid; j < vocab; j += SMP_THREADS) mx = fmaxf(mx, lg[j]);
+    mx = block_reduce(mx, [](float a, float b) { return fmaxf(a, b); }, s_f);
+    float z = 0.f;
+    for (int j = tid; j < vocab; j += SMP_THREADS) z += expf((lg[j] - mx) * invT);
+    z = block_reduce(z, [](float a, float b) { return a + b; }, s_f);
+
+    // radix select: the k-th largest order key
+    uint32_t prefix = 0, pmask = 0;
+    if (tid == 0) s_rem = (uint32_t)k;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = tid; i < 256; i += SMP_THREADS) hist[i] = 0;
+        __syncthreads();
+        for (int j = tid; j < vocab; j += SMP_THREADS) {
+            const uint32_t u = order_key(lg[j]);
+            if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
+        }
+        __syncthreads();
+        if (tid == 0) {
+            uint32_t c = 0, rem = s_rem;
+            int bsel = 0;
+            for (int bk = 255; bk >= 0; --bk) {
+                if (c + hist[bk] >= rem) {
+                    bsel = bk;
+                    break;
+                }
+                c += hist[bk];
+            }
+            s_sel = (uint32_t)bsel;
+            s_rem = rem - c;
+        }
+        __syncthreads();
+        prefix |= s_sel << shift;
+        pmask |= 255u << shift;
+    }
+    // collect every logit with key >= threshold
+    if (tid == 0) s_ncand = 0;
+    for (int i = tid; i < SMP_CAND; i += SMP_THREADS) cand[i] = 0ull;
+    __syncthreads();
+    for (int j = tid; j < vocab; j += SMP_THREADS) {
+        const uint32_t u = order_key(lg[j]);
+        if (u >= prefix) {
+            const uint32_t slot = atomicAdd(&s_ncand, 1u);
+            if (slot < SMP_CAND)
+                cand[slot] = ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)j);
+        }
+    }
+    __syncthreads();
+    if (tid == 0 && s_ncand > SMP_CAND) set_error(err, QW_EINVAL);
+    // bitonic sort, descending
+    for (int size = 2; size <= SMP_CAND; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = tid; i < SMP_CAND; i += SMP_THREADS) {
+                const int jx = i ^ stride;
+                if (jx > i) {
+                    const bool desc = (i & size) == 0;
+                    const unsigned long long a = cand[i], c = cand[jx];
+                    if (desc ? (a < c) : (a > c)) {
+                        cand[i] = c;
+                        cand[jx] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    // probabilities of the k best in order, inclusive prefix sum
+    float p = 0.f;
+    if (tid < k) {
+        const uint32_t u = (uint32_t)(cand[tid] >> 32);
+        const uint32_t bits = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+        p = expf((__uint_as_float(bits) - mx) * invT) / z;
+    }
+    cum[tid] = p;
+    __syncthreads();
+    for (int off = 1; off < SMP_THREADS; off <<= 1) {
+        const float add = tid >= off ? cum[tid - off] : 0.f;
+        __syncthreads();
+        cum[tid] += add;
+        __syncthreads();
+    }
+    // cutoff = min(k, 1 + #(cum < top_p))
+    int below = (tid < k && cum[tid] < top_p) ? 1 : 0;
+    below = block_reduce(below, [](int a, int b) { return a + b; }, s_i);
+    const int cutoff = min(k, below + 1);
+    uint32_t c4[4] = {(uint32_t)rng_counter, (uint32_t)(rng_counter >> 32), 0u, 0u};
+    philox4x32_10(c4, (uint32_t)P.seed, (uint32_t)(P.seed >> 32));
+    const float u = (float)(c4[0] >> 8) * (1.0f / 16777216.0f);
+    const float target = u * cum[cutoff - 1];
+    int first = (tid < cutoff && cum[tid] > target) ? tid : cutoff - 1;
+    first = block_reduce(first, [](int a, int b) { return a < b ? a : b; }, s_i);
+    if (tid == 0) out[row] = (int32_t)(0xFFFFFFFFu - (uint32_t)(cand[first] & 0xFFFFFFFFull));
+}
+
+int launch_sample(const float* logits, int batch, int vocab, const qw_sample_params* params, uint64_t rng_counter,
+                  int32_t* out_ids, int* err, cudaStream_t st) {
+    if (batch <= 0) return QW_OK;
+    sample_kernel<<<batch, SMP_THREADS, 0, st>>>(logits, vocab, params, rng_counter, out_ids, err);
+    return check_launch();
+}
+
+// ---------------------------------------------------------------- weight staging
+__global__ void bf16_to_f32_kernel(const uint16_t* __restrict__ src, float* __restrict__ dst, int n) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) dst[i] = __uint_as_float((uint32_t)src[i] << 16);
+}
+
+int launch_bf16_to_f32(const uint16_t* src, float* dst, int n, cudaStream_t st) {
+    if (n <= 0) return QW_OK;
+    bf16_to_f32_kernel<<<(n + 255) / 256, 256, 0, st>>>(src, dst, n);
+    return check_launch();
+}
+
+}  // namespace qw

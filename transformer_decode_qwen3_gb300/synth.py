@@ -92,9 +92,11 @@ def _fp32_to_bf16_bits(f: torch.Tensor) -> torch.Tensor:
 
 
 def normal_bf16(seed: int, stream: int, n: int, std: float, device="cpu",
-                start: int = 0, chunk: int = 1 << 20) -> torch.Tensor:
+                start: int = 0, chunk: int | None = None) -> torch.Tensor:
     """n approximately N(0, std) values as a torch.bfloat16 tensor (see module doc)."""
     out = torch.empty(n, dtype=torch.int16, device=device)
+    if chunk is None:
+        chunk = (1 << 20) if out.device.type == "cpu" else (1 << 24)
     scale = torch.tensor(std / _IH4_STD, dtype=torch.float32).item()
     scale_t = torch.tensor(scale, dtype=torch.float32, device=device)
     for c0 in range(0, n, chunk):
