@@ -72,7 +72,7 @@ def test_null_arguments_are_rejected(lib):
     assert lib.qw_decode_step(None, None, None, 1, None, None, 1, None, None) == binding.QW_EINVAL
     assert lib.qw_sample(None, None, 1, None, ctypes.c_uint64(0), None, None) == binding.QW_EINVAL
     assert lib.qw_destroy(None) == binding.QW_EINVAL
-    assert lib.qw_debug_gemm(None, None, None, 1, 32, 64, 0, 128, None) == binding.QW_EINVAL
+    assert lib.qw_debug_gemm(None, None, None, 1, 32, 64, 0, 128, 0, None) == binding.QW_EINVAL
     assert b"bad argument" in lib.qw_last_error_message()
 
 

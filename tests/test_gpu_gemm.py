@@ -49,3 +49,32 @@ def test_gemm_swiglu_pairs(bd):
     g, u = ref[:, 0::2], ref[:, 1::2]
     expect = g * torch.sigmoid(g) * u
     torch.testing.assert_close(C.float(), expect, rtol=1e-2, atol=1e-3)
+
+
+@pytest.mark.parametrize("M,N,K,bn,epi", [(1, 4096, 1024, 256, 0), (64, 1024, 2048, 128, 1), (65, 6144, 1024, 256, 2),
+                                          (200, 1024, 3072, 128, 1), (16, 151936, 1024, 256, 0)])
+def test_gemm_split_operand(bd, M, N, K, bn, epi):
+    """Small-M mode: activations as bf16 hi/lo row pairs, summed in the epilogue (~16-bit mantissa)."""
+    g = torch.Generator(device="cpu").manual_seed(M + N)
+    a = (torch.randn(M, K, generator=g) * 0.5).cuda()
+    B = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16).cuda()
+    ref = a @ B.float().T
+    A = bd.split_rows(a)
+    if epi == 2:
+        C = torch.zeros(A.shape[0], N // 2, dtype=torch.bfloat16, device="cuda")
+        bd.debug_gemm(A, B, C, epi=2, bn=bn, split=True, M=M)
+        torch.cuda.synchronize()
+        idx = torch.arange(M, device="cuda")
+        dst = (idx // 64) * 128 + idx % 64
+        got = C[dst].float() + C[dst + 64].float()
+        gt, up = ref[:, 0::2], ref[:, 1::2]
+        expect = gt * torch.sigmoid(gt) * up
+        err = (got - expect).norm() / expect.norm()
+        assert err < 1e-4, f"rel err {err:.3e}"
+        return
+    X = torch.randn(M, N, device="cuda") if epi == 1 else torch.zeros(M, N, device="cuda")
+    C = X.clone()
+    bd.debug_gemm(A, B, C, epi=epi, bn=bn, split=True, M=M)
+    torch.cuda.synchronize()
+    err = (C - X - ref).norm() / ref.norm()
+    assert err < 2e-5, f"rel err {err:.3e}"           # plain bf16 activations would give ~2e-3

@@ -87,7 +87,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qw_last_error_message.restype = ctypes.c_char_p
     lib.qw_debug_hidden.argtypes = [vp, i32, vp, i32, vp]
     lib.qw_set_decode_path.argtypes = [vp, i32]
-    lib.qw_debug_gemm.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, vp]
+    lib.qw_debug_gemm.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
     lib.qw_kernel_launches.argtypes = []
     lib.qw_kernel_launches.restype = ctypes.c_uint64
     for name in EXPORTED:
@@ -260,12 +260,30 @@ def kernel_launches() -> int:
     return int(load().qw_kernel_launches())
 
 
-def debug_gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, epi: int = 0, bn: int = 256, stream=None):
-    """C (epilogue) = A B^T on the tensor-core projection kernel (see qw_debug_gemm)."""
+def debug_gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, epi: int = 0, bn: int = 256, split: bool = False,
+               M: int | None = None, stream=None):
+    """C (epilogue) = A B^T on the tensor-core projection kernel (see qw_debug_gemm).
+    With split, A is the hi/lo layout and M the number of activation rows."""
     lib = load()
-    M, K = A.shape
+    K = A.shape[1]
+    M = A.shape[0] if M is None else M
     N = B.shape[0]
-    _check(lib.qw_debug_gemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, epi, bn, _stream(stream)), "qw_debug_gemm")
+    _check(lib.qw_debug_gemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, epi, bn, int(split), _stream(stream)),
+           "qw_debug_gemm")
+
+
+def split_rows(a: torch.Tensor) -> torch.Tensor:
+    """The hi/lo bf16 layout of float rows a[M][K] that split-mode projections read."""
+    M, K = a.shape
+    tiles = (M + 63) // 64
+    out = torch.zeros(tiles * 128, K, dtype=torch.bfloat16, device=a.device)
+    hi = a.to(torch.bfloat16)
+    lo = (a - hi.float()).to(torch.bfloat16)
+    idx = torch.arange(M, device=a.device)
+    dst = (idx // 64) * 128 + idx % 64
+    out[dst] = hi
+    out[dst + 64] = lo
+    return out
 
 
 def sample_params(rows: list[tuple[float, int, float, int]], device="cuda") -> torch.Tensor:

@@ -251,6 +251,7 @@ int qw_init(const qw_config* cfg, const qw_weights* w, qw_ctx** out) {
     // ---- workspaces
     const int T = std::max(c.max_tokens, c.max_batch);
     ctx->max_rows = T;
+    const int TA = std::max(T, split_rows(SPLIT_MAX_M));   // rows of the bf16 activation buffers
     ctx->max_tiles = c.max_tokens / 64 + c.max_tokens + 1;
     off = 0;
     const size_t ox = take((size_t)T * D * 4);
@@ -258,9 +259,9 @@ int qw_init(const qw_config* cfg, const qw_weights* w, qw_ctx** out) {
     const size_t oq = take((size_t)T * ctx->attn_dim * 4);
     const size_t ologits = take((size_t)c.max_batch * V * 4);
     const size_t opart = take((size_t)c.max_batch * Hq * ctx->max_splits * (d + 2) * 4);
-    const size_t oh = take((size_t)T * D * 2);
-    const size_t oattn = take((size_t)T * ctx->attn_dim * 2);
-    const size_t oact = take((size_t)T * I * 2);
+    const size_t oh = take((size_t)TA * D * 2);
+    const size_t oattn = take((size_t)TA * ctx->attn_dim * 2);
+    const size_t oact = take((size_t)TA * I * 2);
     const size_t otok = take((size_t)T * 4);
     const size_t oiota = take((size_t)c.max_batch * 4);
     const size_t orows = take((size_t)T * 4);
@@ -345,29 +346,33 @@ static int run_layers(qw_ctx* ctx, int n, const int* ids, const int* positions, 
                       const int* bt, int bt_stride, int mode, int n_tiles, cudaStream_t st) {
     const qw_config& c = ctx->cfg;
     const int D = c.hidden, Hq = c.n_heads, Hkv = c.n_kv_heads, I = c.intermediate;
+    const int split = n <= SPLIT_MAX_M;   // small-M projections take hi/lo activation pairs
     QW_TRY(launch_embed(ids, n, ctx->E, c.vocab, D, ctx->x, ctx->err, st), "embed launch");
     for (int l = 0; l < c.n_layers; ++l) {
         const LayerW& Lw = ctx->L[l];
         KvView kvv{kv->base + (int64_t)l * kv->layer_elems, kv->page_elems, kv->n_pages, bt, bt_stride};
-        QW_TRY(launch_rmsnorm_bf16(ctx->x, nullptr, n, D, Lw.in_norm, c.rms_eps, ctx->h, st), "rmsnorm launch");
-        GemmEpilogue e{ctx->qkv, nullptr, ctx->qkv_dim, ctx->err};
+        QW_TRY(launch_rmsnorm_bf16(ctx->x, nullptr, n, D, Lw.in_norm, c.rms_eps, ctx->h, split, st),
+               "rmsnorm launch");
+        GemmEpilogue e{ctx->qkv, nullptr, ctx->qkv_dim, ctx->err, split};
         QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_qkv, 256, n, ctx->qkv_dim, D, EPI_STORE_F32, e, st), "qkv gemm");
         QW_TRY(launch_qkv_post(ctx->qkv, n, positions, tok_seq, Hq, Hkv, Lw.q_norm, Lw.k_norm, ctx->inv_freq,
                                c.rms_eps, ctx->q, kvv, ctx->err, st),
                "qk-norm/rope/kv-write launch");
         if (mode == 0)
-            QW_TRY(launch_attn_prefill(ctx->q, positions, ctx->tiles, n_tiles, Hq, Hkv, kvv, ctx->attn, ctx->err, st),
+            QW_TRY(launch_attn_prefill(ctx->q, positions, ctx->tiles, n_tiles, Hq, Hkv, kvv, ctx->attn, split,
+                                       ctx->err, st),
                    "prefill attention launch");
         else
             QW_TRY(launch_attn_decode(ctx->q, positions, n, Hq, Hkv, kvv, ctx->part, ctx->max_splits, ctx->attn,
-                                      ctx->err, ctx->n_sm, st),
+                                      split, ctx->err, ctx->n_sm, st),
                    "decode attention launch");
-        e = GemmEpilogue{ctx->x, nullptr, D, ctx->err};
+        e = GemmEpilogue{ctx->x, nullptr, D, ctx->err, split};
         QW_TRY(gemm_bf16(ctx->attn, ctx->attn_dim, Lw.tm_o, 128, n, D, ctx->attn_dim, EPI_RESID_ADD, e, st), "o_proj gemm");
-        QW_TRY(launch_rmsnorm_bf16(ctx->x, nullptr, n, D, Lw.post_norm, c.rms_eps, ctx->h, st), "rmsnorm launch");
-        e = GemmEpilogue{nullptr, ctx->act, I, ctx->err};
+        QW_TRY(launch_rmsnorm_bf16(ctx->x, nullptr, n, D, Lw.post_norm, c.rms_eps, ctx->h, split, st),
+               "rmsnorm launch");
+        e = GemmEpilogue{nullptr, ctx->act, I, ctx->err, split};
         QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_gu, 256, n, 2 * I, D, EPI_SWIGLU, e, st), "gate/up gemm");
-        e = GemmEpilogue{ctx->x, nullptr, D, ctx->err};
+        e = GemmEpilogue{ctx->x, nullptr, D, ctx->err, split};
         QW_TRY(gemm_bf16(ctx->act, I, Lw.tm_d, 128, n, D, I, EPI_RESID_ADD, e, st), "down gemm");
         if (ctx->hidden)
             QW_CUDA(cudaMemcpyAsync(ctx->hidden + (size_t)l * ctx->max_rows * D, ctx->x, (size_t)n * D * 4,
@@ -379,8 +384,9 @@ static int run_layers(qw_ctx* ctx, int n, const int* ids, const int* positions, 
 // final RMSNorm of the selected rows and the tied LM head (Step 8)
 static int lm_head(qw_ctx* ctx, const int* rows, int n, float* out, cudaStream_t st) {
     const qw_config& c = ctx->cfg;
-    QW_TRY(launch_rmsnorm_bf16(ctx->x, rows, n, c.hidden, ctx->final_norm, c.rms_eps, ctx->h, st), "final norm");
-    GemmEpilogue e{out, nullptr, c.vocab, ctx->err};
+    const int split = n <= SPLIT_MAX_M;
+    QW_TRY(launch_rmsnorm_bf16(ctx->x, rows, n, c.hidden, ctx->final_norm, c.rms_eps, ctx->h, split, st), "final norm");
+    GemmEpilogue e{out, nullptr, c.vocab, ctx->err, split};
     QW_TRY(gemm_bf16(ctx->h, c.hidden, ctx->tm_E, 256, n, c.vocab, c.hidden, EPI_STORE_F32, e, st), "lm head gemm");
     return QW_OK;
 }
@@ -485,13 +491,14 @@ int qw_debug_hidden(qw_ctx* ctx, int32_t layer, float* out, int32_t n_rows, void
 }
 
 int qw_debug_gemm(const uint16_t* A, const uint16_t* B, void* C, int32_t M, int32_t N, int32_t K, int32_t epi,
-                  int32_t bn, void* stream) {
+                  int32_t bn, int32_t split, void* stream) {
     if (!A || !B || !C || M < 1 || N < 32 || K < 64 || K % 64 || N % 32 || epi < 0 || epi > 2 ||
         (bn != 128 && bn != 256))
         return fail(QW_EINVAL, "qw_debug_gemm: bad argument");
     CUtensorMap tb;
     QW_TRY(make_tmap_bf16(&tb, B, (uint64_t)K, (uint64_t)N, (uint64_t)K * 2, 64, (uint32_t)bn), "tensor map for B");
-    GemmEpilogue e{epi == 2 ? nullptr : (float*)C, epi == 2 ? (uint16_t*)C : nullptr, epi == 2 ? N / 2 : N, nullptr};
+    GemmEpilogue e{epi == 2 ? nullptr : (float*)C, epi == 2 ? (uint16_t*)C : nullptr, epi == 2 ? N / 2 : N, nullptr,
+                   split ? 1 : 0};
     QW_TRY(gemm_bf16(A, K, tb, bn, M, N, K, epi, e, (cudaStream_t)stream), "gemm launch");
     return QW_OK;
 }

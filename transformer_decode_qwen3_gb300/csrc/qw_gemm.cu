@@ -10,6 +10,12 @@
 // (K = 16 per instruction, 4 per 64-wide K block) and commits each stage back
 // to the producer; all four warps then read the accumulator with tcgen05.ld
 // (thread t owns output row t) and apply the fused epilogue.
+//
+// Split-operand mode (small M, e.g. decode batches): every activation row a is
+// stored as two bf16 rows, hi = bf16(a) in tile rows 0..63 and lo = bf16(a - hi)
+// in rows 64..127, so one M=128 MMA yields hi.W and lo.W side by side and the
+// epilogue adds them: the activation enters with ~16 mantissa bits instead of 8,
+// at no extra tensor-core work (the tile would otherwise be half empty).
 #include <cudaTypedefs.h>
 
 #include <vector>
@@ -33,7 +39,49 @@ struct GemmCfg {
 
 QW_DEV float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
+// Destination row of activation row m in the split layout (hi copy; lo is 64 rows further).
+QW_DEV int split_row(int m) { return (m >> 6) * 128 + (m & 63); }
+
 template <int BN, int EPI>
+QW_DEV void epilogue_chunk(const float (&v)[32], int m, int n, const GemmEpilogue& ep) {
+    if (EPI == EPI_STORE_F32) {
+        float4* dst = (float4*)(ep.out + (size_t)m * ep.ldo + n);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    } else if (EPI == EPI_RESID_ADD) {
+        float4* dst = (float4*)(ep.out + (size_t)m * ep.ldo + n);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float4 r = dst[i];
+            r.x += v[4 * i];
+            r.y += v[4 * i + 1];
+            r.z += v[4 * i + 2];
+            r.w += v[4 * i + 3];
+            dst[i] = r;
+        }
+    } else {  // EPI_SWIGLU: columns alternate gate, up
+        float a[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) a[i] = silu_f(v[2 * i]) * v[2 * i + 1];
+        uint32_t hi[8], lo[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            hi[i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
+            lo[i] = pack_bf16x2(a[2 * i] - bf16_lo(hi[i]), a[2 * i + 1] - bf16_hi(hi[i]));
+        }
+        const int row = ep.split ? split_row(m) : m;
+        uint4* dst = (uint4*)(ep.act + (size_t)row * ep.ldo + (n >> 1));
+        dst[0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        dst[1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+        if (ep.split) {
+            uint4* dl = (uint4*)((uint16_t*)dst + (size_t)64 * ep.ldo);
+            dl[0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            dl[1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+        }
+    }
+}
+
+template <int BN, int EPI, bool SPLIT>
 __global__ void __launch_bounds__(128, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         int M, int N, int K, GemmEpilogue ep) {
@@ -109,45 +157,33 @@ __global__ void __launch_bounds__(128, 1)
     }
     __syncwarp();
 
-    // Epilogue: thread t of the CTA owns output row m0 + t.
+    // Epilogue: thread t of the CTA owns accumulator row t.
     const bool ok = mbar_wait(done, 0, ep.err) && !*abort_flag;
     tc_fence_after();
-    const int m = m0 + warp * 32 + lane;
     if (ok) {
         const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+        float* xch = (float*)smem;  // split mode: lo rows handed to the hi rows (stages are idle now)
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
-            if (n0 + c0 >= N) break;  // warp-uniform
+            if (n0 + c0 >= N) break;  // CTA-uniform
             float v[32];
             tmem_ld32(trow + c0, v);
-            if (m >= M) continue;
-            const int n = n0 + c0;
-            if (EPI == EPI_STORE_F32) {
-                float4* dst = (float4*)(ep.out + (size_t)m * ep.ldo + n);
+            if (SPLIT) {
+                if (warp >= 2) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-            } else if (EPI == EPI_RESID_ADD) {
-                float4* dst = (float4*)(ep.out + (size_t)m * ep.ldo + n);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    float4 r = dst[i];
-                    r.x += v[4 * i];
-                    r.y += v[4 * i + 1];
-                    r.z += v[4 * i + 2];
-                    r.w += v[4 * i + 3];
-                    dst[i] = r;
+                    for (int i = 0; i < 32; ++i) xch[((warp - 2) * 32 + lane) * 33 + i] = v[i];
                 }
-            } else {  // EPI_SWIGLU: columns alternate gate, up
-                uint32_t pk[8];
+                __syncthreads();
+                if (warp < 2) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float a0 = silu_f(v[4 * i]) * v[4 * i + 1];
-                    const float a1 = silu_f(v[4 * i + 2]) * v[4 * i + 3];
-                    pk[i] = pack_bf16x2(a0, a1);
+                    for (int i = 0; i < 32; ++i) v[i] += xch[(warp * 32 + lane) * 33 + i];
+                    const int m = blockIdx.y * 64 + warp * 32 + lane;
+                    if (m < M) epilogue_chunk<BN, EPI>(v, m, n0 + c0, ep);
                 }
-                uint4* dst = (uint4*)(ep.act + (size_t)m * ep.ldo + (n >> 1));
-                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                __syncthreads();
+            } else {
+                const int m = m0 + warp * 32 + lane;
+                if (m < M) epilogue_chunk<BN, EPI>(v, m, n0 + c0, ep);
             }
         }
     }
@@ -185,38 +221,48 @@ int make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t 
     return r == CUDA_SUCCESS ? QW_OK : QW_ECUDA;
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool SPLIT>
 static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, const GemmEpilogue& ep,
                      cudaStream_t st) {
     using C = GemmCfg<BN>;
     static bool attr_set = false;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(gemm_bf16_tc_kernel<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(gemm_bf16_tc_kernel<BN, EPI, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::SMEM) != cudaSuccess)
             return QW_ECUDA;
         attr_set = true;
     }
-    dim3 grid((N + BN - 1) / BN, (M + C::BM - 1) / C::BM);
-    gemm_bf16_tc_kernel<BN, EPI><<<grid, 128, C::SMEM, st>>>(ta, tb, M, N, K, ep);
+    const int m_tiles = SPLIT ? (M + 63) / 64 : (M + C::BM - 1) / C::BM;
+    dim3 grid((N + BN - 1) / BN, m_tiles);
+    gemm_bf16_tc_kernel<BN, EPI, SPLIT><<<grid, 128, C::SMEM, st>>>(ta, tb, M, N, K, ep);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ECUDA;
+}
+
+template <bool SPLIT>
+static int launch_split(const CUtensorMap& ta, const CUtensorMap& tb, int bn, int M, int N, int K, int epi,
+                        const GemmEpilogue& ep, cudaStream_t st) {
+    if (bn == 256) {
+        if (epi == EPI_STORE_F32) return launch_bn<256, EPI_STORE_F32, SPLIT>(ta, tb, M, N, K, ep, st);
+        if (epi == EPI_RESID_ADD) return launch_bn<256, EPI_RESID_ADD, SPLIT>(ta, tb, M, N, K, ep, st);
+        return launch_bn<256, EPI_SWIGLU, SPLIT>(ta, tb, M, N, K, ep, st);
+    }
+    if (epi == EPI_STORE_F32) return launch_bn<128, EPI_STORE_F32, SPLIT>(ta, tb, M, N, K, ep, st);
+    if (epi == EPI_RESID_ADD) return launch_bn<128, EPI_RESID_ADD, SPLIT>(ta, tb, M, N, K, ep, st);
+    return launch_bn<128, EPI_SWIGLU, SPLIT>(ta, tb, M, N, K, ep, st);
 }
 
 int gemm_bf16(const void* A, int lda_elems, const CUtensorMap& tmB, int bn, int M, int N, int K, int epi,
               const GemmEpilogue& ep, cudaStream_t st) {
     if (M <= 0) return QW_OK;
     if (K % 64 || N % 32 || (bn != 128 && bn != 256)) return QW_EINVAL;
+    // split layout: ceil(M/64) tiles of 128 rows (64 hi rows, then their 64 lo rows)
+    const uint64_t rows = ep.split ? (uint64_t)((M + 63) / 64) * 128 : (uint64_t)M;
     CUtensorMap ta;
-    int rc = make_tmap_bf16(&ta, A, (uint64_t)K, (uint64_t)M, (uint64_t)lda_elems * 2, 64, 128);
+    int rc = make_tmap_bf16(&ta, A, (uint64_t)K, rows, (uint64_t)lda_elems * 2, 64, 128);
     if (rc) return rc;
-    if (bn == 256) {
-        if (epi == EPI_STORE_F32) return launch_bn<256, EPI_STORE_F32>(ta, tmB, M, N, K, ep, st);
-        if (epi == EPI_RESID_ADD) return launch_bn<256, EPI_RESID_ADD>(ta, tmB, M, N, K, ep, st);
-        return launch_bn<256, EPI_SWIGLU>(ta, tmB, M, N, K, ep, st);
-    }
-    if (epi == EPI_STORE_F32) return launch_bn<128, EPI_STORE_F32>(ta, tmB, M, N, K, ep, st);
-    if (epi == EPI_RESID_ADD) return launch_bn<128, EPI_RESID_ADD>(ta, tmB, M, N, K, ep, st);
-    return launch_bn<128, EPI_SWIGLU>(ta, tmB, M, N, K, ep, st);
+    return ep.split ? launch_split<true>(ta, tmB, bn, M, N, K, epi, ep, st)
+                    : launch_split<false>(ta, tmB, bn, M, N, K, epi, ep, st);
 }
 
 }  // namespace qw

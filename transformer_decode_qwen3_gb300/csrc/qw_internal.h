@@ -18,7 +18,13 @@ struct GemmEpilogue {
     uint16_t* act;   // EPI_SWIGLU: act[m][n/2] = bf16(silu(acc[2j]) * acc[2j+1])
     int ldo;         // row stride (elements) of out / act
     int* err;        // device error word
+    int split;       // A holds hi/lo row pairs (see split_rows); SwiGLU output is written the same way
 };
+
+// Rows an M-row activation occupies in the split (hi/lo) layout.
+inline int split_rows(int M) { return (M + 63) / 64 * 128; }
+// Small-M GEMMs (decode batches) take their activations as hi/lo bf16 pairs.
+constexpr int SPLIT_MAX_M = 256;
 
 // Tensor map of a row-major bf16 matrix [rows][inner] with a (box_rows x box_inner)
 // box and 128-byte swizzling (box_inner * 2 must be 128).
@@ -40,14 +46,14 @@ struct KvView {
 
 int launch_embed(const int* ids, int n, const uint16_t* E, int vocab, int D, float* x, int* err, cudaStream_t st);
 int launch_rmsnorm_bf16(const float* x, const int* rows /*nullable*/, int n, int D, const float* w, float eps,
-                        uint16_t* out, cudaStream_t st);
+                        uint16_t* out, int split, cudaStream_t st);
 int launch_qkv_post(const float* qkv, int n_tok, const int* positions, const int* tok_seq, int Hq, int Hkv,
                     const float* q_norm, const float* k_norm, const float* inv_freq, float eps, float* q_out,
                     const KvView& kv, int* err, cudaStream_t st);
 int launch_attn_prefill(const float* q, const int* positions, const int4* tiles, int n_tiles, int Hq, int Hkv,
-                        const KvView& kv, uint16_t* out, int* err, cudaStream_t st);
+                        const KvView& kv, uint16_t* out, int split, int* err, cudaStream_t st);
 int launch_attn_decode(const float* q, const int* positions, int batch, int Hq, int Hkv, const KvView& kv,
-                       float* part, int max_splits, uint16_t* out, int* err, int n_sm, cudaStream_t st);
+                       float* part, int max_splits, uint16_t* out, int split, int* err, int n_sm, cudaStream_t st);
 int launch_sample(const float* logits, int batch, int vocab, const qw_sample_params* params, uint64_t rng_counter,
                   int32_t* out_ids, int* err, cudaStream_t st);
 int launch_bf16_to_f32(const uint16_t* src, float* dst, int n, cudaStream_t st);

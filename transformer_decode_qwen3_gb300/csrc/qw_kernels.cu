@@ -16,6 +16,20 @@ static inline int check_launch() {
     return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ECUDA;
 }
 
+// Activation rows feeding a small-M projection are written as bf16 hi/lo pairs:
+// row m goes to row split_dst(m) (hi) and split_dst(m) + 64 (lo = bf16(a - hi)).
+QW_DEV int split_dst(int m) { return (m >> 6) * 128 + (m & 63); }
+QW_DEV void store_bf16x2(uint16_t* base, size_t ld, int row, int col, float a, float b, int split) {
+    const uint32_t hi = pack_bf16x2(a, b);
+    if (!split) {
+        *(uint32_t*)(base + (size_t)row * ld + col) = hi;
+        return;
+    }
+    const int r = split_dst(row);
+    *(uint32_t*)(base + (size_t)r * ld + col) = hi;
+    *(uint32_t*)(base + (size_t)(r + 64) * ld + col) = pack_bf16x2(a - bf16_lo(hi), b - bf16_hi(hi));
+}
+
 // ---------------------------------------------------------------- Step 2: embedding
 // x[t][:] = E[ids[t]][:] widened to fp32.  An id outside [0, vocab) gives a zero row
 // and QW_ERANGE in the error word.
@@ -44,7 +58,7 @@ int launch_embed(const int* ids, int n, const uint16_t* E, int vocab, int D, flo
 // ---------------------------------------------------------------- Step 3: RMSNorm
 // out[r] = bf16(x[src] / sqrt(mean(x[src]^2) + eps) * w), one warp per row.
 __global__ void rmsnorm_bf16_kernel(const float* __restrict__ x, const int* __restrict__ rows, int n, int D,
-                                    const float* __restrict__ w, float eps, uint16_t* __restrict__ out) {
+                                    const float* __restrict__ w, float eps, uint16_t* __restrict__ out, int split) {
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (r >= n) return;
     const int src = rows ? rows[r] : r;
@@ -59,15 +73,15 @@ __global__ void rmsnorm_bf16_kernel(const float* __restrict__ x, const int* __re
     for (int c = lane * 4; c < D; c += 128) {
         float4 v = *(const float4*)(xr + c);
         float4 wv = *(const float4*)(w + c);
-        uint2 o = make_uint2(pack_bf16x2(v.x * s * wv.x, v.y * s * wv.y), pack_bf16x2(v.z * s * wv.z, v.w * s * wv.w));
-        *(uint2*)(out + (size_t)r * D + c) = o;
+        store_bf16x2(out, D, r, c, v.x * s * wv.x, v.y * s * wv.y, split);
+        store_bf16x2(out, D, r, c + 2, v.z * s * wv.z, v.w * s * wv.w, split);
     }
 }
 
 int launch_rmsnorm_bf16(const float* x, const int* rows, int n, int D, const float* w, float eps, uint16_t* out,
-                        cudaStream_t st) {
+                        int split, cudaStream_t st) {
     if (n <= 0) return QW_OK;
-    rmsnorm_bf16_kernel<<<(n + 7) / 8, 256, 0, st>>>(x, rows, n, D, w, eps, out);
+    rmsnorm_bf16_kernel<<<(n + 7) / 8, 256, 0, st>>>(x, rows, n, D, w, eps, out, split);
     return check_launch();
 }
 
@@ -173,7 +187,6 @@ QW_DEV void cp_async_wait() {
 // stream from the paged cache in tiles of 64 positions (double-buffered cp.async,
 // XOR-swizzled rows), S = QK^T and PV run on mma.sync m16n8k16 with an online
 // softmax in fp32.  Key position j is visible to a query at position p iff j <= p.
-constexpr int AP_ROWS = 64;
 constexpr int AP_KEYS = 64;
 constexpr int AP_SMEM = 2 * 2 * AP_KEYS * QW_HEAD_DIM * 2;  // 2 buffers x (K, V) x 64 x 128 bf16
 
@@ -181,7 +194,7 @@ __global__ void __launch_bounds__(256) attn_prefill_kernel(const float* __restri
                                                            const int* __restrict__ positions,
                                                            const int4* __restrict__ tiles, int Hq, int Hkv,
                                                            KvView kv, uint16_t* __restrict__ out, float scale_log2,
-                                                           int* err) {
+                                                           int split, int* err) {
     extern __shared__ __align__(128) uint8_t sm[];
     const int4 tile = tiles[blockIdx.x];
     const int seq = tile.x, row0 = tile.y, nrows = tile.z;
@@ -340,13 +353,13 @@ __global__ void __launch_bounds__(256) attn_prefill_kernel(const float* __restri
 #pragma unroll
     for (int nd = 0; nd < 16; ++nd) {
         const int d = h * QW_HEAD_DIM + nd * 8 + 2 * tq;
-        if (ra < nrows) *(uint32_t*)(out + (size_t)(row0 + ra) * ld + d) = pack_bf16x2(o[nd][0] * ia, o[nd][1] * ia);
-        if (rb < nrows) *(uint32_t*)(out + (size_t)(row0 + rb) * ld + d) = pack_bf16x2(o[nd][2] * ib, o[nd][3] * ib);
+        if (ra < nrows) store_bf16x2(out, ld, row0 + ra, d, o[nd][0] * ia, o[nd][1] * ia, split);
+        if (rb < nrows) store_bf16x2(out, ld, row0 + rb, d, o[nd][2] * ib, o[nd][3] * ib, split);
     }
 }
 
 int launch_attn_prefill(const float* q, const int* positions, const int4* tiles, int n_tiles, int Hq, int Hkv,
-                        const KvView& kv, uint16_t* out, int* err, cudaStream_t st) {
+                        const KvView& kv, uint16_t* out, int split, int* err, cudaStream_t st) {
     if (n_tiles <= 0) return QW_OK;
     if (Hq != 2 * Hkv) return QW_EINVAL;
     static bool attr = false;
@@ -358,7 +371,7 @@ int launch_attn_prefill(const float* q, const int* positions, const int4* tiles,
     }
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)QW_HEAD_DIM);
     attn_prefill_kernel<<<dim3(n_tiles, Hkv), 256, AP_SMEM, st>>>(q, positions, tiles, Hq, Hkv, kv, out,
-                                                                  scale_log2, err);
+                                                                  scale_log2, split, err);
     return check_launch();
 }
 
@@ -536,26 +549,28 @@ __global__ void __launch_bounds__(AD_WARPS * 32) attn_decode_kernel(const float*
 }
 
 __global__ void attn_combine_kernel(const float* __restrict__ part, int n_splits, int Hq,
-                                    uint16_t* __restrict__ out) {
-    const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
+                                    uint16_t* __restrict__ out, int split) {
+    const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x * 2;
     const float* base = part + ((size_t)b * Hq + h) * n_splits * AD_PART;
     float M = -INFINITY;
     for (int s = 0; s < n_splits; ++s)
         if (base[s * AD_PART + QW_HEAD_DIM + 1] > 0.f) M = fmaxf(M, base[s * AD_PART + QW_HEAD_DIM]);
-    float Ls = 0.f, O = 0.f;
+    float Ls = 0.f, O0 = 0.f, O1 = 0.f;
     for (int s = 0; s < n_splits; ++s) {
         const float l = base[s * AD_PART + QW_HEAD_DIM + 1];
         if (l > 0.f) {
             const float sc = exp2f(base[s * AD_PART + QW_HEAD_DIM] - M);
             Ls += l * sc;
-            O += base[s * AD_PART + d] * sc;
+            O0 += base[s * AD_PART + d] * sc;
+            O1 += base[s * AD_PART + d + 1] * sc;
         }
     }
-    out[((size_t)b * Hq + h) * QW_HEAD_DIM + d] = f2bf(Ls > 0.f ? O / Ls : 0.f);
+    const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+    store_bf16x2(out, (size_t)Hq * QW_HEAD_DIM, b, h * QW_HEAD_DIM + d, O0 * inv, O1 * inv, split);
 }
 
 int launch_attn_decode(const float* q, const int* positions, int batch, int Hq, int Hkv, const KvView& kv,
-                       float* part, int max_splits, uint16_t* out, int* err, int n_sm, cudaStream_t st) {
+                       float* part, int max_splits, uint16_t* out, int split, int* err, int n_sm, cudaStream_t st) {
     if (batch <= 0) return QW_OK;
     if (Hq != 2 * Hkv) return QW_EINVAL;
     // pages per split: aim for ~8 CTAs per SM when every sequence is at full capacity
@@ -571,7 +586,7 @@ int launch_attn_decode(const float* q, const int* positions, int batch, int Hq, 
     attn_decode_kernel<<<dim3(n_splits, Hkv, batch), AD_WARPS * 32, 0, st>>>(q, positions, Hq, Hkv, kv, chunk,
                                                                              n_splits, part, scale_log2, err);
     if (check_launch()) return QW_ECUDA;
-    attn_combine_kernel<<<dim3(Hq, batch), QW_HEAD_DIM, 0, st>>>(part, n_splits, Hq, out);
+    attn_combine_kernel<<<dim3(Hq, batch), QW_HEAD_DIM / 2, 0, st>>>(part, n_splits, Hq, out, split);
     return check_launch();
 }
 
