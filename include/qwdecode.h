@@ -163,6 +163,20 @@ int qw_decode_step(qw_ctx* ctx, const int32_t* tokens, const int32_t* positions,
 int qw_sample(qw_ctx* ctx, const float* logits, int32_t batch, const qw_sample_params* params,
               uint64_t rng_counter, int32_t* out_ids, void* stream);
 
+/* Decode attention of one layer over the paged cache (Step 5 for one new token per
+ * sequence): out[b][h] = softmax(q[b][h] . K^T / sqrt(128)) V over the cached positions
+ * 0 .. positions[b] of sequence b, with query head h reading KV head
+ * h / (n_heads / n_kv_heads).
+ *   q            DEVICE float[batch][n_heads][128], after QK-Norm and RoPE.
+ *   positions    DEVICE int32[batch]; block_tables DEVICE int32[batch][bt_stride].
+ *   layer        which layer's pages of `kv` to read.
+ *   out          DEVICE bf16[batch][n_heads * 128].
+ * The cache is split into chunks whose partial results (running max, sum, weighted
+ * values) go to the context's workspace and are merged by a second kernel.
+ * 1 <= batch <= max_batch. */
+int qw_attn_decode(qw_ctx* ctx, const float* q, const int32_t* positions, int32_t batch, qw_kv* kv,
+                   int32_t layer, const int32_t* block_tables, int32_t bt_stride, uint16_t* out, void* stream);
+
 /* Wait for `stream`, then return and clear the first error the kernels recorded
  * since the last check (QW_OK if none). */
 int qw_check(qw_ctx* ctx, void* stream);

@@ -94,6 +94,25 @@ def softmax(s: np.ndarray, axis: int = -1) -> np.ndarray:
     return e / np.sum(e, axis=axis, keepdims=True)
 
 
+def gqa_attention(q, k, v, kpos, qpos):
+    """Step 5 core: softmax(q k^T / sqrt(d)) v per query head, query head h reading kv
+    head h // (n_heads / n_kv_heads) (the article expands K and V with repeat), keys at
+    positions above the query's position excluded.
+
+    q [Hq, T, d], k and v [Hkv, L, d], kpos [L], qpos [T] -> [Hq, T, d]."""
+    Hq, T, d = q.shape
+    group = Hq // k.shape[0]
+    K = np.repeat(k, group, axis=0)
+    V = np.repeat(v, group, axis=0)
+    visible = np.asarray(kpos, dtype=np.int64)[None, :] <= np.asarray(qpos, dtype=np.int64)[:, None]
+    out = np.empty((Hq, T, d))
+    for h in range(Hq):
+        scores = (q[h] @ K[h].T) * d ** -0.5
+        scores = np.where(visible, scores, -np.inf)
+        out[h] = softmax(scores) @ V[h]
+    return out
+
+
 class LayerCache:
     """Per-layer, per-sequence cache of post-RoPE keys and values (Step 5, 'The KV cache').
 
@@ -144,16 +163,7 @@ class Qwen3Oracle:
         else:
             c.append(k, v, positions)
         cache[layer] = c
-        group = S.n_heads // S.n_kv_heads
-        K = np.repeat(c.k, group, axis=0)     # GQA: kv head j serves query heads j*group .. j*group+group-1
-        V = np.repeat(c.v, group, axis=0)
-        scale = S.head_dim ** -0.5
-        visible = c.pos[None, :] <= np.asarray(positions, dtype=np.int64)[:, None]   # [T, total]
-        out = np.empty((S.n_heads, T, S.head_dim))
-        for h in range(S.n_heads):
-            scores = (q[h] @ K[h].T) * scale
-            scores = np.where(visible, scores, -np.inf)
-            out[h] = softmax(scores) @ V[h]
+        out = gqa_attention(q, c.k, c.v, c.pos, positions)
         out = out.transpose(1, 0, 2).reshape(T, S.n_heads * S.head_dim)
         return out @ W[f"{p}.o_proj.weight"].T
 

@@ -26,7 +26,7 @@ QW_MAX_TOP_K = 1024
 
 EXPORTED = ["qw_config_default", "qw_init", "qw_destroy", "qw_kv_create", "qw_kv_destroy", "qw_kv_layout",
             "qw_prefill", "qw_decode_step", "qw_sample", "qw_check", "qw_last_error_message",
-            "qw_debug_hidden", "qw_set_decode_path", "qw_debug_gemm", "qw_kernel_launches"]
+            "qw_debug_hidden", "qw_set_decode_path", "qw_debug_gemm", "qw_kernel_launches", "qw_attn_decode"]
 
 
 class QwConfig(ctypes.Structure):
@@ -88,6 +88,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qw_debug_hidden.argtypes = [vp, i32, vp, i32, vp]
     lib.qw_set_decode_path.argtypes = [vp, i32]
     lib.qw_debug_gemm.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
+    lib.qw_attn_decode.argtypes = [vp, vp, vp, i32, vp, i32, vp, i32, vp, vp]
     lib.qw_kernel_launches.argtypes = []
     lib.qw_kernel_launches.restype = ctypes.c_uint64
     for name in EXPORTED:
@@ -200,6 +201,11 @@ class Model:
         batch = out_ids.numel() if batch is None else batch
         _check(_lib.qw_sample(self.handle, _ptr(logits), batch, _ptr(params), ctypes.c_uint64(rng_counter),
                               _ptr(out_ids), _stream(stream)), "qw_sample")
+
+    def attn_decode(self, q, positions, kv: "KVPool", layer: int, block_tables, out, stream=None):
+        _check(_lib.qw_attn_decode(self.handle, _ptr(q), _ptr(positions), positions.numel(), kv.handle, layer,
+                                   _ptr(block_tables), block_tables.shape[1], _ptr(out), _stream(stream)),
+               "qw_attn_decode")
 
     def check(self, stream=None):
         _check(_lib.qw_check(self.handle, _stream(stream)), "qw_check")

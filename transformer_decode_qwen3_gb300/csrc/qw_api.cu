@@ -466,6 +466,19 @@ int qw_sample(qw_ctx* ctx, const float* logits, int32_t batch, const qw_sample_p
     return QW_OK;
 }
 
+int qw_attn_decode(qw_ctx* ctx, const float* q, const int32_t* positions, int32_t batch, qw_kv* kv, int32_t layer,
+                   const int32_t* bt, int32_t bt_stride, uint16_t* out, void* stream) {
+    if (!ctx || !q || !positions || !kv || !bt || !out) return fail(QW_EINVAL, "qw_attn_decode: null argument");
+    if (kv->ctx != ctx) return fail(QW_EINVAL, "qw_attn_decode: kv pool belongs to another context");
+    if (batch < 1 || batch > ctx->cfg.max_batch || layer < 0 || layer >= ctx->cfg.n_layers || bt_stride < 1)
+        return fail(QW_EINVAL, "qw_attn_decode: batch, layer or bt_stride out of range");
+    KvView kvv{kv->base + (int64_t)layer * kv->layer_elems, kv->page_elems, kv->n_pages, bt, bt_stride};
+    QW_TRY(launch_attn_decode(q, positions, batch, ctx->cfg.n_heads, ctx->cfg.n_kv_heads, kvv, ctx->part,
+                              ctx->max_splits, out, 0, ctx->err, ctx->n_sm, (cudaStream_t)stream),
+           "decode attention launch");
+    return QW_OK;
+}
+
 int qw_check(qw_ctx* ctx, void* stream) {
     if (!ctx) return fail(QW_EINVAL, "null context");
     QW_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
