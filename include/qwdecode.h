@@ -48,6 +48,7 @@ extern "C" {
 #define QW_PAGE_SIZE 16   /* tokens per KV page */
 #define QW_HEAD_DIM 128   /* the only head size the kernels implement */
 #define QW_MAX_TOP_K 1024 /* largest top_k qw_sample accepts */
+#define QW_NOALLOC_SCRATCH_FLOATS (1 << 20) /* fixed scratch of qw_attn_decode_noalloc: 4 MiB */
 
 typedef struct qw_ctx qw_ctx;
 typedef struct qw_kv qw_kv;
@@ -176,6 +177,34 @@ int qw_sample(qw_ctx* ctx, const float* logits, int32_t batch, const qw_sample_p
  * 1 <= batch <= max_batch. */
 int qw_attn_decode(qw_ctx* ctx, const float* q, const int32_t* positions, int32_t batch, qw_kv* kv,
                    int32_t layer, const int32_t* block_tables, int32_t bt_stride, uint16_t* out, void* stream);
+
+/* qw_attn_decode for callers that cannot allocate device memory.  The article has no
+ * counterpart: this is a memory-management variant of the call above, not a step of
+ * the method.
+ *
+ * Who needs it: code that must not call cudaMalloc/cudaFree on its path, such as a
+ * latency-critical decode loop (cudaMalloc and cudaFree can synchronise the whole
+ * device and stall other streams), a process whose device memory is entirely handed to
+ * another allocator (a framework's caching allocator or a fixed-size pool, where an extra
+ * allocation fails or fragments it), or a library that must own no device memory.  It
+ * takes no context and allocates nothing: the caller passes the query, the pages of one
+ * layer, the block tables and the output, and the split partials go to a fixed array
+ * of QW_NOALLOC_SCRATCH_FLOATS floats (4 MiB) compiled into this library, which every
+ * GPU that loads the library holds until the process exits.
+ *   kv_layer   DEVICE bf16 pages of one layer, [n_pages][2][n_kv_heads][16][128]
+ *              (qw_kv_layout's base plus layer * layer_stride for a qw_kv pool).
+ *   q, positions, block_tables, bt_stride, out: as in qw_attn_decode; n_heads must be
+ *              2 * n_kv_heads.
+ * Limits: batch * n_heads * 130 <= QW_NOALLOC_SCRATCH_FLOATS (batch * n_heads <= 8065),
+ * else QW_EINVAL with nothing launched.  Page ids outside [0, n_pages) are skipped but,
+ * with no context, not reported.
+ * The first call on each device looks up the array's device address (once per device,
+ * with that device current); make that first call before any stream capture.  All calls
+ * share the one array and nothing in it needs to start at zero: calls whose GPU work can
+ * overlap (different streams, several host threads) race on it, so serialise them. */
+int qw_attn_decode_noalloc(const float* q, const int32_t* positions, int32_t batch, int32_t n_heads,
+                           int32_t n_kv_heads, const uint16_t* kv_layer, int32_t n_pages,
+                           const int32_t* block_tables, int32_t bt_stride, uint16_t* out, void* stream);
 
 /* Wait for `stream`, then return and clear the first error the kernels recorded
  * since the last check (QW_OK if none). */

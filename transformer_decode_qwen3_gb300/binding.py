@@ -26,7 +26,7 @@ QW_MAX_TOP_K = 1024
 
 EXPORTED = ["qw_config_default", "qw_init", "qw_destroy", "qw_kv_create", "qw_kv_destroy", "qw_kv_layout",
             "qw_prefill", "qw_decode_step", "qw_sample", "qw_check", "qw_last_error_message",
-            "qw_debug_hidden", "qw_set_decode_path", "qw_debug_gemm", "qw_kernel_launches", "qw_attn_decode"]
+            "qw_debug_hidden", "qw_set_decode_path", "qw_debug_gemm", "qw_kernel_launches", "qw_attn_decode", "qw_attn_decode_noalloc"]
 
 
 class QwConfig(ctypes.Structure):
@@ -89,6 +89,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qw_set_decode_path.argtypes = [vp, i32]
     lib.qw_debug_gemm.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
     lib.qw_attn_decode.argtypes = [vp, vp, vp, i32, vp, i32, vp, i32, vp, vp]
+    lib.qw_attn_decode_noalloc.argtypes = [vp, vp, i32, i32, i32, vp, i32, vp, i32, vp, vp]
     lib.qw_kernel_launches.argtypes = []
     lib.qw_kernel_launches.restype = ctypes.c_uint64
     for name in EXPORTED:
@@ -259,6 +260,15 @@ def _tensor_from_ptr(ptr: int, numel: int, dtype) -> torch.Tensor:
                                              "data": (ptr, False), "version": 3}
     t = torch.as_tensor(_Holder(), device="cuda")
     return t.view(dtype) if dtype == torch.bfloat16 else t
+
+
+def attn_decode_noalloc(q, positions, n_heads: int, n_kv_heads: int, kv_layer_ptr: int, n_pages: int,
+                        block_tables, out, stream=None):
+    """qw_attn_decode_noalloc: decode attention with the library's fixed scratch (no allocation)."""
+    lib = load()
+    _check(lib.qw_attn_decode_noalloc(_ptr(q), _ptr(positions), positions.numel(), n_heads, n_kv_heads, kv_layer_ptr,
+                                      n_pages, _ptr(block_tables), block_tables.shape[1], _ptr(out), _stream(stream)),
+           "qw_attn_decode_noalloc")
 
 
 def kernel_launches() -> int:

@@ -26,6 +26,10 @@ int fail(int code, const std::string& msg) {
 }
 }  // namespace
 
+namespace qw {
+int report_error(int code, const char* msg) { return fail(code, msg); }
+}  // namespace qw
+
 #define QW_CUDA(call)                                                                              \
     do {                                                                                           \
         cudaError_t e_ = (call);                                                                   \

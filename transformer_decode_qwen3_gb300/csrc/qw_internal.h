@@ -11,6 +11,9 @@ namespace qw {
 // Counts every kernel launch the library makes (read by qw_kernel_launches).
 void count_launches(int n);
 
+// Record `msg` for qw_last_error_message() on this thread and return `code`.
+int report_error(int code, const char* msg);
+
 enum { EPI_STORE_F32 = 0, EPI_RESID_ADD = 1, EPI_SWIGLU = 2 };
 
 struct GemmEpilogue {
