@@ -231,6 +231,16 @@ int qw_debug_hidden(qw_ctx* ctx, int32_t layer, float* out, int32_t n_rows, void
 int qw_debug_gemm(const uint16_t* A, const uint16_t* B, void* C, int32_t M, int32_t N, int32_t K, int32_t epi,
                   int32_t bn, int32_t split, void* stream);
 
+/* Tracing hook of the fused batch-1 decode kernel.  enable = 1: the following fused
+ * steps record %globaltimer stamps (ns) at every phase boundary; enable = 0: stop.
+ * host_out (nullable, HOST uint64[n]): receives the stamps of the last traced step,
+ * [CTA][layer 0..n_layers][16 slots] (slot 0/1: before/after the wait for the layer
+ * input, 2: q|k|v published, 3: attention input ready, 4: attention split published,
+ * 5: attention merged, 6: o_proj published, 7: MLP input ready, 8: layer published,
+ * 9: the producer has issued the layer's weights; layer n_layers: LM head wait
+ * begin/end and done).  *n_needed receives the buffer length.  Synchronous. */
+int qw_debug_trace(qw_ctx* ctx, int32_t enable, uint64_t* host_out, int64_t n, int64_t* n_needed);
+
 /* Number of kernels this library has launched in the process so far (all contexts). */
 uint64_t qw_kernel_launches(void);
 

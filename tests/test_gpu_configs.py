@@ -54,7 +54,7 @@ def _greedy(model, bd, logits):
     return ids.cpu().numpy()
 
 
-def _prompt_then_greedy(full, T, steps, call):
+def _prompt_then_greedy(full, T, steps, call, path=0):
     bd, model, orc = full
     n_pages = math.ceil((T + steps) / Q.PAGE) + 1
     kv = bd.KVPool(model, n_pages)
@@ -73,6 +73,19 @@ def _prompt_then_greedy(full, T, steps, call):
     errs = [Q.rel_l2_rows(last.cpu().numpy(), ref).max()]
     gpu_ids, ref_rows, ref_ids = [_greedy(model, bd, last)[0]], [ref[0]], [int(np.argmax(ref[0]))]
     logits = torch.empty(1, V, device="cuda")
+    model.set_decode_path(path)
+    try:
+        _decode_loop(model, bd, orc, kv, bt, cache, T, steps, logits, errs, gpu_ids, ref_rows, ref_ids)
+    finally:
+        model.set_decode_path(0)
+    model.check()
+    assert max(errs) < Q.LOGIT_TOL, f"worst logits rel L2 {max(errs):.2e} at step {int(np.argmax(errs))}"
+    checked = Q.assert_tokens_match(gpu_ids, ref_rows, ref_ids)
+    assert checked >= len(gpu_ids) // 2
+    return max(errs)
+
+
+def _decode_loop(model, bd, orc, kv, bt, cache, T, steps, logits, errs, gpu_ids, ref_rows, ref_ids):
     for step in range(steps):
         tok, pos = ref_ids[-1], T + step                       # teacher forcing with the oracle's choice
         model.decode_step(torch.tensor([tok], dtype=torch.int32).cuda(),
@@ -82,11 +95,6 @@ def _prompt_then_greedy(full, T, steps, call):
         gpu_ids.append(_greedy(model, bd, logits)[0])
         ref_rows.append(ref[0])
         ref_ids.append(int(np.argmax(ref[0])))
-    model.check()
-    assert max(errs) < Q.LOGIT_TOL, f"worst logits rel L2 {max(errs):.2e} at step {int(np.argmax(errs))}"
-    checked = Q.assert_tokens_match(gpu_ids, ref_rows, ref_ids)
-    assert checked >= len(gpu_ids) // 2
-    return max(errs)
 
 
 def test_config1_prompt5_greedy8(full):
@@ -95,6 +103,43 @@ def test_config1_prompt5_greedy8(full):
 
 def test_config2_prompt512_greedy256(full):
     _prompt_then_greedy(full, 512, 256, call=1)
+
+
+def test_config1_fused_decode(full):
+    """The same workload through the fused persistent decode kernel."""
+    _prompt_then_greedy(full, 5, 8, call=0, path=2)
+
+
+def test_config2_fused_decode(full):
+    _prompt_then_greedy(full, 512, 256, call=1, path=2)
+
+
+def test_fused_greedy_hint_and_paths_agree(full):
+    """Fused and per-op decode give the same logits within tolerance, and greedy sampling
+    from the context's logits (the fused argmax) equals the scan of the returned logits."""
+    bd, model, orc = full
+    T = 40
+    kv = bd.KVPool(model, 8)
+    bt = torch.arange(8, dtype=torch.int32, device="cuda").view(1, 8)
+    ids = synth.token_ids(0, 7, T, V).cuda()
+    model.prefill(ids, torch.arange(T, dtype=torch.int32, device="cuda"), [0, T], kv, bt, None)
+    tok = torch.tensor([17], dtype=torch.int32, device="cuda")
+    pos = torch.tensor([T], dtype=torch.int32, device="cuda")
+    a, b = torch.empty(1, V, device="cuda"), torch.empty(1, V, device="cuda")
+    model.set_decode_path(1)
+    model.decode_step(tok, pos, kv, bt, a)
+    model.set_decode_path(2)
+    try:
+        model.decode_step(tok, pos, kv, bt, b)
+        assert Q.rel_l2_rows(b.cpu().numpy(), a.cpu().numpy()).max() < Q.LOGIT_TOL
+        model.decode_step(tok, pos, kv, bt, None)
+        params = bd.sample_params([(0.0, 1, 1.0, 0)])
+        out = torch.empty(1, dtype=torch.int32, device="cuda")
+        model.sample(params, 0, out)
+        model.check()
+        assert int(out) == int(torch.argmax(b[0]))
+    finally:
+        model.set_decode_path(0)
 
 
 def test_config3_prefill_8x2048(full):

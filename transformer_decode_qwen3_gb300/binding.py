@@ -26,7 +26,7 @@ QW_MAX_TOP_K = 1024
 
 EXPORTED = ["qw_config_default", "qw_init", "qw_destroy", "qw_kv_create", "qw_kv_destroy", "qw_kv_layout",
             "qw_prefill", "qw_decode_step", "qw_sample", "qw_check", "qw_last_error_message",
-            "qw_debug_hidden", "qw_set_decode_path", "qw_debug_gemm", "qw_kernel_launches", "qw_attn_decode", "qw_attn_decode_noalloc"]
+            "qw_debug_hidden", "qw_set_decode_path", "qw_debug_gemm", "qw_kernel_launches", "qw_attn_decode", "qw_attn_decode_noalloc", "qw_debug_trace"]
 
 
 class QwConfig(ctypes.Structure):
@@ -90,6 +90,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qw_debug_gemm.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]
     lib.qw_attn_decode.argtypes = [vp, vp, vp, i32, vp, i32, vp, i32, vp, vp]
     lib.qw_attn_decode_noalloc.argtypes = [vp, vp, i32, i32, i32, vp, i32, vp, i32, vp, vp]
+    lib.qw_debug_trace.argtypes = [vp, i32, vp, i64, ctypes.POINTER(i64)]
     lib.qw_kernel_launches.argtypes = []
     lib.qw_kernel_launches.restype = ctypes.c_uint64
     for name in EXPORTED:
@@ -207,6 +208,17 @@ class Model:
         _check(_lib.qw_attn_decode(self.handle, _ptr(q), _ptr(positions), positions.numel(), kv.handle, layer,
                                    _ptr(block_tables), block_tables.shape[1], _ptr(out), _stream(stream)),
                "qw_attn_decode")
+
+    def trace(self, enable: bool, fetch: bool = False):
+        """Fused-decode phase stamps: returns a uint64 tensor [CTA, layers + 1, 16] when fetch."""
+        need = ctypes.c_int64()
+        _check(_lib.qw_debug_trace(self.handle, int(enable), None, 0, ctypes.byref(need)), "qw_debug_trace")
+        if not fetch:
+            return None
+        out = torch.zeros(need.value, dtype=torch.int64)
+        _check(_lib.qw_debug_trace(self.handle, int(enable), out.data_ptr(), need.value, ctypes.byref(need)),
+               "qw_debug_trace")
+        return out.view(-1, self.shape.n_layers + 1, 16)
 
     def check(self, stream=None):
         _check(_lib.qw_check(self.handle, _stream(stream)), "qw_check")

@@ -67,6 +67,7 @@ struct qw_ctx {
     int last_rows = 0, logits_rows = 0;
     int decode_path = 0;
     FusedDecode* fused = nullptr;
+    bool last_fused = false;   // the last decode step ran the fused kernel (its argmax is valid)
 };
 
 struct qw_kv {
@@ -297,6 +298,25 @@ int qw_init(const qw_config* cfg, const qw_weights* w, qw_ctx** out) {
         QW_INIT_CUDA(cudaMemcpy(ctx->iota, iota.data(), iota.size() * 4, cudaMemcpyHostToDevice));
         QW_INIT_CUDA(cudaMemset(ctx->err, 0, 64));
     }
+    {
+        FusedWeights fw;
+        fw.E = ctx->E;
+        fw.final_norm = ctx->final_norm;
+        fw.inv_freq = ctx->inv_freq;
+        for (int l = 0; l < c.n_layers; ++l) {
+            const LayerW& Lw = ctx->L[l];
+            fw.wqkv.push_back(Lw.wqkv);
+            fw.wo.push_back(Lw.wo);
+            fw.wgu.push_back(Lw.wgu);
+            fw.wd.push_back(Lw.wd);
+            fw.in_norm.push_back(Lw.in_norm);
+            fw.post_norm.push_back(Lw.post_norm);
+            fw.q_norm.push_back(Lw.q_norm);
+            fw.k_norm.push_back(Lw.k_norm);
+        }
+        ctx->fused = fused_create(fw, c.n_layers, V, c.rms_eps, D, Hq, Hkv, I);
+        cudaGetLastError();  // a shape the fused kernel does not take is not an error
+    }
     QW_INIT_CUDA(cudaDeviceSynchronize());
 #undef QW_INIT_CUDA
     *out = ctx;
@@ -427,6 +447,7 @@ int qw_prefill(qw_ctx* ctx, const int32_t* ids, const int32_t* positions, const 
     int rc = run_layers(ctx, n, ids, positions, ctx->tok_seq, kv, bt, bt_stride, 0, (int)tiles.size(), st);
     if (rc) return rc;
     ctx->last_rows = n;
+    ctx->last_fused = false;
     float* out = last_logits ? last_logits : ctx->logits;
     if ((rc = lm_head(ctx, ctx->rows_last, n_seqs, out, st))) return rc;
     ctx->logits_rows = last_logits ? 0 : n_seqs;
@@ -441,9 +462,13 @@ int qw_decode_step(qw_ctx* ctx, const int32_t* tokens, const int32_t* positions,
     if (bt_stride < 1) return fail(QW_EINVAL, "qw_decode_step: bt_stride must be >= 1");
     cudaStream_t st = (cudaStream_t)stream;
     float* out = logits ? logits : ctx->logits;
-    const bool fused = ctx->decode_path == 2 || (ctx->decode_path == 0 && fused_supported(ctx->fused, batch));
+    // automatic choice: the fused kernel for batch 1, unless per-layer residuals are kept for checking
+    const bool fused = fused_supported(ctx->fused, batch) &&
+                       (ctx->decode_path == 2 || (ctx->decode_path == 0 && !ctx->hidden));
+    if (ctx->decode_path == 2 && !fused) return fail(QW_EINVAL, "qw_decode_step: the fused path takes batch 1 only");
     int rc;
-    if (fused && ctx->fused) {
+    ctx->last_fused = fused;
+    if (fused) {
         rc = fused_decode(ctx->fused, tokens, positions, batch, kv->base, kv->layer_elems, kv->page_elems,
                           kv->n_pages, bt, bt_stride, out, ctx->err, st);
         if (rc) return fail(rc, "fused decode launch failed");
@@ -465,7 +490,9 @@ int qw_sample(qw_ctx* ctx, const float* logits, int32_t batch, const qw_sample_p
         if (ctx->logits_rows < batch) return fail(QW_EINVAL, "qw_sample: the context holds fewer logits rows than batch");
         logits = ctx->logits;
     }
-    QW_TRY(launch_sample(logits, batch, ctx->cfg.vocab, params, rng_counter, out_ids, ctx->err, (cudaStream_t)stream),
+    const int* hint = (logits == ctx->logits && ctx->last_fused && batch == 1) ? fused_argmax(ctx->fused) : nullptr;
+    QW_TRY(launch_sample(logits, batch, ctx->cfg.vocab, params, rng_counter, out_ids, hint, ctx->err,
+                         (cudaStream_t)stream),
            "sample launch");
     return QW_OK;
 }
@@ -490,6 +517,10 @@ int qw_check(qw_ctx* ctx, void* stream) {
     QW_CUDA(cudaMemcpy(&h, ctx->err, 4, cudaMemcpyDeviceToHost));
     if (h) {
         QW_CUDA(cudaMemset(ctx->err, 0, 4));
+        if (ctx->fused) {
+            fused_reset(ctx->fused, (cudaStream_t)stream);
+            QW_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+        }
         return fail(h, h == QW_ERANGE ? "device: token id, position or page id out of range"
                        : h == QW_ETIMEOUT ? "device: a bounded wait timed out"
                                           : "device: invalid sampling parameters or too many tied logits");
@@ -502,6 +533,7 @@ int qw_debug_hidden(qw_ctx* ctx, int32_t layer, float* out, int32_t n_rows, void
     if (!ctx->hidden) return fail(QW_EINVAL, "context was created without debug_hidden");
     if (layer < 0 || layer >= ctx->cfg.n_layers) return fail(QW_EINVAL, "layer out of range");
     if (n_rows < 1 || n_rows > ctx->last_rows) return fail(QW_EINVAL, "n_rows exceeds the rows of the last call");
+    if (ctx->last_fused) return fail(QW_EINVAL, "the fused decode path keeps no per-layer residuals");
     QW_CUDA(cudaMemcpyAsync(out, ctx->hidden + (size_t)layer * ctx->max_rows * ctx->cfg.hidden,
                             (size_t)n_rows * ctx->cfg.hidden * 4, cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
     return QW_OK;
@@ -517,6 +549,13 @@ int qw_debug_gemm(const uint16_t* A, const uint16_t* B, void* C, int32_t M, int3
     GemmEpilogue e{epi == 2 ? nullptr : (float*)C, epi == 2 ? (uint16_t*)C : nullptr, epi == 2 ? N / 2 : N, nullptr,
                    split ? 1 : 0};
     QW_TRY(gemm_bf16(A, K, tb, bn, M, N, K, epi, e, (cudaStream_t)stream), "gemm launch");
+    return QW_OK;
+}
+
+int qw_debug_trace(qw_ctx* ctx, int32_t enable, uint64_t* host_out, int64_t n, int64_t* n_needed) {
+    if (!ctx) return fail(QW_EINVAL, "null context");
+    if (!ctx->fused) return fail(QW_EINVAL, "no fused decode kernel in this context");
+    QW_TRY(fused_trace(ctx->fused, enable, host_out, n, n_needed), "trace copy failed");
     return QW_OK;
 }
 

@@ -102,6 +102,11 @@ QW_DEV void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t
         : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (16-byte aligned address, size a multiple of 16).
+QW_DEV void prefetch_l2(const void* gsrc, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((uint64_t)gsrc), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------------------------ tcgen05 (5th-gen tensor core)
 // Shared-memory matrix descriptor for a K-major operand tile laid out by TMA with
 // 128-byte swizzling: rows of 128 bytes (64 bf16), 8-row core groups 1024 bytes

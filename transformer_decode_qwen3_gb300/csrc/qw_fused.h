@@ -1,16 +1,36 @@
-// Fused persistent decode for small batches (declared here, used by qw_api.cu).
+// Fused persistent decode for one sequence (declared here, used by qw_api.cu).
 #pragma once
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <vector>
 
 namespace qw {
 
 struct FusedDecode;
 
+// Device pointers into the context's packed weights.
+struct FusedWeights {
+    const uint16_t* E;
+    const float* final_norm;
+    const float* inv_freq;
+    std::vector<const uint16_t*> wqkv, wo, wgu, wd;   // wo: [hidden][n_heads*128], wd: [hidden][intermediate]
+    std::vector<const float*> in_norm, post_norm, q_norm, k_norm;
+};
+
+// nullptr when the shape or the device does not fit the fused kernel.
+FusedDecode* fused_create(const FusedWeights& w, int n_layers, int V, float eps, int hidden, int n_heads,
+                          int n_kv_heads, int intermediate);
 bool fused_supported(const FusedDecode* f, int batch);
 int fused_decode(FusedDecode* f, const int* tokens, const int* positions, int batch, uint16_t* kv_base,
                  int64_t layer_elems, int64_t page_elems, int n_pages, const int* block_tables, int bt_stride,
                  float* logits, int* err, cudaStream_t st);
+// Clear the step counters and accumulators (after a device error left them mid-step).
+int fused_reset(FusedDecode* f, cudaStream_t st);
+// Device int holding the argmax of the last fused step's logits.
+const int* fused_argmax(const FusedDecode* f);
+// Phase timestamps of the following fused steps (enable), copied out to host_out.
+int fused_trace(FusedDecode* f, int enable, uint64_t* host_out, int64_t n, int64_t* n_needed);
 void fused_destroy(FusedDecode* f);
 
 }  // namespace qw

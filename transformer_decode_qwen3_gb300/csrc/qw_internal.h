@@ -57,8 +57,10 @@ int launch_attn_prefill(const float* q, const int* positions, const int4* tiles,
                         const KvView& kv, uint16_t* out, int split, int* err, cudaStream_t st);
 int launch_attn_decode(const float* q, const int* positions, int batch, int Hq, int Hkv, const KvView& kv,
                        float* part, int max_splits, uint16_t* out, int split, int* err, int n_sm, cudaStream_t st);
+// argmax_hint (nullable, batch 1): the argmax of the logits row, already computed by the
+// fused decode; greedy rows then skip the scan.
 int launch_sample(const float* logits, int batch, int vocab, const qw_sample_params* params, uint64_t rng_counter,
-                  int32_t* out_ids, int* err, cudaStream_t st);
+                  int32_t* out_ids, const int* argmax_hint, int* err, cudaStream_t st);
 int launch_bf16_to_f32(const uint16_t* src, float* dst, int n, cudaStream_t st);
 
 }  // namespace qw

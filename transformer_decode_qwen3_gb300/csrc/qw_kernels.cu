@@ -628,7 +628,7 @@ QW_DEV T block_reduce(T v, Op op, T* scratch) {
 __global__ void __launch_bounds__(SMP_THREADS) sample_kernel(const float* __restrict__ logits, int vocab,
                                                              const qw_sample_params* __restrict__ params,
                                                              uint64_t rng_counter, int32_t* __restrict__ out,
-                                                             int* err) {
+                                                             const int* __restrict__ argmax_hint, int* err) {
     const int row = blockIdx.x, tid = threadIdx.x;
     const float* lg = logits + (size_t)row * vocab;
     const qw_sample_params P = params[row];
@@ -640,6 +640,10 @@ __global__ void __launch_bounds__(SMP_THREADS) sample_kernel(const float* __rest
     __shared__ uint32_t s_sel, s_rem, s_ncand;
     __shared__ float cum[SMP_THREADS];
 
+    if (!(P.temperature > 0.f) && argmax_hint) {
+        if (tid == 0) out[row] = argmax_hint[row];
+        return;
+    }
     if (!(P.temperature > 0.f)) {
         // greedy: pack (order key, ~index) so one max reduction picks the lowest id among equal maxima
         unsigned long long best = 0ull;
@@ -756,9 +760,9 @@ __global__ void __launch_bounds__(SMP_THREADS) sample_kernel(const float* __rest
 }
 
 int launch_sample(const float* logits, int batch, int vocab, const qw_sample_params* params, uint64_t rng_counter,
-                  int32_t* out_ids, int* err, cudaStream_t st) {
+                  int32_t* out_ids, const int* argmax_hint, int* err, cudaStream_t st) {
     if (batch <= 0) return QW_OK;
-    sample_kernel<<<batch, SMP_THREADS, 0, st>>>(logits, vocab, params, rng_counter, out_ids, err);
+    sample_kernel<<<batch, SMP_THREADS, 0, st>>>(logits, vocab, params, rng_counter, out_ids, argmax_hint, err);
     return check_launch();
 }
 
