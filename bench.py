@@ -1,18 +1,19 @@
 """Benchmark of the Qwen3-0.6B-shaped decoder pass on GB300.
 
-Default workload (one GPU): batch-1 decode after a 512-token random prompt,
-greedy, the cache growing from 512 to 512 + K positions (K = 256 covers the
-512 -> 768 range).  One timed step = one full decode step: embedding, 28 blocks,
-final norm, tied LM head and the greedy sampler, with the sampled id fed back on
-the device as the next step's token.
+Workloads (--workload; the default is the headline):
+  decode_bs1   batch-1 greedy decode after a 512-token random prompt, the cache
+               growing from 512 to 512 + K positions (K = 256 covers 512 -> 768).
+               One step = embedding, 28 blocks, final norm, tied LM head and the
+               greedy sampler, the sampled id fed back on the device.
+  decode_bs64  64 sequences over ragged synthetic caches of 128..4096 positions
+               (16-token pages), one decode step + sampling (T 0.7, top-k 50,
+               top-p 0.9, Philox seeded by sequence id) per timed step.
+  prefill      prefill of 8 x 2048 random tokens (causal), last-token logits.
+The other two workloads are also measured briefly and reported under "secondary".
 
-Also reported (secondary, same process): batch-64 decode over ragged synthetic
-caches of 128..4096 positions (sampled, T 0.7 / top-k 50 / top-p 0.9) and
-prefill of 8 x 2048 tokens.
-
-Random-init weights (seeded, N(0, 0.02)-shaped) and random token ids: no
-dataset, no checkpoint.  Inputs are larger than L2 (1.19 GB of weights per
-step), so no flush is needed between steps.
+Random-init weights (seeded, N(0, 0.02)-shaped) and random token ids: no dataset,
+no checkpoint.  Every step streams 1.19 GB of weights, more than the 129 MB L2,
+so no flush is needed between steps.
 
 --impl reference times the CPU oracle (numpy float64) on the host cores on the
 same workload and metric.
@@ -41,13 +42,23 @@ from transformer_decode_qwen3_gb300 import synth  # noqa: E402
 
 S = synth.QWEN3_0_6B
 PAGE = 16
-LAYER_WEIGHT_BYTES = 2 * (S.n_heads * S.head_dim * S.hidden + 2 * S.n_kv_heads * S.head_dim * S.hidden +
-                          S.hidden * S.n_heads * S.head_dim + 3 * S.intermediate * S.hidden)
+LAYER_PARAMS = (S.n_heads * S.head_dim * S.hidden + 2 * S.n_kv_heads * S.head_dim * S.hidden +
+                S.hidden * S.n_heads * S.head_dim + 3 * S.intermediate * S.hidden)
 NORM_BYTES = 2 * (2 * S.hidden + 2 * S.head_dim)
-WEIGHT_BYTES = S.n_layers * (LAYER_WEIGHT_BYTES + NORM_BYTES) + 2 * S.hidden + 2 * S.vocab * S.hidden
+WEIGHT_BYTES = S.n_layers * (2 * LAYER_PARAMS + NORM_BYTES) + 2 * S.hidden + 2 * S.vocab * S.hidden
 KV_BYTES_PER_POS = S.n_layers * 2 * S.n_kv_heads * S.head_dim * 2          # 114,688 B per cached position
-LINEAR_FLOP_PER_TOKEN = 2 * S.n_layers * LAYER_WEIGHT_BYTES // 2            # 2 * weights per layer stack
+KV_LAYER_BYTES_PER_POS = KV_BYTES_PER_POS // S.n_layers                     # 4,096 B
 PROMPT, PREFILL_B, PREFILL_T, BS64 = 512, 8, 2048, 64
+METRICS = {
+    "decode_bs1": "decode tok/s @bs1 (Qwen3-0.6B shape, 512-token prompt, greedy)",
+    "decode_bs64": "decode tok/s @bs64 (Qwen3-0.6B shape, ragged caches 128..4096, sampled)",
+    "prefill": "prefill tok/s (Qwen3-0.6B shape, 8 x 2048 causal)",
+}
+WORKLOAD_NAMES = {
+    "decode_bs1": "decode bs1, prompt 512, cache 512->768, greedy (configs[1])",
+    "decode_bs64": "decode bs64, ragged paged caches 128..4096, T 0.7 / top-k 50 / top-p 0.9 (configs[3])",
+    "prefill": "prefill 8 x 2048, causal GQA (configs[2])",
+}
 
 
 def peaks():
@@ -68,6 +79,7 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
+        self.out = ""
 
     def __enter__(self):
         try:
@@ -80,7 +92,6 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
-        self.out = ""
         if self.proc is not None:
             time.sleep(0.2)
             self.proc.terminate()
@@ -88,12 +99,11 @@ class ClockSampler:
                 self.out, _ = self.proc.communicate(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-                self.out = ""
 
     def summary(self):
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in (getattr(self, "out", "") or "").splitlines():
+        for line in (self.out or "").splitlines():
             f = [t.strip() for t in line.split(",")]
             if len(f) < 8:
                 continue
@@ -137,27 +147,9 @@ def max_over_ranks(world, v: float) -> float:
     return float(t.item())
 
 
-# ------------------------------------------------------------------ our path
-def bs1_decode(bd, model, K, W, world):
-    """configs[1]: prompt of 512 random ids, then greedy decode steps."""
-    n_pages = math.ceil((PROMPT + max(K, W) + 1) / PAGE) + 1
-    kv = bd.KVPool(model, n_pages)
-    bt = torch.arange(n_pages, dtype=torch.int32, device="cuda").view(1, -1)
-    ids = synth.token_ids(0, 1, PROMPT, S.vocab, device="cuda")
-    model.prefill(ids, torch.arange(PROMPT, dtype=torch.int32, device="cuda"), [0, PROMPT], kv, bt, None)
-    params = bd.sample_params([(0.0, 1, 1.0, 0)])
-    n = max(K, W)
-    toks = torch.empty(n + 1, dtype=torch.int32, device="cuda")
-    pos = torch.arange(PROMPT, PROMPT + n, dtype=torch.int32, device="cuda")
-    model.sample(params, 0, toks[0:1])
-    model.check()
-
-    def step(i):
-        model.decode_step(toks[i:i + 1], pos[i:i + 1], kv, bt, None)
-        model.sample(params, i + 1, toks[i + 1:i + 2])
-
-    for i in range(W):                       # warm-up (positions 512 .. 512+W-1, rewritten below)
-        step(i)
+def timed(fn, K, world):
+    """Run fn(i) for i < K between barriers and synchronizes; CUDA-event milliseconds and launches."""
+    from transformer_decode_qwen3_gb300 import binding as bd
     torch.cuda.synchronize()
     barrier(world)
     launches0 = bd.kernel_launches()
@@ -165,146 +157,274 @@ def bs1_decode(bd, model, K, W, world):
     torch.cuda.synchronize()
     e0.record()
     for i in range(K):
-        step(i)
+        fn(i)
     e1.record()
     torch.cuda.synchronize()
     barrier(world)
-    ms = e0.elapsed_time(e1)
-    launches = bd.kernel_launches() - launches0
-    model.check()
-    # per-step decode time alone (the forward kernels without the sampler), for the roofline
-    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    d0.record()
-    for i in range(K):
-        model.decode_step(toks[i:i + 1], pos[i:i + 1], kv, bt, None)
-    d1.record()
-    torch.cuda.synchronize()
-    decode_ms = d0.elapsed_time(d1) / K
-    # end to end through the public API with host buffers: pinned token/position in,
-    # sampled id out, every step
-    h_tok = torch.empty(1, dtype=torch.int32).pin_memory()
-    h_pos = torch.empty(1, dtype=torch.int32).pin_memory()
-    h_out = torch.empty(1, dtype=torch.int32).pin_memory()
-    d_tok = torch.empty(1, dtype=torch.int32, device="cuda")
-    d_pos = torch.empty(1, dtype=torch.int32, device="cuda")
-    d_out = torch.empty(1, dtype=torch.int32, device="cuda")
-    h_tok[0] = int(toks[0])
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for i in range(K):
-        h_pos[0] = PROMPT + i
-        d_tok.copy_(h_tok, non_blocking=True)
-        d_pos.copy_(h_pos, non_blocking=True)
-        model.decode_step(d_tok, d_pos, kv, bt, None)
-        model.sample(params, i + 1, d_out)
-        h_out.copy_(d_out, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-        h_tok[0] = int(h_out[0])
-    e2e_s = time.perf_counter() - t0
-    kv_bytes = sum((PROMPT + i + 1) * KV_BYTES_PER_POS for i in range(K)) / K
-    kv.close()
-    return {"ms": ms, "decode_ms": decode_ms, "launches": launches, "e2e_s": e2e_s,
-            "bytes_per_step": WEIGHT_BYTES + kv_bytes}
+    return e0.elapsed_time(e1), bd.kernel_launches() - launches0
 
 
-def bs64_decode(bd, model, reps=5):
-    """configs[3]: 64 sequences, ragged synthetic caches of 128..4096 positions, one sampled step."""
-    lens = synth.uniform_ints(0, synth.STREAM_LENGTHS, BS64, 128, 4096).tolist()
-    per = 4096 // PAGE + 2
-    kv = bd.KVPool(model, BS64 * per)
-    pool = kv.view()
-    bt = torch.arange(BS64 * per, dtype=torch.int32, device="cuda").view(BS64, per)
-    for s, L in enumerate(lens):
-        n_p = math.ceil(L / PAGE)
-        for layer in range(S.n_layers):
-            for which, std in ((0, 1.0), (1, 0.64)):
-                vals = synth.kv_values(0, layer, which, s * (1 << 15) * 1024, L * 1024, std, "cuda")
-                vals = torch.cat([vals.view(L, 8, 128), torch.zeros(n_p * PAGE - L, 8, 128, dtype=torch.bfloat16,
-                                                                     device="cuda")])
-                pool[layer, s * per:s * per + n_p, which] = vals.view(n_p, PAGE, 8, 128).permute(0, 2, 1, 3)
-    toks = synth.token_ids(0, 3, BS64, S.vocab, device="cuda")
-    pos = torch.tensor(lens, dtype=torch.int32, device="cuda")
-    params = bd.sample_params([(0.7, 50, 0.9, s) for s in range(BS64)])
-    out = torch.empty(BS64, dtype=torch.int32, device="cuda")
-    for _ in range(2):
-        model.decode_step(toks, pos, kv, bt, None)
-        model.sample(params, 0, out)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for r in range(reps):
-        model.decode_step(toks, pos, kv, bt, None)
-        model.sample(params, r, out)
-    e1.record()
-    torch.cuda.synchronize()
-    model.check()
-    ms = e0.elapsed_time(e1) / reps
-    kv_bytes = sum((L + 1) * KV_BYTES_PER_POS for L in lens)
-    kv.close()
-    return {"ms": ms, "tok_s": BS64 / (ms / 1e3), "bytes": WEIGHT_BYTES + kv_bytes}
+# ------------------------------------------------------------------ workloads
+class DecodeBs1:
+    """configs[1]: prompt of 512 random ids, then greedy decode steps."""
+    units_per_step = 1
+
+    def __init__(self, bd, model, n_steps):
+        self.bd, self.model = bd, model
+        self.n_pages = math.ceil((PROMPT + n_steps + 1) / PAGE) + 1
+        self.kv = bd.KVPool(model, self.n_pages)
+        self.bt = torch.arange(self.n_pages, dtype=torch.int32, device="cuda").view(1, -1)
+        ids = synth.token_ids(0, 1, PROMPT, S.vocab, device="cuda")
+        model.prefill(ids, torch.arange(PROMPT, dtype=torch.int32, device="cuda"), [0, PROMPT], self.kv, self.bt,
+                      None)
+        self.params = bd.sample_params([(0.0, 1, 1.0, 0)])
+        self.toks = torch.empty(n_steps + 1, dtype=torch.int32, device="cuda")
+        self.pos = torch.arange(PROMPT, PROMPT + n_steps, dtype=torch.int32, device="cuda")
+        model.sample(self.params, 0, self.toks[0:1])
+        model.check()
+
+    def step(self, i):
+        self.model.decode_step(self.toks[i:i + 1], self.pos[i:i + 1], self.kv, self.bt, None)
+        self.model.sample(self.params, i + 1, self.toks[i + 1:i + 2])
+
+    def kernel_only(self, i):  # the forward pass alone (the fused kernel when it is taken)
+        self.model.decode_step(self.toks[i:i + 1], self.pos[i:i + 1], self.kv, self.bt, None)
+
+    def bytes_per_step(self, K):
+        return WEIGHT_BYTES + sum((PROMPT + i + 1) * KV_BYTES_PER_POS for i in range(K)) / K
+
+    def e2e(self, K):
+        """Token and position from pinned host memory in, sampled id out, every step."""
+        h_tok = torch.empty(1, dtype=torch.int32).pin_memory()
+        h_pos = torch.empty(1, dtype=torch.int32).pin_memory()
+        h_out = torch.empty(1, dtype=torch.int32).pin_memory()
+        d_tok = torch.empty(1, dtype=torch.int32, device="cuda")
+        d_pos = torch.empty(1, dtype=torch.int32, device="cuda")
+        d_out = torch.empty(1, dtype=torch.int32, device="cuda")
+        h_tok[0] = int(self.toks[0])
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(K):
+            h_pos[0] = PROMPT + i
+            d_tok.copy_(h_tok, non_blocking=True)
+            d_pos.copy_(h_pos, non_blocking=True)
+            self.model.decode_step(d_tok, d_pos, self.kv, self.bt, None)
+            self.model.sample(self.params, i + 1, d_out)
+            h_out.copy_(d_out, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+            h_tok[0] = int(h_out[0])
+        return time.perf_counter() - t0, 8, 4
+
+    def close(self):
+        self.kv.close()
 
 
-def prefill(bd, model, reps=3):
-    """configs[2]: prefill only, 8 x 2048 random prompts."""
-    B, T = PREFILL_B, PREFILL_T
-    kv = bd.KVPool(model, B * T // PAGE)
-    bt = torch.arange(B * T // PAGE, dtype=torch.int32, device="cuda").view(B, -1)
-    ids = synth.token_ids(0, 2, B * T, S.vocab, device="cuda")
-    pos = torch.arange(T, dtype=torch.int32, device="cuda").repeat(B)
-    cu = [T * s for s in range(B + 1)]
-    last = torch.empty(B, S.vocab, device="cuda")
-    model.prefill(ids, pos, cu, kv, bt, last)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
-        model.prefill(ids, pos, cu, kv, bt, last)
-    e1.record()
-    torch.cuda.synchronize()
-    model.check()
-    ms = e0.elapsed_time(e1) / reps
-    linear = LINEAR_FLOP_PER_TOKEN * B * T
-    attn = 2 * S.n_heads * S.head_dim * T * T * S.n_layers * B
-    kv.close()
-    return {"ms": ms, "tok_s": B * T / (ms / 1e3), "linear_flop": linear, "flop": linear + attn}
+class DecodeBs64:
+    """configs[3]: 64 sequences over ragged synthetic caches, one sampled step each."""
+    units_per_step = BS64
+
+    def __init__(self, bd, model):
+        self.bd, self.model = bd, model
+        self.lens = synth.uniform_ints(0, synth.STREAM_LENGTHS, BS64, 128, 4096).tolist()
+        per = 4096 // PAGE + 2
+        self.kv = bd.KVPool(model, BS64 * per)
+        pool = self.kv.view()
+        self.bt = torch.arange(BS64 * per, dtype=torch.int32, device="cuda").view(BS64, per)
+        for s, L in enumerate(self.lens):
+            n_p = math.ceil(L / PAGE)
+            for layer in range(S.n_layers):
+                for which, std in ((0, 1.0), (1, 0.64)):
+                    v = synth.kv_values(0, layer, which, s * (1 << 15) * 1024, L * 1024, std, "cuda")
+                    v = torch.cat([v.view(L, 8, 128), torch.zeros(n_p * PAGE - L, 8, 128, dtype=torch.bfloat16,
+                                                                  device="cuda")])
+                    pool[layer, s * per:s * per + n_p, which] = v.view(n_p, PAGE, 8, 128).permute(0, 2, 1, 3)
+        self.toks = synth.token_ids(0, 3, BS64, S.vocab, device="cuda")
+        self.pos = torch.tensor(self.lens, dtype=torch.int32, device="cuda")
+        self.params = bd.sample_params([(0.7, 50, 0.9, s) for s in range(BS64)])
+        self.out = torch.empty(BS64, dtype=torch.int32, device="cuda")
+        self.q = torch.randn(BS64, S.n_heads, 128, device="cuda")
+        self.attn_out = torch.empty(BS64, S.n_heads * 128, dtype=torch.bfloat16, device="cuda")
+
+    def step(self, i):
+        self.model.decode_step(self.toks, self.pos, self.kv, self.bt, None)
+        self.model.sample(self.params, i, self.out)
+
+    def attention_only(self, i):  # the dominant kernel alone: one layer's split-KV attention
+        self.model.attn_decode(self.q, self.pos, self.kv, i % S.n_layers, self.bt, self.attn_out)
+
+    def bytes_per_step(self, K=None):
+        return WEIGHT_BYTES + sum((L + 1) * KV_BYTES_PER_POS for L in self.lens)
+
+    def attention_bytes(self):
+        return sum((L + 1) * KV_LAYER_BYTES_PER_POS for L in self.lens)
+
+    def e2e(self, K):
+        h_in = torch.empty(2, BS64, dtype=torch.int32).pin_memory()
+        h_in[0] = self.toks.cpu()
+        h_in[1] = self.pos.cpu()
+        h_out = torch.empty(BS64, dtype=torch.int32).pin_memory()
+        d_in = torch.empty(2, BS64, dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(K):
+            d_in.copy_(h_in, non_blocking=True)
+            self.model.decode_step(d_in[0], d_in[1], self.kv, self.bt, None)
+            self.model.sample(self.params, i, self.out)
+            h_out.copy_(self.out, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+        return time.perf_counter() - t0, 2 * BS64 * 4, BS64 * 4
+
+    def close(self):
+        self.kv.close()
+
+
+class Prefill:
+    """configs[2]: prefill only, 8 x 2048 random prompts, last-token logits."""
+    units_per_step = PREFILL_B * PREFILL_T
+
+    def __init__(self, bd, model):
+        self.bd, self.model = bd, model
+        B, T = PREFILL_B, PREFILL_T
+        self.kv = bd.KVPool(model, B * T // PAGE)
+        self.bt = torch.arange(B * T // PAGE, dtype=torch.int32, device="cuda").view(B, -1)
+        self.ids = synth.token_ids(0, 2, B * T, S.vocab, device="cuda")
+        self.pos = torch.arange(T, dtype=torch.int32, device="cuda").repeat(B)
+        self.cu = [T * s for s in range(B + 1)]
+        self.last = torch.empty(B, S.vocab, device="cuda")
+        self.params = bd.sample_params([(0.0, 1, 1.0, s) for s in range(B)])
+        self.out = torch.empty(B, dtype=torch.int32, device="cuda")
+
+    def step(self, i):
+        self.model.prefill(self.ids, self.pos, self.cu, self.kv, self.bt, self.last)
+
+    def flops(self):
+        B, T = PREFILL_B, PREFILL_T
+        linear = 2 * LAYER_PARAMS * S.n_layers * B * T
+        attn = 2 * S.n_heads * S.head_dim * T * T * S.n_layers * B      # causal: half of 4 H d T^2
+        head = 2 * S.hidden * S.vocab * B
+        return linear, attn, head
+
+    def e2e(self, K):
+        B, T = PREFILL_B, PREFILL_T
+        h_in = torch.empty(2, B * T, dtype=torch.int32).pin_memory()
+        h_in[0] = self.ids.cpu()
+        h_in[1] = self.pos.cpu()
+        h_out = torch.empty(B, dtype=torch.int32).pin_memory()
+        d_in = torch.empty(2, B * T, dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(K):
+            d_in.copy_(h_in, non_blocking=True)
+            self.model.prefill(d_in[0], d_in[1], self.cu, self.kv, self.bt, self.last)
+            self.model.sample(self.params, 0, self.out, logits=self.last)
+            h_out.copy_(self.out, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+        return time.perf_counter() - t0, 2 * B * T * 4, B * 4
+
+    def close(self):
+        self.kv.close()
 
 
 # ------------------------------------------------------------------ CPU oracle
-def oracle_decode_rate(max_seconds=20.0, min_steps=2):
-    """Oracle decode steps per second at batch 1 after the 512-token prompt (prefill not timed)."""
+def oracle_rate(workload: str, max_seconds=15.0):
+    """The oracle, unmodified, on a bounded sample of the workload; (units/s, sample text)."""
     import numpy as np
     from oracle import qwen3_ref as R
     w = synth.make_weights(S)
     orc = R.Qwen3Oracle(w, S)
+    if workload == "prefill":
+        T = 256                         # a 256-token prefix of sequence 0
+        ids = synth.token_ids(0, 2, T, S.vocab).numpy()
+        t0 = time.perf_counter()
+        orc.forward(ids, np.arange(T), orc.new_cache(), last_only=True)
+        dt = time.perf_counter() - t0
+        return T / dt, f"prefill of the first {T} tokens of one 2048-token sequence ({dt:.1f} s)"
+    if workload == "decode_bs64":
+        lens = synth.uniform_ints(0, synth.STREAM_LENGTHS, BS64, 128, 4096).tolist()
+        toks = synth.token_ids(0, 3, BS64, S.vocab)
+        t0 = time.perf_counter()
+        n = 0
+        while n < 2 or (time.perf_counter() - t0 < max_seconds and n < BS64):
+            cache = [None] * S.n_layers
+            for layer in range(S.n_layers):
+                per_tok = S.n_kv_heads * 128
+                k = synth.kv_values(0, layer, 0, n * (1 << 15) * per_tok, lens[n] * per_tok, 1.0)
+                v = synth.kv_values(0, layer, 1, n * (1 << 15) * per_tok, lens[n] * per_tok, 0.64)
+                cache[layer] = R.LayerCache(R.bf16_to_f64(k).reshape(lens[n], 8, 128).transpose(1, 0, 2),
+                                            R.bf16_to_f64(v).reshape(lens[n], 8, 128).transpose(1, 0, 2),
+                                            np.arange(lens[n]))
+            logits = orc.forward([int(toks[n])], [lens[n]], cache, last_only=True)
+            R.sample(logits[0], 0.7, 50, 0.9, R.sampling_uniform(n, 0))
+            n += 1
+        dt = time.perf_counter() - t0
+        return n / dt, f"{n} of the 64 sequences, one sampled decode step each ({dt:.1f} s, cache set-up included)"
     ids = synth.token_ids(0, 1, PROMPT, S.vocab).numpy()
     cache = orc.new_cache()
     logits = orc.forward(ids, np.arange(PROMPT), cache, last_only=True)
     tok = int(np.argmax(logits[0]))
     t0 = time.perf_counter()
     n = 0
-    while n < min_steps or time.perf_counter() - t0 < max_seconds:
+    while n < 2 or time.perf_counter() - t0 < max_seconds:
         logits = orc.forward([tok], [PROMPT + n], cache, last_only=True)
         tok = int(np.argmax(logits[0]))
         n += 1
     dt = time.perf_counter() - t0
-    return {"value": n / dt, "steps": n, "seconds": dt}
+    return n / dt, f"{n} batch-1 decode steps after the 512-token prompt ({dt:.1f} s; prefill untimed)"
 
 
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    r = oracle_decode_rate(max_seconds=max(5.0, 2.0 * args.steps / 64))
-    cores = os.cpu_count()
-    line = {"metric": "decode tok/s @bs1 (Qwen3-0.6B shape, 512-token prompt, greedy)", "value": r["value"],
-            "unit": "tok/s", "n_gpus": args.gpus, "steps": r["steps"], "warmup": 0,
-            "ms_per_step": 1e3 / r["value"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "f64", "data": "synthetic (seeded random-init weights and token ids)", "impl": "reference",
-            "config": {"workload": "decode bs1, prompt 512, cache 512->768, greedy", "global_batch": 1,
-                       "seq_len": PROMPT},
-            "cpu_baseline": {"value": r["value"], "unit": "tok/s", "cores": cores, "kind": "oracle",
-                             "sample": f"{r['steps']} decode steps after the 512-token prompt ({r['seconds']:.1f} s)"},
-            "e2e": {"value": r["value"], "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    v, sample = oracle_rate(args.workload, max_seconds=max(5.0, min(60.0, 0.25 * args.steps)))
+    unit = "tok/s"
+    line = {"metric": METRICS[args.workload], "value": v, "unit": unit, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded random-init weights and token ids)",
+            "impl": "reference", "config": {"workload": WORKLOAD_NAMES[args.workload]},
+            "cpu_baseline": {"value": v, "unit": unit, "cores": os.cpu_count(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ main
+def measure(name, bd, model, K, W, world, hbm, tf_burst):
+    """Returns the JSON fields of one workload measured with K timed steps after W warm-ups."""
+    if name == "decode_bs1":
+        wl = DecodeBs1(bd, model, max(K, W))
+    elif name == "decode_bs64":
+        wl = DecodeBs64(bd, model)
+    else:
+        wl = Prefill(bd, model)
+    for i in range(W):
+        wl.step(i)
+    ms, launches = timed(wl.step, K, world)
+    ms = max_over_ranks(world, ms)
+    out = {"ms_per_step": ms / K, "value": world * wl.units_per_step * K / (ms / 1e3), "gpu_launches": launches}
+    if name == "decode_bs1":
+        kms, _ = timed(wl.kernel_only, K, world)
+        ach = wl.bytes_per_step(K) / (kms / K / 1e3) / 1e9
+        out["roofline"] = {"bound": "hbm", "kernel": "decode step (the fused batch-1 kernel)", "achieved": ach,
+                           "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": None,
+                           "algorithmic_bytes": wl.bytes_per_step(K), "kernel_ms": kms / K}
+    elif name == "decode_bs64":
+        kms, _ = timed(wl.attention_only, K, world)
+        ach = wl.attention_bytes() / (kms / K / 1e3) / 1e9
+        out["roofline"] = {"bound": "hbm", "kernel": "split-KV decode attention (one layer)", "achieved": ach,
+                           "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": None,
+                           "algorithmic_bytes": wl.attention_bytes(), "kernel_ms": kms / K,
+                           "step_hbm_frac": wl.bytes_per_step() / (ms / K / 1e3) / 1e9 / hbm}
+    else:
+        lin, attn, head = wl.flops()
+        ach = (lin + attn + head) / (ms / K / 1e3) / 1e12
+        out["roofline"] = {"bound": "tensor", "kernel": "prefill step (GEMMs + attention)", "achieved": ach,
+                           "peak": tf_burst, "unit": "TFLOP/s", "frac": ach / tf_burst, "traffic": None,
+                           "algorithmic_flop": lin + attn + head,
+                           "linear_frac_of_peak": lin / (ms / K / 1e3) / 1e12 / tf_burst}
+    e2e_s, h2d, d2h = wl.e2e(K)
+    out["e2e"] = {"value": world * wl.units_per_step * K / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": h2d,
+                  "d2h_bytes_per_step": d2h}
+    wl.close()
+    return out
 
 
 def main():
@@ -312,8 +432,9 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=256)
     ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--workload", default="decode_bs1", choices=list(METRICS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-secondary", action="store_true", help="skip the batch-64 decode and prefill numbers")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the other two workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -331,42 +452,30 @@ def main():
     del w
     torch.cuda.empty_cache()
     with ClockSampler(torch.cuda.current_device()) as clk:
-        r = bs1_decode(bd, model, args.steps, args.warmup, world)
-    ms_max = max_over_ranks(world, r["ms"])
-    value = world * args.steps / (ms_max / 1e3)
-    achieved = r["bytes_per_step"] / (r["decode_ms"] / 1e3) / 1e9
-    line = {
-        "metric": "decode tok/s @bs1 (Qwen3-0.6B shape, 512-token prompt, greedy)",
-        "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic (seeded random-init bf16 weights and token ids)",
-        "config": {"workload": "decode bs1, prompt 512, cache 512->768, greedy (configs[1])", "global_batch": world,
-                   "seq_len": PROMPT, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (1.19 GB of weights streamed per step)"},
-        "roofline": {"bound": "hbm", "kernel": "decode step (all forward kernels)",
-                     "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                     "peak_kind": f"{peak_kind} copy bandwidth", "traffic": None,
-                     "bytes_per_step": r["bytes_per_step"]},
-        "e2e": {"value": world * args.steps / r["e2e_s"], "unit": "tok/s", "h2d_bytes_per_step": 8,
-                "d2h_bytes_per_step": 4},
-        "gpu_launches": r["launches"],
-        "clocks": clk.summary(),
-    }
+        m = measure(args.workload, bd, model, args.steps, args.warmup, world, hbm, tf_burst)
+    m["roofline"]["peak_kind"] = f"{peak_kind} ({'copy bandwidth' if m['roofline']['unit'] == 'GB/s' else 'bf16 burst'})"
+    line = {"metric": METRICS[args.workload], "value": m["value"], "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded random-init bf16 weights and token ids)",
+            "config": {"workload": WORKLOAD_NAMES[args.workload], "global_batch": world *
+                       {"decode_bs1": 1, "decode_bs64": BS64, "prefill": PREFILL_B}[args.workload],
+                       "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2 (1.19 GB of weights streamed per step)"},
+            "roofline": m["roofline"], "e2e": m["e2e"], "gpu_launches": m["gpu_launches"], "clocks": clk.summary()}
     if not args.no_secondary and rank == 0:
-        b64 = bs64_decode(bd, model)
-        pf = prefill(bd, model)
-        line["secondary"] = {
-            "decode_bs64": {"tok_s": b64["tok_s"], "ms_per_step": b64["ms"], "workload": "configs[3]",
-                            "hbm_frac": b64["bytes"] / (b64["ms"] / 1e3) / 1e9 / hbm},
-            "prefill_8x2048": {"tok_s": pf["tok_s"], "ms": pf["ms"], "workload": "configs[2]",
-                               "tflops": pf["flop"] / (pf["ms"] / 1e3) / 1e12,
-                               "tensor_frac_linear_of_burst": pf["linear_flop"] / (pf["ms"] / 1e3) / 1e12 / tf_burst},
-        }
+        sec = {}
+        for name in METRICS:
+            if name == args.workload:
+                continue
+            r = measure(name, bd, model, 5 if name != "decode_bs1" else 64, 3, 1, hbm, tf_burst)
+            sec[name] = {"tok_s": r["value"], "ms_per_step": r["ms_per_step"], "roofline": r["roofline"],
+                         "e2e_tok_s": r["e2e"]["value"]}
+        line["secondary"] = sec
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cb = oracle_decode_rate(max_seconds=15.0)
-        line["cpu_baseline"] = {"value": cb["value"], "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
-                                "sample": f"{cb['steps']} batch-1 decode steps after the 512-token prompt "
-                                          f"({cb['seconds']:.1f} s; prefill untimed)"}
+        v, sample = oracle_rate(args.workload)
+        line["cpu_baseline"] = {"value": v, "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": sample}
     if rank == 0:
         print(json.dumps(line), flush=True)
     model.close()

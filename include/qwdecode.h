@@ -241,6 +241,10 @@ int qw_debug_gemm(const uint16_t* A, const uint16_t* B, void* C, int32_t M, int3
  * begin/end and done).  *n_needed receives the buffer length.  Synchronous. */
 int qw_debug_trace(qw_ctx* ctx, int32_t enable, uint64_t* host_out, int64_t n, int64_t* n_needed);
 
+/* Select the prefill attention kernel: 0 = tcgen05/TMEM flash kernel (default),
+ * 1 = mma.sync flash kernel.  For comparisons in tests. */
+int qw_set_prefill_attention(qw_ctx* ctx, int32_t variant);
+
 /* Number of kernels this library has launched in the process so far (all contexts). */
 uint64_t qw_kernel_launches(void);
 

@@ -155,3 +155,26 @@ def test_device_errors_are_reported_and_the_context_survives(small):
     assert model.check_code() == bd.QW_OK
     with pytest.raises(bd.QwError):                                   # empty sequence: rejected on the host
         model.prefill(one(3), one(0), [0, 0], kv, bt, logits)
+
+
+@pytest.mark.parametrize("variant", [0, 1])
+def test_prefill_attention_kernels_match_oracle(small, variant):
+    """The tcgen05 flash kernel (0) and the mma.sync one (1), ragged lengths across tile edges."""
+    bd, w, model, orc = small
+    lens = [1, 63, 65, 127, 129, 100]         # 485 tokens <= max_tokens; 1 and 2 key tiles, ragged q tiles
+    cap = 144
+    n_pages = len(lens) * (cap // Q.PAGE)
+    kv = bd.KVPool(model, n_pages)
+    bt_np, _ = Q.block_tables(lens, cap, n_pages, seed=3)
+    ids, pos, cu = _prefill_inputs(lens, call=9)
+    last = torch.empty(len(lens), S.vocab, device="cuda")
+    model.set_prefill_attention(variant)
+    try:
+        model.prefill(ids.cuda(), pos.cuda(), cu, kv, torch.from_numpy(bt_np).cuda(), last)
+        model.check()
+    finally:
+        model.set_prefill_attention(0)
+    for s, L in enumerate(lens):
+        ref = orc.forward(ids[cu[s]:cu[s + 1]].numpy(), np.arange(L), orc.new_cache(), last_only=True)
+        err = Q.rel_l2_rows(last[s:s + 1].cpu().numpy(), ref)
+        assert err.max() < Q.LOGIT_TOL, f"variant {variant} seq {s} (L={L}): {err.max():.2e}"

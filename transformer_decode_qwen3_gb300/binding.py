@@ -26,7 +26,8 @@ QW_MAX_TOP_K = 1024
 
 EXPORTED = ["qw_config_default", "qw_init", "qw_destroy", "qw_kv_create", "qw_kv_destroy", "qw_kv_layout",
             "qw_prefill", "qw_decode_step", "qw_sample", "qw_check", "qw_last_error_message",
-            "qw_debug_hidden", "qw_set_decode_path", "qw_debug_gemm", "qw_kernel_launches", "qw_attn_decode", "qw_attn_decode_noalloc", "qw_debug_trace"]
+            "qw_debug_hidden", "qw_set_decode_path", "qw_debug_gemm", "qw_kernel_launches", "qw_attn_decode", "qw_attn_decode_noalloc", "qw_debug_trace",
+            "qw_set_prefill_attention"]
 
 
 class QwConfig(ctypes.Structure):
@@ -91,6 +92,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qw_attn_decode.argtypes = [vp, vp, vp, i32, vp, i32, vp, i32, vp, vp]
     lib.qw_attn_decode_noalloc.argtypes = [vp, vp, i32, i32, i32, vp, i32, vp, i32, vp, vp]
     lib.qw_debug_trace.argtypes = [vp, i32, vp, i64, ctypes.POINTER(i64)]
+    lib.qw_set_prefill_attention.argtypes = [vp, i32]
     lib.qw_kernel_launches.argtypes = []
     lib.qw_kernel_launches.restype = ctypes.c_uint64
     for name in EXPORTED:
@@ -183,6 +185,9 @@ class Model:
             self.close()
         except Exception:
             pass
+
+    def set_prefill_attention(self, variant: int):
+        _check(_lib.qw_set_prefill_attention(self.handle, variant), "qw_set_prefill_attention")
 
     def set_decode_path(self, path: int):
         _check(_lib.qw_set_decode_path(self.handle, path), "qw_set_decode_path")

@@ -60,12 +60,13 @@ struct qw_ctx {
     // workspaces
     uint8_t* wsbuf = nullptr;
     float *x = nullptr, *qkv = nullptr, *q = nullptr, *logits = nullptr, *part = nullptr, *hidden = nullptr;
-    uint16_t *h = nullptr, *attn = nullptr, *act = nullptr;
+    uint16_t *h = nullptr, *attn = nullptr, *act = nullptr, *q_bf16 = nullptr;
     int *tok_seq = nullptr, *iota = nullptr, *rows_last = nullptr, *err = nullptr;
     int4* tiles = nullptr;
     int max_rows = 0, max_splits = 128, max_tiles = 0;
     int last_rows = 0, logits_rows = 0;
     int decode_path = 0;
+    int prefill_attn = 0;   // 0: tcgen05 kernel, 1: mma.sync kernel
     FusedDecode* fused = nullptr;
     bool last_fused = false;   // the last decode step ran the fused kernel (its argmax is valid)
 };
@@ -262,6 +263,7 @@ int qw_init(const qw_config* cfg, const qw_weights* w, qw_ctx** out) {
     const size_t ox = take((size_t)T * D * 4);
     const size_t oqkv = take((size_t)T * ctx->qkv_dim * 4);
     const size_t oq = take((size_t)T * ctx->attn_dim * 4);
+    const size_t oqb = take((size_t)T * ctx->attn_dim * 2);
     const size_t ologits = take((size_t)c.max_batch * V * 4);
     const size_t opart = take((size_t)c.max_batch * Hq * ctx->max_splits * (d + 2) * 4);
     const size_t oh = take((size_t)TA * D * 2);
@@ -281,6 +283,7 @@ int qw_init(const qw_config* cfg, const qw_weights* w, qw_ctx** out) {
     ctx->x = (float*)(W + ox);
     ctx->qkv = (float*)(W + oqkv);
     ctx->q = (float*)(W + oq);
+    ctx->q_bf16 = (uint16_t*)(W + oqb);
     ctx->logits = (float*)(W + ologits);
     ctx->part = (float*)(W + opart);
     ctx->h = (uint16_t*)(W + oh);
@@ -340,6 +343,11 @@ int qw_kv_create(qw_ctx* ctx, int32_t n_pages, qw_kv** out) {
     if (bytes + ((size_t)256 << 20) > free_b) return fail(QW_EKVFULL, "KV pool larger than free device memory");
     void* p = nullptr;
     if (cudaMalloc(&p, bytes) != cudaSuccess) return fail(QW_ENOMEM, "KV pool allocation failed");
+    // zeroed once: slots never written hold finite values, so masked keys contribute exactly 0
+    if (cudaMemset(p, 0, bytes) != cudaSuccess) {
+        cudaFree(p);
+        return fail(QW_ECUDA, "KV pool clear failed");
+    }
     qw_kv* kv = new qw_kv{ctx, (uint16_t*)p, n_pages, page_elems, (int64_t)n_pages * page_elems};
     *out = kv;
     return QW_OK;
@@ -379,10 +387,15 @@ static int run_layers(qw_ctx* ctx, int n, const int* ids, const int* positions, 
                "rmsnorm launch");
         GemmEpilogue e{ctx->qkv, nullptr, ctx->qkv_dim, ctx->err, split};
         QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_qkv, 256, n, ctx->qkv_dim, D, EPI_STORE_F32, e, st), "qkv gemm");
+        const bool tc_attn = mode == 0 && ctx->prefill_attn == 0;
         QW_TRY(launch_qkv_post(ctx->qkv, n, positions, tok_seq, Hq, Hkv, Lw.q_norm, Lw.k_norm, ctx->inv_freq,
-                               c.rms_eps, ctx->q, kvv, ctx->err, st),
+                               c.rms_eps, ctx->q, tc_attn ? ctx->q_bf16 : nullptr, kvv, ctx->err, st),
                "qk-norm/rope/kv-write launch");
-        if (mode == 0)
+        if (tc_attn)
+            QW_TRY(launch_attn_prefill_tc(ctx->q_bf16, n, positions, ctx->tiles, n_tiles, Hq, Hkv, kvv, ctx->attn,
+                                          split, ctx->err, st),
+                   "prefill attention launch");
+        else if (mode == 0)
             QW_TRY(launch_attn_prefill(ctx->q, positions, ctx->tiles, n_tiles, Hq, Hkv, kvv, ctx->attn, split,
                                        ctx->err, st),
                    "prefill attention launch");
@@ -556,6 +569,12 @@ int qw_debug_trace(qw_ctx* ctx, int32_t enable, uint64_t* host_out, int64_t n, i
     if (!ctx) return fail(QW_EINVAL, "null context");
     if (!ctx->fused) return fail(QW_EINVAL, "no fused decode kernel in this context");
     QW_TRY(fused_trace(ctx->fused, enable, host_out, n, n_needed), "trace copy failed");
+    return QW_OK;
+}
+
+int qw_set_prefill_attention(qw_ctx* ctx, int32_t variant) {
+    if (!ctx || variant < 0 || variant > 1) return fail(QW_EINVAL, "qw_set_prefill_attention: bad argument");
+    ctx->prefill_attn = variant;
     return QW_OK;
 }
 

@@ -1,0 +1,418 @@
+// Causal prefill attention of the article's Step 5 on the 5th-generation tensor core.
+//
+// One CTA takes 64 consecutive query positions of one sequence and one KV head g:
+// its 128 MMA rows are those positions for query head 2g (rows 0..63) and 2g+1
+// (rows 64..127), which share the KV head (grouped-query attention).  Keys and
+// values stream from the paged cache in tiles of 64 positions (4 pages), loaded by
+// TMA through a 4-D view of the pool ([page][K/V, head][slot][dim], 16-slot boxes,
+// 128-byte swizzle) into a 4-deep ring, so loads run three tiles ahead.
+//
+//   warp 0      TMA producer (Q once, then K/V tiles)
+//   warp 1      MMA issuer: S_j = Q K_j^T into one of two TMEM buffers, then
+//               O += P_j V_j (V as an MN-major operand) into a TMEM accumulator
+//   warps 2..5  softmax: thread = row; reads S_j from TMEM, masks keys beyond the
+//               row's position, keeps the running max m and sum l, rescales O in
+//               TMEM when m grows, writes P_j (bf16) to shared memory
+// Scores are in log2 units (scale 1/sqrt(128) * log2 e); the output is O / l.
+#include <cudaTypedefs.h>
+
+#include "qw_common.cuh"
+#include "qw_internal.h"
+
+namespace qw {
+namespace fa {
+
+constexpr int BM = 128, BN = 64, HD = 128;
+constexpr int CHUNK = 128 * 64 * 2;           // 128 rows x 64 bf16, one 128-byte-swizzle column block
+constexpr int KCHUNK = BN * 64 * 2;           // 64 keys x 64 dims: one column block of a K or V tile
+constexpr int Q_BYTES = 2 * CHUNK;            // 32 KB
+constexpr int KV_STAGES = 4;
+constexpr int KV_STAGE = 4 * KCHUNK;          // K (2 blocks) + V (2 blocks) = 32 KB
+constexpr int P_BYTES = BM * BN * 2;          // 16 KB: one 64-key block
+constexpr int SMEM = Q_BYTES + KV_STAGES * KV_STAGE + P_BYTES + 1024 + 256;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 256;           // S0 [0,64), S1 [64,128), O [128,256)
+
+// Instruction descriptor: bf16 x bf16 -> f32, M = 128, N = 128, A K-major, B K-major
+// (S = Q K^T) or B MN-major (bit 16: O += P V with V stored [key][dim]).
+constexpr uint32_t IDESC_S = umma_idesc_bf16(BM, BN);
+constexpr uint32_t IDESC_PV = umma_idesc_bf16(BM, HD) | (1u << 16);
+
+// MN-major operand with 128-byte swizzle: 8 K-rows of 128 bytes (64 MN elements) per
+// atom; LBO = byte stride between atoms along MN, SBO = between 8-row groups along K.
+QW_DEV uint64_t desc_mn_sw128(uint32_t smem_addr, uint32_t lbo_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+QW_DEV void tma_load_4d(void* smem_dst, const CUtensorMap* m, int c0, int c1, int c2, int c3, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+        "[%6];" ::"r"(smem_u32(smem_dst)),
+        "l"((uint64_t)m), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// 32 lanes x 32 columns into v[0..31]; completes at the next tmem_wait_ld().
+QW_DEV void tmem_ld32_nowait(uint32_t taddr, float* v) {
+    uint32_t* r = (uint32_t*)v;
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+QW_DEV void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// v[0..31] into 32 lanes x 32 columns; complete with tcgen05.wait::st.
+QW_DEV void tmem_st32_nowait(uint32_t taddr, const float* v) {
+    const uint32_t* r = (const uint32_t*)v;
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+QW_DEV int split_dst(int m) { return (m >> 6) * 128 + (m & 63); }
+
+// 2^x on the special-function unit (relative error ~2^-22; P is rounded to bf16 next)
+QW_DEV float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
+                           const int* __restrict__ positions, const int4* __restrict__ tiles,
+                           const int* __restrict__ block_tables, int bt_stride, int n_pages, int Hq, int Hkv,
+                           uint16_t* __restrict__ out, float scale_log2, int split, int* err) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* sQ = sm;
+    uint8_t* sKV = sm + Q_BYTES;                       // stage s: K blocks at s*KV_STAGE, V blocks at +2*KCHUNK
+    uint8_t* sP = sm + Q_BYTES + KV_STAGES * KV_STAGE;
+    uint64_t* bars = (uint64_t*)(sP + P_BYTES);
+    uint64_t* q_full = bars;
+    uint64_t* kv_full = bars + 1;                  // [KV_STAGES]
+    uint64_t* kv_empty = kv_full + KV_STAGES;      // [KV_STAGES]
+    uint64_t* s_full = kv_empty + KV_STAGES;       // [2]
+    uint64_t* p_full = s_full + 2;
+    uint64_t* o_done = p_full + 1;
+    uint32_t* tmem_slot = (uint32_t*)(o_done + 1);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+
+    // a CTA of this launch already gave up on a wait: end quickly instead of timing out again
+    if (err && *(volatile int*)err == QW_ETIMEOUT) return;
+    const int4 tile = tiles[blockIdx.x];
+    const int seq = tile.x, row0 = tile.y, nrows = tile.z;
+    const int g = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pmax = positions[row0 + nrows - 1];
+    const int nt = pmax < 0 ? 0 : pmax / BN + 1;
+    const int* bt = block_tables + (size_t)seq * bt_stride;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < KV_STAGES; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) mbar_init(&s_full[s], 1);
+        mbar_init(p_full, 4);
+        mbar_init(o_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmKV);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (nt > 0) {
+            // the whole warp runs the producer loop: lanes look up one page id each, lane 0 issues
+            constexpr int PPT = BN / QW_PAGE_SIZE;  // pages per key tile
+            auto page_of = [&](int j) {
+                const int pidx = j * PPT + (lane & (PPT - 1));
+                int page = pidx < bt_stride ? __ldg(bt + pidx) : -1;
+                if (page < 0 || page >= n_pages) {
+                    if (lane < PPT && pidx * QW_PAGE_SIZE <= pmax) set_error(err, QW_ERANGE);
+                    page = n_pages;  // out of the tensor map: TMA fills zeros
+                }
+                return page;
+            };
+            if (lane == 0) {
+                // Q: rows 0..63 = head 2g, rows 64..127 = head 2g+1, two 64-dim blocks each
+                mbar_arrive_expect_tx(q_full, Q_BYTES);
+                for (int hh = 0; hh < 2; ++hh)
+                    for (int c = 0; c < 2; ++c)
+                        tma_load_2d(sQ + c * CHUNK + hh * (CHUNK / 2), &tmQ, (2 * g + hh) * HD + 64 * c, row0,
+                                    q_full);
+            }
+            int next_page = page_of(0);
+            for (int j = 0; j < nt; ++j) {
+                const int s = j % KV_STAGES;
+                const int my_page = next_page;
+                if (j + 1 < nt) next_page = page_of(j + 1);   // in flight while this tile waits
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait(&kv_empty[s], ((j / KV_STAGES) & 1) ^ 1, err) && !*abort_flag;
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) {
+                    if (lane == 0) *abort_flag = 1;
+                    break;
+                }
+                uint8_t* st = sKV + s * KV_STAGE;
+                if (lane == 0) mbar_arrive_expect_tx(&kv_full[s], KV_STAGE);
+                for (int pi = 0; pi < PPT; ++pi) {
+                    const int page = __shfl_sync(0xffffffffu, my_page, pi);
+                    if (lane == 0) {
+                        for (int c = 0; c < 2; ++c) {
+                            tma_load_4d(st + c * KCHUNK + pi * QW_PAGE_SIZE * 128, &tmKV, 64 * c, 0, g, page,
+                                        &kv_full[s]);
+                            tma_load_4d(st + (2 + c) * KCHUNK + pi * QW_PAGE_SIZE * 128, &tmKV, 64 * c, 0, Hkv + g,
+                                        page, &kv_full[s]);
+                        }
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && nt > 0) {
+            const uint32_t aq = smem_u32(sQ), ap = smem_u32(sP);
+            bool ok = mbar_wait(q_full, 0, err);
+            auto issue_s = [&](int j) {
+                const uint32_t k0 = smem_u32(sKV + (j % KV_STAGES) * KV_STAGE);
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint32_t qoff = (kk >> 2) * CHUNK + (kk & 3) * 32;
+                    const uint32_t koff = (kk >> 2) * KCHUNK + (kk & 3) * 32;
+                    umma_bf16(tmem + (j & 1) * BN, umma_desc_sw128(aq + qoff), umma_desc_sw128(k0 + koff), IDESC_S,
+                              kk != 0);
+                }
+                umma_commit(&s_full[j & 1]);
+            };
+            if (ok) ok = mbar_wait(&kv_full[0], 0, err);
+            if (ok) {
+                tc_fence_after();
+                issue_s(0);
+            }
+            for (int j = 0; j < nt && ok; ++j) {
+                if (j + 1 < nt) {
+                    if (!mbar_wait(&kv_full[(j + 1) % KV_STAGES], ((j + 1) / KV_STAGES) & 1, err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    issue_s(j + 1);
+                }
+                if (!mbar_wait(p_full, j & 1, err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t v0 = smem_u32(sKV + (j % KV_STAGES) * KV_STAGE + 2 * KCHUNK);
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    // A = P (K-major, keys 16 kk ..), B = V (MN-major: keys 16 kk .. are rows 16 kk ..)
+                    umma_bf16(tmem + 2 * BN, umma_desc_sw128(ap + kk * 32), desc_mn_sw128(v0 + kk * 16 * 128, KCHUNK),
+                              IDESC_PV, (j | kk) != 0);
+                }
+                umma_commit(o_done);
+                umma_commit(&kv_empty[j % KV_STAGES]);
+            }
+            if (!ok) {
+                *abort_flag = 1;
+                // release the softmax warps
+                for (int s = 0; s < 2; ++s) mbar_arrive(&s_full[s]);
+                mbar_arrive(o_done);
+            }
+        }
+    } else {
+        // softmax warps 2..5: TMEM lane group (warp % 4), thread = row
+        const int r = 32 * (warp & 3) + lane;
+        const int hh = r >> 6, ri = r & 63;
+        const int qp = ri < nrows ? positions[row0 + ri] : -1;
+        const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+        float m = -INFINITY, l = 0.f;
+        for (int j = 0; j < nt; ++j) {
+            if (!mbar_wait(&s_full[j & 1], (j >> 1) & 1, err) || *abort_flag) break;
+            tc_fence_after();
+            // S row: four 32-column TMEM loads in flight, one wait
+            const uint32_t sbase = tmem + (j & 1) * BN + lane_off;
+            const int kbase = j * BN;
+            const bool full_tile = kbase + BN - 1 <= qp;     // no key of this tile is masked for this row
+            float sv[BN];
+            tmem_ld32_nowait(sbase + 0, sv + 0);
+            tmem_ld32_nowait(sbase + 32, sv + 32);
+            tmem_wait_ld();
+            float rmax = -INFINITY;
+            if (full_tile) {
+#pragma unroll
+                for (int i = 0; i < BN; ++i) rmax = fmaxf(rmax, sv[i]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < BN; ++i) {
+                    if (kbase + i > qp) sv[i] = -INFINITY;
+                    rmax = fmaxf(rmax, sv[i]);
+                }
+            }
+            // Lazy reference max: m moves (and O is rescaled) only when the tile's max exceeds it by
+            // more than 8 (log2 units), so P <= 2^8; O and l share the reference, so O / l is exact.
+            const float cand = rmax * scale_log2;
+            float alpha = 1.f;
+            if (cand > m + 8.f) {
+                alpha = m == -INFINITY ? 0.f : ex2_approx(m - cand);
+                m = cand;
+            }
+            const float neg = m == -INFINITY ? 0.f : -m;
+            // P_j may overwrite P_{j-1} and O may be rescaled once P_{j-1} V_{j-1} is done
+            if (j > 0) {
+                if (!mbar_wait(o_done, (j - 1) & 1, err) || *abort_flag) break;
+                tc_fence_after();
+                // tcgen05.ld/st are warp-collective: rescale when any row of the warp needs it
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+                    for (int half = 0; half < 2; ++half) {  // 64 columns at a time (registers: S is live)
+                        float o[64];
+                        const uint32_t ob = tmem + 2 * BN + lane_off + 64 * half;
+                        tmem_ld32_nowait(ob + 0, o + 0);
+                        tmem_ld32_nowait(ob + 32, o + 32);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) o[i] *= alpha;
+                        tmem_st32_nowait(ob + 0, o + 0);
+                        tmem_st32_nowait(ob + 32, o + 32);
+                        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                    }
+                }
+            }
+            // p = 2^(s * scale - m), row sum, P row r as bf16 in the 128-byte-swizzled layout
+            float sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < BN; ++i) {
+                sv[i] = sv[i] == -INFINITY ? 0.f : ex2_approx(fmaf(sv[i], scale_log2, neg));
+                sum += sv[i];
+            }
+#pragma unroll
+            for (int unit = 0; unit < BN / 8; ++unit) {   // 16-byte units of the row's 128 bytes
+                const float* p8 = sv + 8 * unit;
+                const uint4 w = make_uint4(pack_bf16x2(p8[0], p8[1]), pack_bf16x2(p8[2], p8[3]),
+                                           pack_bf16x2(p8[4], p8[5]), pack_bf16x2(p8[6], p8[7]));
+                *(uint4*)(sP + r * 128 + ((unit ^ (r & 7)) << 4)) = w;
+            }
+            l = l * alpha + sum;
+            fence_proxy_async();   // the MMA reads P through the async proxy
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+        }
+        if (nt > 0 && !*abort_flag && mbar_wait(o_done, (nt - 1) & 1, err)) {
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const size_t ld = (size_t)Hq * HD;
+            const int h = 2 * g + hh;
+#pragma unroll 1
+            for (int c = 0; c < HD / 32; ++c) {
+                float o[32];
+                tmem_ld32(tmem + 2 * BN + lane_off + 32 * c, o);
+                if (ri < nrows) {
+                    const int row = row0 + ri;
+                    uint32_t hi[16], lo[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        hi[i] = pack_bf16x2(o[2 * i] * inv, o[2 * i + 1] * inv);
+                        lo[i] = pack_bf16x2(o[2 * i] * inv - bf16_lo(hi[i]), o[2 * i + 1] * inv - bf16_hi(hi[i]));
+                    }
+                    const int dst_row = split ? split_dst(row) : row;
+                    uint4* dst = (uint4*)(out + (size_t)dst_row * ld + h * HD + 32 * c);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hi[4 * i], hi[4 * i + 1], hi[4 * i + 2], hi[4 * i + 3]);
+                    if (split) {
+                        uint4* dl = (uint4*)(out + (size_t)(dst_row + 64) * ld + h * HD + 32 * c);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            dl[i] = make_uint4(lo[4 * i], lo[4 * i + 1], lo[4 * i + 2], lo[4 * i + 3]);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+}  // namespace fa
+
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode_fa = nullptr;
+
+static int encode(CUtensorMap* map, void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+                  const cuuint32_t* box) {
+    if (!g_encode_fa) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return QW_ECUDA;
+        g_encode_fa = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    }
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return g_encode_fa(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, base, dims, strides, box, es,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS
+               ? QW_OK
+               : QW_ECUDA;
+}
+
+int launch_attn_prefill_tc(const uint16_t* q_bf16, int n_tok, const int* positions, const int4* tiles, int n_tiles,
+                           int Hq, int Hkv, const KvView& kv, uint16_t* out, int split, int* err, cudaStream_t st) {
+    if (n_tiles <= 0) return QW_OK;
+    if (Hq != 2 * Hkv) return QW_EINVAL;
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(fa::attn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, fa::SMEM) !=
+            cudaSuccess)
+            return QW_ECUDA;
+        attr = true;
+    }
+    CUtensorMap tq, tkv;
+    {   // q as [tokens][Hq * 128] bf16, boxes of 64 dims x 64 tokens
+        cuuint64_t dims[2] = {(cuuint64_t)Hq * 128, (cuuint64_t)n_tok};
+        cuuint64_t strides[1] = {(cuuint64_t)Hq * 128 * 2};
+        cuuint32_t box[2] = {64, 64};
+        if (encode(&tq, const_cast<uint16_t*>(q_bf16), 2, dims, strides, box)) return QW_ECUDA;
+    }
+    {   // this layer's pool as [page][K/V x head][slot][dim], boxes of 64 dims x 16 slots
+        cuuint64_t dims[4] = {128, QW_PAGE_SIZE, (cuuint64_t)2 * Hkv, (cuuint64_t)kv.n_pages};
+        cuuint64_t strides[3] = {128 * 2, (cuuint64_t)QW_PAGE_SIZE * 128 * 2, (cuuint64_t)kv.page_stride * 2};
+        cuuint32_t box[4] = {64, QW_PAGE_SIZE, 1, 1};
+        if (encode(&tkv, kv.base, 4, dims, strides, box)) return QW_ECUDA;
+    }
+    const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
+    fa::attn_prefill_tc_kernel<<<dim3(n_tiles, Hkv), fa::THREADS, fa::SMEM, st>>>(
+        tq, tkv, positions, tiles, kv.block_tables, kv.bt_stride, kv.n_pages, Hq, Hkv, out, scale_log2, split, err);
+    count_launches(1);
+    return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ECUDA;
+}
+
+}  // namespace qw

@@ -11,10 +11,10 @@
 
 #define QW_DEV __device__ __forceinline__
 
-// Spin budget of every bounded wait (mbarrier or global flag).  ~2^26 polls with
-// backoff is several seconds: far beyond any legitimate wait, short enough that a
+// Spin budget of every bounded wait (mbarrier or global flag).  ~2^24 polls with
+// backoff is about a second: far beyond any legitimate wait, short enough that a
 // lost arrival ends in QW_ETIMEOUT instead of a hung GPU.
-#define QW_SPIN_LIMIT (1u << 26)
+#define QW_SPIN_LIMIT (1u << 24)
 
 namespace qw {
 

@@ -48,7 +48,6 @@ constexpr int MAX_ROWS = 64;          // per-phase result slots (q|k|v rows per 
 constexpr int MAX_LAYERS = 64;
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr int TRACE_SLOTS = 16;
-constexpr unsigned long long L2_AHEAD = 320 * 1024;   // weight bytes the L2 prefetch runs ahead of the ring
 
 struct LayerPtrs {
     const uint16_t *wqkv, *woT, *wgu, *wdT;
@@ -195,69 +194,12 @@ QW_DEV Work make_work(const Params& p, int c, int G, int pos, bool bad_pos) {
 }
 
 // ---------------------------------------------------------------- producer
-// Walks the CTA's weight stream (the ring's order without the KV pages) in ring-sized
-// pieces; the producer keeps it L2_AHEAD bytes ahead of the ring with L2 prefetches, so
-// refills after a stall come from L2 instead of a fresh HBM round trip.
-struct L2Cursor {
-    int l = 0, ph = 0, off = 0;
-    unsigned long long bytes = 0;
-    QW_DEV bool next(const Params& p, const Work& w, const uint16_t*& a, int& nbytes) {
-        for (;;) {
-            if (l > p.n_layers) return false;
-            const uint16_t* base;
-            int n;
-            if (l == p.n_layers) {
-                base = p.E + (size_t)w.v0 * D;
-                n = w.v1 - w.v0;
-            } else {
-                const LayerPtrs& L = p.layers[l];
-                if (ph == 0) {
-                    base = L.wqkv + (size_t)w.q0 * D;
-                    n = w.q1 - w.q0;
-                } else if (ph == 1) {
-                    base = L.woT + (size_t)w.j0 * D;
-                    n = w.j1 - w.j0;
-                } else if (ph == 2) {
-                    base = L.wgu + (size_t)2 * w.p0 * D;
-                    n = 2 * (w.p1 - w.p0);
-                } else {
-                    base = L.wdT + (size_t)w.p0 * D;
-                    n = w.p1 - w.p0;
-                }
-            }
-            if (off < n) {
-                const int k = min(ROWS_PER_STAGE, n - off);
-                a = base + (size_t)off * D;
-                nbytes = k * ROW_B;
-                off += k;
-                bytes += nbytes;
-                return true;
-            }
-            off = 0;
-            if (l == p.n_layers || ++ph == 4) {
-                ph = 0;
-                ++l;
-            }
-        }
-    }
-};
-
 struct Producer {
     uint8_t* ring;
     Smem* sm;
     int* err;
-    const Params* prm;
-    const Work* wk;
     unsigned it = 0;
     bool stop = false;
-    unsigned long long issued = 0;  // weight bytes put in the ring
-    L2Cursor l2;
-
-    QW_DEV void run_ahead() {
-        const uint16_t* a;
-        int nb;
-        while (l2.bytes < issued + L2_AHEAD && l2.next(*prm, *wk, a, nb)) prefetch_l2(a, (uint32_t)nb);
-    }
 
     QW_DEV bool acquire(int& s) {
         s = it % NS;
@@ -274,8 +216,6 @@ struct Producer {
     QW_DEV void rows(const uint16_t* base, int nrows) {
         for (int r0 = 0; r0 < nrows && !stop; r0 += ROWS_PER_STAGE) {
             const int n = min(ROWS_PER_STAGE, nrows - r0);
-            issued += (unsigned long long)n * ROW_B;
-            run_ahead();
             int s;
             if (!acquire(s)) {
                 stop = true;
@@ -297,14 +237,13 @@ struct Producer {
                 stop = true;
                 return;
             }
+            int pgs[PAGES_PER_STAGE];
             int valid = 0;
-            for (int i = 0; i < n; ++i) {
-                const int pg = bt[p0 + i];
-                valid += (pg >= 0 && pg < n_pages);
-            }
+            for (int i = 0; i < PAGES_PER_STAGE; ++i) pgs[i] = i < n ? __ldg(bt + p0 + i) : -1;  // loads in flight together
+            for (int i = 0; i < n; ++i) valid += (pgs[i] >= 0 && pgs[i] < n_pages);
             mbar_arrive_expect_tx(&sm->full[s], valid * 2 * PAGE_B);
             for (int i = 0; i < n; ++i) {
-                const int pg = bt[p0 + i];
+                const int pg = pgs[i];
                 if (pg < 0 || pg >= n_pages) continue;
                 const uint16_t* kp = kv_layer + (int64_t)pg * page_elems + (int64_t)g * QW_PAGE_SIZE * HD;
                 bulk_load(ring + s * STAGE + i * 2 * PAGE_B, kp, PAGE_B, &sm->full[s]);
@@ -464,7 +403,7 @@ __global__ void __launch_bounds__(THREADS, 1) fused_decode_kernel(Params p) {
     if (warp == 0) {
         // ------------------------------------------------ producer
         if (lane == 0) {
-            Producer pr{ring, &sm, p.err, &p, &w};
+            Producer pr{ring, &sm, p.err};
             for (int l = 0; l < p.n_layers && !pr.stop; ++l) {
                 const LayerPtrs& L = p.layers[l];
                 pr.rows(L.wqkv + (size_t)w.q0 * D, w.q1 - w.q0);

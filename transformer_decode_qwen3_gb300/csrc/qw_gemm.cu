@@ -5,11 +5,12 @@
 // (gate/up/down_proj) and Step 8 (LM head) whenever a call carries more than a
 // few rows (prefill, batched decode).
 //
-// One CTA computes a 128 x BN output tile.  Warp 0 (one lane) issues TMA loads
-// into a STAGES-deep shared-memory ring, warp 1 (one lane) issues tcgen05.mma
-// (K = 16 per instruction, 4 per 64-wide K block) and commits each stage back
-// to the producer; all four warps then read the accumulator with tcgen05.ld
-// (thread t owns output row t) and apply the fused epilogue.
+// Persistent: one CTA per SM walks 128 x BN output tiles.  Warp 0 (one lane)
+// issues TMA loads into a STAGES-deep shared-memory ring, warp 1 (one lane)
+// issues tcgen05.mma (K = 16 per instruction, 4 per 64-wide K block) into one of
+// two TMEM accumulators and commits each stage back to the producer; warps 4..7
+// read the other accumulator with tcgen05.ld (thread t owns output row t) and
+// apply the fused epilogue, so a tile's epilogue overlaps the next tile's MMAs.
 //
 // Split-operand mode (small M, e.g. decode batches): every activation row a is
 // stored as two bf16 rows, hi = bf16(a) in tile rows 0..63 and lo = bf16(a - hi)
@@ -33,8 +34,10 @@ struct GemmCfg {
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int TMEM_COLS = BN;                // power of two >= 32
-    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int TMEM_COLS = 2 * BN;            // two accumulators; power of two >= 32
+    static constexpr int XCH_BYTES = 64 * 33 * 4;       // split-mode hand-over of the lo rows
+    static constexpr int SMEM = STAGES * STAGE_BYTES + XCH_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+    static constexpr int THREADS = 256;                 // warps 0-3: TMA, MMA, TMEM owner, idle; 4-7: epilogue
 };
 
 QW_DEV float silu_f(float g) { return g / (1.0f + expf(-g)); }
@@ -81,31 +84,40 @@ QW_DEV void epilogue_chunk(const float (&v)[32], int m, int n, const GemmEpilogu
     }
 }
 
+QW_DEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 template <int BN, int EPI, bool SPLIT>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(256, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        int M, int N, int K, GemmEpilogue ep) {
+                        int M, int N, int K, int tiles_m, int tiles_n, GemmEpilogue ep) {
     using C = GemmCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
     uint8_t* sB = smem + C::STAGES * C::A_BYTES;
-    uint64_t* full = (uint64_t*)(smem + C::STAGES * C::STAGE_BYTES);
+    float* xch = (float*)(smem + C::STAGES * C::STAGE_BYTES);
+    uint64_t* full = (uint64_t*)(smem + C::STAGES * C::STAGE_BYTES + C::XCH_BYTES);
     uint64_t* empty = full + C::STAGES;
-    uint64_t* done = empty + C::STAGES;
-    uint32_t* tmem_slot = (uint32_t*)(done + 1);
+    uint64_t* tfull = empty + C::STAGES;   // [2] accumulator ready for the epilogue
+    uint64_t* tempty = tfull + 2;          // [2] accumulator drained by the epilogue
+    uint32_t* tmem_slot = (uint32_t*)(tempty + 2);
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
+    // a CTA of this launch already gave up on a wait: end quickly instead of timing out again
+    if (ep.err && *(volatile int*)ep.err == QW_ETIMEOUT) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * BN, m0 = blockIdx.y * C::BM;
     const int nk = K / C::BK;
+    const int n_tiles = tiles_m * tiles_n;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(done, 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 4);      // one arrival per epilogue warp
+        }
         *abort_flag = 0;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
@@ -117,74 +129,106 @@ __global__ void __launch_bounds__(128, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0 && lane == 0) {
-        // TMA producer
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % C::STAGES;
-            const uint32_t ph = (kb / C::STAGES) & 1;
-            if (!mbar_wait(&empty[s], ph ^ 1, ep.err)) break;
-            if (*abort_flag) break;
-            mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
-            tma_load_2d(sA + s * C::A_BYTES, &tmA, kb * C::BK, m0, &full[s]);
-            tma_load_2d(sB + s * C::B_BYTES, &tmB, kb * C::BK, n0, &full[s]);
-        }
-    } else if (warp == 1 && lane == 0) {
-        // MMA issuer
-        constexpr uint32_t idesc = umma_idesc_bf16(C::BM, BN);
-        bool ok = true;
-        for (int kb = 0; kb < nk; ++kb) {
-            const int s = kb % C::STAGES;
-            const uint32_t ph = (kb / C::STAGES) & 1;
-            if (!mbar_wait(&full[s], ph, ep.err)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t a0 = smem_u32(sA + s * C::A_BYTES), b0 = smem_u32(sB + s * C::B_BYTES);
-#pragma unroll
-            for (int k = 0; k < C::BK / 16; ++k) {
-                umma_bf16(tmem, umma_desc_sw128(a0 + k * 32), umma_desc_sw128(b0 + k * 32), idesc,
-                          (kb | k) != 0);
-            }
-            umma_commit(&empty[s]);
-        }
-        if (ok) {
-            umma_commit(done);
-        } else {
-            *abort_flag = 1;
-            mbar_arrive(done);
-        }
-    }
-    __syncwarp();
+    // tile t -> (m, n): consecutive CTAs share the B (weight) tile
+    auto tile_mn = [&](int t, int& tm, int& tn) {
+        tn = t / tiles_m;
+        tm = t % tiles_m;
+    };
 
-    // Epilogue: thread t of the CTA owns accumulator row t.
-    const bool ok = mbar_wait(done, 0, ep.err) && !*abort_flag;
-    tc_fence_after();
-    if (ok) {
-        const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
-        float* xch = (float*)smem;  // split mode: lo rows handed to the hi rows (stages are idle now)
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-            if (n0 + c0 >= N) break;  // CTA-uniform
-            float v[32];
-            tmem_ld32(trow + c0, v);
-            if (SPLIT) {
-                if (warp >= 2) {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) xch[((warp - 2) * 32 + lane) * 33 + i] = v[i];
+    if (warp == 0) {
+        if (lane == 0) {  // TMA producer
+            uint32_t kb_all = 0;
+            for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
+                int tm, tn;
+                tile_mn(t, tm, tn);
+                for (int kb = 0; kb < nk; ++kb, ++kb_all) {
+                    const int s = kb_all % C::STAGES;
+                    const uint32_t ph = (kb_all / C::STAGES) & 1;
+                    if (!mbar_wait(&empty[s], ph ^ 1, ep.err) || *abort_flag) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+                    tma_load_2d(sA + s * C::A_BYTES, &tmA, kb * C::BK, tm * C::BM, &full[s]);
+                    tma_load_2d(sB + s * C::B_BYTES, &tmB, kb * C::BK, tn * BN, &full[s]);
                 }
-                __syncthreads();
-                if (warp < 2) {
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // MMA issuer
+            constexpr uint32_t idesc = umma_idesc_bf16(C::BM, BN);
+            uint32_t kb_all = 0;
+            int local = 0;
+            for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++local) {
+                const int acc = local & 1;
+                const uint32_t use = (uint32_t)(local >> 1);
+                bool ok = !*abort_flag && mbar_wait(&tempty[acc], (use & 1) ^ 1, ep.err);
+                tc_fence_after();
+                const uint32_t dtm = tmem + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < nk && ok; ++kb, ++kb_all) {
+                    const int s = kb_all % C::STAGES;
+                    const uint32_t ph = (kb_all / C::STAGES) & 1;
+                    if (!mbar_wait(&full[s], ph, ep.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sA + s * C::A_BYTES), b0 = smem_u32(sB + s * C::B_BYTES);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] += xch[(warp * 32 + lane) * 33 + i];
-                    const int m = blockIdx.y * 64 + warp * 32 + lane;
+                    for (int k = 0; k < C::BK / 16; ++k)
+                        umma_bf16(dtm, umma_desc_sw128(a0 + k * 32), umma_desc_sw128(b0 + k * 32), idesc,
+                                  (kb | k) != 0);
+                    umma_commit(&empty[s]);
+                }
+                if (!ok) {
+                    *abort_flag = 1;
+                    mbar_arrive(&tfull[acc]);  // release the epilogue, which sees the abort flag
+                    break;
+                }
+                umma_commit(&tfull[acc]);
+            }
+        }
+    } else if (warp >= 4) {
+        // Epilogue warpgroup: warp 4 + i reads TMEM lanes 32 i .. 32 i + 31.
+        const int ew = warp - 4;
+        const int et = threadIdx.x - 128;
+        int local = 0;
+        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++local) {
+            int tm, tn;
+            tile_mn(t, tm, tn);
+            const int acc = local & 1;
+            const uint32_t use = (uint32_t)(local >> 1);
+            const bool ok = mbar_wait(&tfull[acc], use & 1, ep.err) && !*abort_flag;
+            tc_fence_after();
+            if (!ok) break;
+            const uint32_t trow = tmem + (uint32_t)(acc * BN) + ((uint32_t)(ew * 32) << 16);
+            const int n0 = tn * BN;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                if (n0 + c0 >= N) break;  // uniform over the warpgroup
+                float v[32];
+                tmem_ld32(trow + c0, v);
+                if (SPLIT) {
+                    if (ew >= 2) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) xch[((ew - 2) * 32 + lane) * 33 + i] = v[i];
+                    }
+                    epi_bar();
+                    if (ew < 2) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] += xch[(ew * 32 + lane) * 33 + i];
+                        const int m = tm * 64 + ew * 32 + lane;
+                        if (m < M) epilogue_chunk<BN, EPI>(v, m, n0 + c0, ep);
+                    }
+                    epi_bar();
+                } else {
+                    const int m = tm * C::BM + et;
                     if (m < M) epilogue_chunk<BN, EPI>(v, m, n0 + c0, ep);
                 }
-                __syncthreads();
-            } else {
-                const int m = m0 + warp * 32 + lane;
-                if (m < M) epilogue_chunk<BN, EPI>(v, m, n0 + c0, ep);
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
         }
     }
     tc_fence_before();
@@ -232,9 +276,16 @@ static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N,
             return QW_ECUDA;
         attr_set = true;
     }
-    const int m_tiles = SPLIT ? (M + 63) / 64 : (M + C::BM - 1) / C::BM;
-    dim3 grid((N + BN - 1) / BN, m_tiles);
-    gemm_bf16_tc_kernel<BN, EPI, SPLIT><<<grid, 128, C::SMEM, st>>>(ta, tb, M, N, K, ep);
+    static int n_sm = 0;
+    if (!n_sm) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    }
+    const int tiles_m = SPLIT ? (M + 63) / 64 : (M + C::BM - 1) / C::BM;
+    const int tiles_n = (N + BN - 1) / BN;
+    const int grid = tiles_m * tiles_n < n_sm ? tiles_m * tiles_n : n_sm;
+    gemm_bf16_tc_kernel<BN, EPI, SPLIT><<<grid, C::THREADS, C::SMEM, st>>>(ta, tb, M, N, K, tiles_m, tiles_n, ep);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ECUDA;
 }

@@ -52,9 +52,12 @@ int launch_rmsnorm_bf16(const float* x, const int* rows /*nullable*/, int n, int
                         uint16_t* out, int split, cudaStream_t st);
 int launch_qkv_post(const float* qkv, int n_tok, const int* positions, const int* tok_seq, int Hq, int Hkv,
                     const float* q_norm, const float* k_norm, const float* inv_freq, float eps, float* q_out,
-                    const KvView& kv, int* err, cudaStream_t st);
+                    uint16_t* q_bf16 /*nullable*/, const KvView& kv, int* err, cudaStream_t st);
 int launch_attn_prefill(const float* q, const int* positions, const int4* tiles, int n_tiles, int Hq, int Hkv,
                         const KvView& kv, uint16_t* out, int split, int* err, cudaStream_t st);
+// Prefill attention on tcgen05 (q as bf16 [n_tok][Hq * 128]).
+int launch_attn_prefill_tc(const uint16_t* q_bf16, int n_tok, const int* positions, const int4* tiles, int n_tiles,
+                           int Hq, int Hkv, const KvView& kv, uint16_t* out, int split, int* err, cudaStream_t st);
 int launch_attn_decode(const float* q, const int* positions, int batch, int Hq, int Hkv, const KvView& kv,
                        float* part, int max_splits, uint16_t* out, int split, int* err, int n_sm, cudaStream_t st);
 // argmax_hint (nullable, batch 1): the argmax of the logits row, already computed by the

@@ -93,7 +93,7 @@ int launch_rmsnorm_bf16(const float* x, const int* rows, int n, int D, const flo
 __global__ void qkv_post_kernel(const float* __restrict__ qkv, const int* __restrict__ positions,
                                 const int* __restrict__ tok_seq, int Hq, int Hkv, const float* __restrict__ q_norm,
                                 const float* __restrict__ k_norm, const float* __restrict__ inv_freq, float eps,
-                                float* __restrict__ q_out, KvView kv, int* err) {
+                                float* __restrict__ q_out, uint16_t* __restrict__ q_bf16, KvView kv, int* err) {
     const int t = blockIdx.x;
     const int hh = blockIdx.y * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     const int nh = Hq + 2 * Hkv;
@@ -123,6 +123,11 @@ __global__ void qkv_post_kernel(const float* __restrict__ qkv, const int* __rest
         float* dst = q_out + ((size_t)t * Hq + hh) * QW_HEAD_DIM;
 #pragma unroll
         for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = y[i];
+        if (q_bf16) {
+            uint16_t* qb = q_bf16 + ((size_t)t * Hq + hh) * QW_HEAD_DIM;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) qb[lane + 32 * i] = f2bf(y[i]);
+        }
         return;
     }
     const int seq = tok_seq[t];
@@ -145,11 +150,11 @@ __global__ void qkv_post_kernel(const float* __restrict__ qkv, const int* __rest
 
 int launch_qkv_post(const float* qkv, int n_tok, const int* positions, const int* tok_seq, int Hq, int Hkv,
                     const float* q_norm, const float* k_norm, const float* inv_freq, float eps, float* q_out,
-                    const KvView& kv, int* err, cudaStream_t st) {
+                    uint16_t* q_bf16, const KvView& kv, int* err, cudaStream_t st) {
     if (n_tok <= 0) return QW_OK;
     dim3 grid(n_tok, (Hq + 2 * Hkv + 3) / 4);
-    qkv_post_kernel<<<grid, 128, 0, st>>>(qkv, positions, tok_seq, Hq, Hkv, q_norm, k_norm, inv_freq, eps, q_out, kv,
-                                          err);
+    qkv_post_kernel<<<grid, 128, 0, st>>>(qkv, positions, tok_seq, Hq, Hkv, q_norm, k_norm, inv_freq, eps, q_out,
+                                          q_bf16, kv, err);
     return check_launch();
 }
 
@@ -439,8 +444,10 @@ __global__ void __launch_bounds__(AD_WARPS * 32) attn_decode_kernel(const float*
     const int* bt = kv.block_tables + (size_t)b * kv.bt_stride;
     const int64_t v_off = (int64_t)Hkv * QW_PAGE_SIZE * QW_HEAD_DIM;
 
+    int next_page = p_lo + warp < p_hi ? __ldg(bt + p_lo + warp) : 0;
     for (int pi = p_lo + warp; pi < p_hi; pi += AD_WARPS) {
-        const int page = bt[pi];
+        const int page = next_page;  // the next lookup is in flight while this page is processed
+        if (pi + AD_WARPS < p_hi) next_page = __ldg(bt + pi + AD_WARPS);
         if (page < 0 || page >= kv.n_pages) {
             if (lane == 0) set_error(err, QW_ERANGE);
             continue;
