@@ -223,7 +223,8 @@ int qw_debug_hidden(qw_ctx* ctx, int32_t layer, float* out, int32_t n_rows, void
  *   N % 32 == 0, bn = 128 or 256 (output tile width) and the epilogue
  *   epi = 0: C is float[M][N], C = A B^T;  1: C += A B^T (residual add);
  *   epi = 2: C is bf16[M][N/2], C[m][j] = silu(Y[m][2j]) * Y[m][2j+1] with Y = A B^T
- *   (the SwiGLU of Step 6 on gate/up rows interleaved).
+ *   (the SwiGLU of Step 6 on gate/up rows interleaved);
+ *   epi = 3: C += A B^T with K split across SMs and fp32 atomic adds (small-M path).
  * split = 1: A holds ceil(M/64) blocks of 128 rows, rows 0..63 of a block the bf16 "hi"
  *   parts of 64 activation rows and rows 64..127 their "lo" remainders; the product uses
  *   hi + lo (the layout decode batches use), and with epi = 2 the output is written in the

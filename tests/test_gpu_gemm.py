@@ -78,3 +78,19 @@ def test_gemm_split_operand(bd, M, N, K, bn, epi):
     torch.cuda.synchronize()
     err = (C - X - ref).norm() / ref.norm()
     assert err < 2e-5, f"rel err {err:.3e}"           # plain bf16 activations would give ~2e-3
+
+
+@pytest.mark.parametrize("M,N,K,bn", [(1, 4096, 1024, 256), (64, 1024, 3072, 128), (64, 6144, 1024, 256),
+                                      (200, 1024, 2048, 128)])
+def test_gemm_split_k_atomic(bd, M, N, K, bn):
+    """Small-M split-K: every SM takes a K slice and adds its partial product atomically."""
+    g = torch.Generator(device="cpu").manual_seed(M * 3 + N)
+    a = (torch.randn(M, K, generator=g) * 0.5).cuda()
+    B = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16).cuda()
+    X = torch.randn(M, N, device="cuda")
+    C = X.clone()
+    bd.debug_gemm(bd.split_rows(a), B, C, epi=3, bn=bn, split=True, M=M)
+    torch.cuda.synchronize()
+    ref = a @ B.float().T
+    err = (C - X - ref).norm() / ref.norm()
+    assert err < 2e-5, f"rel err {err:.3e}"

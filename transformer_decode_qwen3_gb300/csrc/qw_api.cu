@@ -60,6 +60,7 @@ struct qw_ctx {
     // workspaces
     uint8_t* wsbuf = nullptr;
     float *x = nullptr, *qkv = nullptr, *q = nullptr, *logits = nullptr, *part = nullptr, *hidden = nullptr;
+    float* gu = nullptr;   // split-K gate/up sums of small-M calls [SPLIT_MAX_M][2 * intermediate]
     uint16_t *h = nullptr, *attn = nullptr, *act = nullptr, *q_bf16 = nullptr;
     int *tok_seq = nullptr, *iota = nullptr, *rows_last = nullptr, *err = nullptr;
     int4* tiles = nullptr;
@@ -265,6 +266,7 @@ int qw_init(const qw_config* cfg, const qw_weights* w, qw_ctx** out) {
     const size_t oq = take((size_t)T * ctx->attn_dim * 4);
     const size_t oqb = take((size_t)T * ctx->attn_dim * 2);
     const size_t ologits = take((size_t)c.max_batch * V * 4);
+    const size_t ogu = take((size_t)SPLIT_MAX_M * 2 * I * 4);
     const size_t opart = take((size_t)c.max_batch * Hq * ctx->max_splits * (d + 2) * 4);
     const size_t oh = take((size_t)TA * D * 2);
     const size_t oattn = take((size_t)TA * ctx->attn_dim * 2);
@@ -285,6 +287,7 @@ int qw_init(const qw_config* cfg, const qw_weights* w, qw_ctx** out) {
     ctx->q = (float*)(W + oq);
     ctx->q_bf16 = (uint16_t*)(W + oqb);
     ctx->logits = (float*)(W + ologits);
+    ctx->gu = (float*)(W + ogu);
     ctx->part = (float*)(W + opart);
     ctx->h = (uint16_t*)(W + oh);
     ctx->attn = (uint16_t*)(W + oattn);
@@ -385,8 +388,11 @@ static int run_layers(qw_ctx* ctx, int n, const int* ids, const int* positions, 
         KvView kvv{kv->base + (int64_t)l * kv->layer_elems, kv->page_elems, kv->n_pages, bt, bt_stride};
         QW_TRY(launch_rmsnorm_bf16(ctx->x, nullptr, n, D, Lw.in_norm, c.rms_eps, ctx->h, split, st),
                "rmsnorm launch");
+        // small M: split-K with atomic accumulation (zeroed targets) so every SM streams weights
         GemmEpilogue e{ctx->qkv, nullptr, ctx->qkv_dim, ctx->err, split};
-        QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_qkv, 256, n, ctx->qkv_dim, D, EPI_STORE_F32, e, st), "qkv gemm");
+        if (split) QW_CUDA(cudaMemsetAsync(ctx->qkv, 0, (size_t)n * ctx->qkv_dim * 4, st));
+        QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_qkv, 256, n, ctx->qkv_dim, D, split ? EPI_ADD_ATOMIC : EPI_STORE_F32, e, st),
+               "qkv gemm");
         const bool tc_attn = mode == 0 && ctx->prefill_attn == 0;
         QW_TRY(launch_qkv_post(ctx->qkv, n, positions, tok_seq, Hq, Hkv, Lw.q_norm, Lw.k_norm, ctx->inv_freq,
                                c.rms_eps, ctx->q, tc_attn ? ctx->q_bf16 : nullptr, kvv, ctx->err, st),
@@ -404,13 +410,23 @@ static int run_layers(qw_ctx* ctx, int n, const int* ids, const int* positions, 
                                       split, ctx->err, ctx->n_sm, st),
                    "decode attention launch");
         e = GemmEpilogue{ctx->x, nullptr, D, ctx->err, split};
-        QW_TRY(gemm_bf16(ctx->attn, ctx->attn_dim, Lw.tm_o, 128, n, D, ctx->attn_dim, EPI_RESID_ADD, e, st), "o_proj gemm");
+        QW_TRY(gemm_bf16(ctx->attn, ctx->attn_dim, Lw.tm_o, 128, n, D, ctx->attn_dim,
+                         split ? EPI_ADD_ATOMIC : EPI_RESID_ADD, e, st),
+               "o_proj gemm");
         QW_TRY(launch_rmsnorm_bf16(ctx->x, nullptr, n, D, Lw.post_norm, c.rms_eps, ctx->h, split, st),
                "rmsnorm launch");
-        e = GemmEpilogue{nullptr, ctx->act, I, ctx->err, split};
-        QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_gu, 256, n, 2 * I, D, EPI_SWIGLU, e, st), "gate/up gemm");
+        if (split) {
+            QW_CUDA(cudaMemsetAsync(ctx->gu, 0, (size_t)n * 2 * I * 4, st));
+            e = GemmEpilogue{ctx->gu, nullptr, 2 * I, ctx->err, split};
+            QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_gu, 256, n, 2 * I, D, EPI_ADD_ATOMIC, e, st), "gate/up gemm");
+            QW_TRY(launch_swiglu_split(ctx->gu, n, I, ctx->act, st), "swiglu launch");
+        } else {
+            e = GemmEpilogue{nullptr, ctx->act, I, ctx->err, split};
+            QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_gu, 256, n, 2 * I, D, EPI_SWIGLU, e, st), "gate/up gemm");
+        }
         e = GemmEpilogue{ctx->x, nullptr, D, ctx->err, split};
-        QW_TRY(gemm_bf16(ctx->act, I, Lw.tm_d, 128, n, D, I, EPI_RESID_ADD, e, st), "down gemm");
+        QW_TRY(gemm_bf16(ctx->act, I, Lw.tm_d, 128, n, D, I, split ? EPI_ADD_ATOMIC : EPI_RESID_ADD, e, st),
+               "down gemm");
         if (ctx->hidden)
             QW_CUDA(cudaMemcpyAsync(ctx->hidden + (size_t)l * ctx->max_rows * D, ctx->x, (size_t)n * D * 4,
                                     cudaMemcpyDeviceToDevice, st));
@@ -554,7 +570,7 @@ int qw_debug_hidden(qw_ctx* ctx, int32_t layer, float* out, int32_t n_rows, void
 
 int qw_debug_gemm(const uint16_t* A, const uint16_t* B, void* C, int32_t M, int32_t N, int32_t K, int32_t epi,
                   int32_t bn, int32_t split, void* stream) {
-    if (!A || !B || !C || M < 1 || N < 32 || K < 64 || K % 64 || N % 32 || epi < 0 || epi > 2 ||
+    if (!A || !B || !C || M < 1 || N < 32 || K < 64 || K % 64 || N % 32 || epi < 0 || epi > 3 ||
         (bn != 128 && bn != 256))
         return fail(QW_EINVAL, "qw_debug_gemm: bad argument");
     CUtensorMap tb;

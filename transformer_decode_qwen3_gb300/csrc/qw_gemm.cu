@@ -51,6 +51,10 @@ QW_DEV void epilogue_chunk(const float (&v)[32], int m, int n, const GemmEpilogu
         float4* dst = (float4*)(ep.out + (size_t)m * ep.ldo + n);
 #pragma unroll
         for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    } else if (EPI == EPI_ADD_ATOMIC) {  // one K-slice of a split-K product: out += partial
+        float4* dst = (float4*)(ep.out + (size_t)m * ep.ldo + n);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) atomicAdd(dst + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
     } else if (EPI == EPI_RESID_ADD) {
         float4* dst = (float4*)(ep.out + (size_t)m * ep.ldo + n);
 #pragma unroll
@@ -89,7 +93,7 @@ QW_DEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 template <int BN, int EPI, bool SPLIT>
 __global__ void __launch_bounds__(256, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        int M, int N, int K, int tiles_m, int tiles_n, GemmEpilogue ep) {
+                        int M, int N, int K, int tiles_m, int tiles_n, int ksplit, GemmEpilogue ep) {
     using C = GemmCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -107,7 +111,7 @@ __global__ void __launch_bounds__(256, 1)
     if (ep.err && *(volatile int*)ep.err == QW_ETIMEOUT) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = K / C::BK;
-    const int n_tiles = tiles_m * tiles_n;
+    const int n_tiles = tiles_m * tiles_n * ksplit;   // work units: (m tile, n tile, K slice)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -129,19 +133,22 @@ __global__ void __launch_bounds__(256, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // tile t -> (m, n): consecutive CTAs share the B (weight) tile
-    auto tile_mn = [&](int t, int& tm, int& tn) {
-        tn = t / tiles_m;
-        tm = t % tiles_m;
+    // unit t -> (m tile, n tile, K blocks [kb0, kb1)); consecutive CTAs share the B (weight) tile
+    auto unit = [&](int t, int& tm, int& tn, int& kb0, int& kb1) {
+        const int ks = t % ksplit, rest = t / ksplit;
+        tn = rest / tiles_m;
+        tm = rest % tiles_m;
+        kb0 = ks * nk / ksplit;
+        kb1 = (ks + 1) * nk / ksplit;
     };
 
     if (warp == 0) {
         if (lane == 0) {  // TMA producer
             uint32_t kb_all = 0;
             for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
-                int tm, tn;
-                tile_mn(t, tm, tn);
-                for (int kb = 0; kb < nk; ++kb, ++kb_all) {
+                int tm, tn, kb0, kb1;
+                unit(t, tm, tn, kb0, kb1);
+                for (int kb = kb0; kb < kb1; ++kb, ++kb_all) {
                     const int s = kb_all % C::STAGES;
                     const uint32_t ph = (kb_all / C::STAGES) & 1;
                     if (!mbar_wait(&empty[s], ph ^ 1, ep.err) || *abort_flag) {
@@ -165,7 +172,9 @@ __global__ void __launch_bounds__(256, 1)
                 bool ok = !*abort_flag && mbar_wait(&tempty[acc], (use & 1) ^ 1, ep.err);
                 tc_fence_after();
                 const uint32_t dtm = tmem + (uint32_t)(acc * BN);
-                for (int kb = 0; kb < nk && ok; ++kb, ++kb_all) {
+                int tm, tn, kb0, kb1;
+                unit(t, tm, tn, kb0, kb1);
+                for (int kb = kb0; kb < kb1 && ok; ++kb, ++kb_all) {
                     const int s = kb_all % C::STAGES;
                     const uint32_t ph = (kb_all / C::STAGES) & 1;
                     if (!mbar_wait(&full[s], ph, ep.err)) {
@@ -177,7 +186,7 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                     for (int k = 0; k < C::BK / 16; ++k)
                         umma_bf16(dtm, umma_desc_sw128(a0 + k * 32), umma_desc_sw128(b0 + k * 32), idesc,
-                                  (kb | k) != 0);
+                                  (kb != kb0) || k != 0);
                     umma_commit(&empty[s]);
                 }
                 if (!ok) {
@@ -194,8 +203,8 @@ __global__ void __launch_bounds__(256, 1)
         const int et = threadIdx.x - 128;
         int local = 0;
         for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++local) {
-            int tm, tn;
-            tile_mn(t, tm, tn);
+            int tm, tn, kb0, kb1;
+            unit(t, tm, tn, kb0, kb1);
             const int acc = local & 1;
             const uint32_t use = (uint32_t)(local >> 1);
             const bool ok = mbar_wait(&tfull[acc], use & 1, ep.err) && !*abort_flag;
@@ -284,8 +293,18 @@ static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N,
     }
     const int tiles_m = SPLIT ? (M + 63) / 64 : (M + C::BM - 1) / C::BM;
     const int tiles_n = (N + BN - 1) / BN;
-    const int grid = tiles_m * tiles_n < n_sm ? tiles_m * tiles_n : n_sm;
-    gemm_bf16_tc_kernel<BN, EPI, SPLIT><<<grid, C::THREADS, C::SMEM, st>>>(ta, tb, M, N, K, tiles_m, tiles_n, ep);
+    // split-K (atomic epilogue only): enough K slices to give every SM a unit
+    int ksplit = 1;
+    if (EPI == EPI_ADD_ATOMIC) {
+        const int nk = K / C::BK, units = tiles_m * tiles_n;
+        ksplit = units < n_sm ? n_sm / units : 1;
+        if (ksplit > nk) ksplit = nk;
+        if (ksplit < 1) ksplit = 1;
+    }
+    const int work = tiles_m * tiles_n * ksplit;
+    const int grid = work < n_sm ? work : n_sm;
+    gemm_bf16_tc_kernel<BN, EPI, SPLIT><<<grid, C::THREADS, C::SMEM, st>>>(ta, tb, M, N, K, tiles_m, tiles_n, ksplit,
+                                                                         ep);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ECUDA;
 }
@@ -296,10 +315,12 @@ static int launch_split(const CUtensorMap& ta, const CUtensorMap& tb, int bn, in
     if (bn == 256) {
         if (epi == EPI_STORE_F32) return launch_bn<256, EPI_STORE_F32, SPLIT>(ta, tb, M, N, K, ep, st);
         if (epi == EPI_RESID_ADD) return launch_bn<256, EPI_RESID_ADD, SPLIT>(ta, tb, M, N, K, ep, st);
+        if (epi == EPI_ADD_ATOMIC) return launch_bn<256, EPI_ADD_ATOMIC, SPLIT>(ta, tb, M, N, K, ep, st);
         return launch_bn<256, EPI_SWIGLU, SPLIT>(ta, tb, M, N, K, ep, st);
     }
     if (epi == EPI_STORE_F32) return launch_bn<128, EPI_STORE_F32, SPLIT>(ta, tb, M, N, K, ep, st);
     if (epi == EPI_RESID_ADD) return launch_bn<128, EPI_RESID_ADD, SPLIT>(ta, tb, M, N, K, ep, st);
+    if (epi == EPI_ADD_ATOMIC) return launch_bn<128, EPI_ADD_ATOMIC, SPLIT>(ta, tb, M, N, K, ep, st);
     return launch_bn<128, EPI_SWIGLU, SPLIT>(ta, tb, M, N, K, ep, st);
 }
 

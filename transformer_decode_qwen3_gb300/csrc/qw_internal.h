@@ -14,7 +14,9 @@ void count_launches(int n);
 // Record `msg` for qw_last_error_message() on this thread and return `code`.
 int report_error(int code, const char* msg);
 
-enum { EPI_STORE_F32 = 0, EPI_RESID_ADD = 1, EPI_SWIGLU = 2 };
+// EPI_ADD_ATOMIC: out += acc with fp32 atomics; the launch splits K so that every SM gets
+// work (small-M products: decode batches).
+enum { EPI_STORE_F32 = 0, EPI_RESID_ADD = 1, EPI_SWIGLU = 2, EPI_ADD_ATOMIC = 3 };
 
 struct GemmEpilogue {
     float* out;      // EPI_STORE_F32: out[m][n]; EPI_RESID_ADD: out[m][n] += acc
@@ -65,5 +67,7 @@ int launch_attn_decode(const float* q, const int* positions, int batch, int Hq, 
 int launch_sample(const float* logits, int batch, int vocab, const qw_sample_params* params, uint64_t rng_counter,
                   int32_t* out_ids, const int* argmax_hint, int* err, cudaStream_t st);
 int launch_bf16_to_f32(const uint16_t* src, float* dst, int n, cudaStream_t st);
+// act (split hi/lo layout) = silu(gu[m][2j]) * gu[m][2j+1] for m < n, j < I.
+int launch_swiglu_split(const float* gu, int n, int I, uint16_t* act, cudaStream_t st);
 
 }  // namespace qw
