@@ -49,6 +49,7 @@ extern "C" {
 #define QW_HEAD_DIM 128   /* the only head size the kernels implement */
 #define QW_MAX_TOP_K 1024 /* largest top_k qw_sample accepts */
 #define QW_NOALLOC_SCRATCH_FLOATS (1 << 20) /* fixed scratch of qw_attn_decode_noalloc: 4 MiB */
+#define QW_TRACE_SLOTS 24  /* timestamps per CTA and layer in qw_debug_trace */
 
 typedef struct qw_ctx qw_ctx;
 typedef struct qw_kv qw_kv;
@@ -235,11 +236,14 @@ int qw_debug_gemm(const uint16_t* A, const uint16_t* B, void* C, int32_t M, int3
 /* Tracing hook of the fused batch-1 decode kernel.  enable = 1: the following fused
  * steps record %globaltimer stamps (ns) at every phase boundary; enable = 0: stop.
  * host_out (nullable, HOST uint64[n]): receives the stamps of the last traced step,
- * [CTA][layer 0..n_layers][16 slots] (slot 0/1: before/after the wait for the layer
+ * [CTA][layer 0..n_layers][QW_TRACE_SLOTS] (slot 0/1: before/after the wait for the layer
  * input, 2: q|k|v published, 3: attention input ready, 4: attention split published,
  * 5: attention merged, 6: o_proj published, 7: MLP input ready, 8: layer published,
- * 9: the producer has issued the layer's weights; layer n_layers: LM head wait
- * begin/end and done).  *n_needed receives the buffer length.  Synchronous. */
+ * 9: the producer has issued the layer's weights, 10/12: normalised input ready for
+ * q|k|v / gate-up, 11/13: their dot products done, 14: down_proj rows done, 15: o_proj
+ * rows start, 16/17: first weight stage of q|k|v / gate-up arrived, 18/19: attention
+ * keys start / done, 20/21: first key stage arrived / its scores published, 22/23: SM
+ * clock64 at 20/21 (cycles, not ns); layer n_layers: LM head wait begin/end and done).  *n_needed receives the buffer length.  Synchronous. */
 int qw_debug_trace(qw_ctx* ctx, int32_t enable, uint64_t* host_out, int64_t n, int64_t* n_needed);
 
 /* Select the prefill attention kernel: 0 = tcgen05/TMEM flash kernel (default),

@@ -23,6 +23,7 @@ QW_OK, QW_EINVAL, QW_ERANGE, QW_ENOMEM, QW_EKVFULL, QW_ECUDA, QW_ETIMEOUT = 0, -
 QW_PAGE_SIZE = 16
 QW_HEAD_DIM = 128
 QW_MAX_TOP_K = 1024
+QW_TRACE_SLOTS = 24
 
 EXPORTED = ["qw_config_default", "qw_init", "qw_destroy", "qw_kv_create", "qw_kv_destroy", "qw_kv_layout",
             "qw_prefill", "qw_decode_step", "qw_sample", "qw_check", "qw_last_error_message",
@@ -215,7 +216,7 @@ class Model:
                "qw_attn_decode")
 
     def trace(self, enable: bool, fetch: bool = False):
-        """Fused-decode phase stamps: returns a uint64 tensor [CTA, layers + 1, 16] when fetch."""
+        """Fused-decode phase stamps: returns a uint64 tensor [CTA, layers + 1, QW_TRACE_SLOTS] when fetch."""
         need = ctypes.c_int64()
         _check(_lib.qw_debug_trace(self.handle, int(enable), None, 0, ctypes.byref(need)), "qw_debug_trace")
         if not fetch:
@@ -223,7 +224,7 @@ class Model:
         out = torch.zeros(need.value, dtype=torch.int64)
         _check(_lib.qw_debug_trace(self.handle, int(enable), out.data_ptr(), need.value, ctypes.byref(need)),
                "qw_debug_trace")
-        return out.view(-1, self.shape.n_layers + 1, 16)
+        return out.view(-1, self.shape.n_layers + 1, QW_TRACE_SLOTS)
 
     def check(self, stream=None):
         _check(_lib.qw_check(self.handle, _stream(stream)), "qw_check")

@@ -47,7 +47,8 @@ constexpr int PART = HD + 2;
 constexpr int MAX_ROWS = 64;          // per-phase result slots (q|k|v rows per CTA <= 4096/G + 1)
 constexpr int MAX_LAYERS = 64;
 constexpr uint64_t WAIT_NS = 2000000000ull;
-constexpr int TRACE_SLOTS = 16;
+constexpr int TRACE_SLOTS = QW_TRACE_SLOTS;
+constexpr int NSH = 8;   // accumulator shards: CTA c adds into shard c % NSH (fewer adds per address)
 
 struct LayerPtrs {
     const uint16_t *wqkv, *woT, *wgu, *wdT;
@@ -71,8 +72,8 @@ struct Params {
     int n_pages;
     float* logits;
     float* R;      // [2][D]
-    float* oacc;   // [2][D]
-    float* dacc;   // [2][D]
+    float* oacc;   // [2][NSH][D]
+    float* dacc;   // [2][NSH][D]
     float* qkv;    // [QKVR]
     float* part;   // [HQ][nsa][PART]
     float* lm_part;  // [G][2]
@@ -109,17 +110,25 @@ QW_DEV void stamp(const Params& p, int l, int k) {
 
 struct Smem {
     uint64_t full[NS], empty[NS];
+    int spg[NS][PAGES_PER_STAGE];  // page ids of a KV stage (-1: none or out of range)
     volatile int abort_flag;
     int pad;
     alignas(16) float h[D];  // normalised activation of the current phase (read as float4)
     float res[MAX_ROWS];   // dot products of the current phase
     float coef[MAX_ROWS];  // scale of each row in the scaled-row phases
     float wsum[NCW];
-    float q[2][HD], kn[HD], vn[HD];
-    float am[NCW][2], al[NCW][2];
-    float ao[NCW][2][HD];
+    // rotated queries, pre-scaled to log2 units: dim 8 u + 4 h + e of head hh at q[hh][h][u][e], so
+    // that the float4 reads of 8 different chunks u hit 8 different bank groups
+    alignas(16) float q[2][2][HD / 8][4];
+    alignas(16) uint16_t kn_b[HD];   // the new key and value as bf16 (as the cache holds them)
+    alignas(16) uint16_t vn_b[HD];
+    alignas(16) float pp[2][2][64];  // attention: exp2(s - m_w) per key slot (two stage buffers)
+    float am[2][NCW][2], al[2][NCW][2];  // per-warp max and sum of those (two stage buffers)
+    alignas(16) float ao[PAGES_PER_STAGE][2][HD];  // per-page partial outputs
+    float alq[PAGES_PER_STAGE][2];
     float lm_val[NCW];
     int lm_idx[NCW];
+    int last_cta;
 };
 constexpr int SMEM_BYTES = NS * STAGE + 1024 + (int)sizeof(Smem);
 
@@ -240,11 +249,15 @@ struct Producer {
             int pgs[PAGES_PER_STAGE];
             int valid = 0;
             for (int i = 0; i < PAGES_PER_STAGE; ++i) pgs[i] = i < n ? __ldg(bt + p0 + i) : -1;  // loads in flight together
-            for (int i = 0; i < n; ++i) valid += (pgs[i] >= 0 && pgs[i] < n_pages);
+            for (int i = 0; i < PAGES_PER_STAGE; ++i) {
+                if (pgs[i] < 0 || pgs[i] >= n_pages) pgs[i] = -1;
+                valid += pgs[i] >= 0;
+                sm->spg[s][i] = pgs[i];  // published to the consumers by the arrive below
+            }
             mbar_arrive_expect_tx(&sm->full[s], valid * 2 * PAGE_B);
             for (int i = 0; i < n; ++i) {
                 const int pg = pgs[i];
-                if (pg < 0 || pg >= n_pages) continue;
+                if (pg < 0) continue;
                 const uint16_t* kp = kv_layer + (int64_t)pg * page_elems + (int64_t)g * QW_PAGE_SIZE * HD;
                 bulk_load(ring + s * STAGE + i * 2 * PAGE_B, kp, PAGE_B, &sm->full[s]);
                 bulk_load(ring + s * STAGE + i * 2 * PAGE_B + PAGE_B, kp + (int64_t)HKV * QW_PAGE_SIZE * HD, PAGE_B,
@@ -274,13 +287,14 @@ struct Consumer {
         if (!ok) sm->abort_flag = 1;
         return ring + s * STAGE;
     }
+    QW_DEV int slot() const { return it % NS; }
     QW_DEV void stage_release() {
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm->empty[it % NS]);
         ++it;
     }
     // Dot products of `nrows` streamed rows with sm->h; results to sm->res[0..nrows).
-    QW_DEV bool dot_rows(int nrows, bool ok) {
+    QW_DEV bool dot_rows(int nrows, bool ok, const Params* tp = nullptr, int tl = 0, int tslot = 0) {
         float hreg[4][8];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -292,6 +306,7 @@ struct Consumer {
         for (int r0 = 0; r0 < nrows; r0 += ROWS_PER_STAGE) {
             const int n = min(ROWS_PER_STAGE, nrows - r0);
             const uint8_t* st = stage_wait(ok);
+            if (tp && r0 == 0 && cw == 0 && lane == 0) stamp(*tp, tl, tslot);
             if (ok) {
                 // rows cw and cw + 8 together: two independent chains per row, loads issued first
                 for (int r = cw; r < n; r += 2 * NCW) {
@@ -357,6 +372,22 @@ struct Consumer {
         return ok;
     }
 };
+
+// Sum over the NSH shards of a [NSH][D] accumulator at entries k0 .. k0+3 (loads in flight together).
+QW_DEV float4 sum_shards(const float* base, int k0) {
+    float4 v[NSH];
+#pragma unroll
+    for (int s = 0; s < NSH; ++s) v[s] = __ldcg((const float4*)(base + s * D + k0));
+    float4 t = v[0];
+#pragma unroll
+    for (int s = 1; s < NSH; ++s) {
+        t.x += v[s].x;
+        t.y += v[s].y;
+        t.z += v[s].z;
+        t.w += v[s].w;
+    }
+    return t;
+}
 
 // Add this lane's 4 output columns into global dst (one 16-byte atomic).
 QW_DEV void add_columns(const float (&acc)[4], float* dst, int cw, int lane) {
@@ -449,14 +480,14 @@ __global__ void __launch_bounds__(THREADS, 1) fused_decode_kernel(Params p) {
             if (c == 0 && tid == 0 && !(tok >= 0 && tok < p.V)) set_error(p.err, QW_ERANGE);
         } else {
             const float4 r = __ldcg((const float4*)(p.R + qb * D + k0));
-            const float4 o = __ldcg((const float4*)(p.oacc + qb * D + k0));
-            const float4 d = __ldcg((const float4*)(p.dacc + qb * D + k0));
+            const float4 o = sum_shards(p.oacc + qb * NSH * D, k0);
+            const float4 d = sum_shards(p.dacc + qb * NSH * D, k0);
             x[0] = r.x + o.x + d.x; x[1] = r.y + o.y + d.y; x[2] = r.z + o.z + d.z; x[3] = r.w + o.w + d.w;
         }
         if (own) *(float4*)(p.R + pb * D + k0) = make_float4(x[0], x[1], x[2], x[3]);
         norm_into_h(sm, x, k0, L.in_norm, p.eps, tid);
         if (tid == 0) stamp(p, l, 10);
-        ok = cs.dot_rows(w.q1 - w.q0, ok);
+        ok = cs.dot_rows(w.q1 - w.q0, ok, &p, l, 16);
         if (tid == 0) stamp(p, l, 11);
         bar_consumers();
         for (int r = tid; r < w.q1 - w.q0; r += 256) p.qkv[w.q0 + r] = sm.res[r];
@@ -519,91 +550,157 @@ __global__ void __launch_bounds__(THREADS, 1) fused_decode_kernel(Params p) {
                         }
                     }
                 }
-                float* dsts = cw < 2 ? sm.q[cw] : (cw == 2 ? sm.kn : sm.vn);
-                const float sc2 = cw < 2 ? scale_log2 : 1.f;
+                if (cw < 2) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) dsts[lane + 32 * i] = y[i] * sc2;
+                    for (int i = 0; i < 4; ++i) {
+                        const int dd = lane + 32 * i;
+                        sm.q[cw][(dd >> 2) & 1][dd >> 3][dd & 3] = y[i] * scale_log2;
+                    }
+                } else {
+                    uint16_t* db = cw == 2 ? sm.kn_b : sm.vn_b;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) db[lane + 32 * i] = f2bf(y[i]);
+                }
             }
             bar_consumers();
-            // keys: warp cw takes stage keys 8cw..8cw+7; lane holds dims 4 lane .. +3
-            float m[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.f, 0.f}, o[2][4];
-            float qr[2][4];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    o[hh][e] = 0.f;
-                    qr[hh][e] = sm.q[hh][4 * lane + e];
-                }
-            auto attend = [&](const float (&kk)[4], const float (&vv)[4], bool vis) {
-                float sc[2];
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float t = qr[hh][0] * kk[0] + qr[hh][1] * kk[1] + qr[hh][2] * kk[2] + qr[hh][3] * kk[3];
-                    sc[hh] = warp_sum(t);
-                }
-                if (!vis) return;
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const float mn = fmaxf(m[hh], sc[hh]);
-                    const float al = exp2f(m[hh] - mn);  // m = -inf first: 0
-                    const float pe = exp2f(sc[hh] - mn);
-                    lsum[hh] = lsum[hh] * al + pe;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) o[hh][e] = o[hh][e] * al + pe * vv[e];
-                    m[hh] = mn;
-                }
-            };
-            for (int pg0 = w.pg_lo; pg0 < w.pg_hi; pg0 += PAGES_PER_STAGE) {
+            if (tid == 0) stamp(p, l, 18);
+            // Each stage holds up to 4 pages (64 key slots).  Scores: warp cw takes slots
+            // 8 cw .. 8 cw + 7, one per 4-lane group (kg = lane >> 2); lane dq = lane & 3 of a group
+            // takes the 16-byte chunks u = 4 c' + dq, c' = c ^ (kg & 1), of the key row (the xor
+            // puts the 8 lanes of each shared-memory phase on 8 different bank groups), and publishes exp2(s - m_w) with its warp max m_w and sum
+            // l_w.  P.V: thread (page pi = tid >> 6, dim pair dp = tid & 63) sums the 16 slots of
+            // page pi for both query heads under one running max M shared by all threads, so
+            // the four page partials add up without rescaling at the end.
+            const int kg = lane >> 2, dq = lane & 3;
+            const int vpi = tid >> 6, dp = tid & 63;
+            float Mr[2] = {-INFINITY, -INFINITY}, lq[2] = {0.f, 0.f}, oq[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+            int buf = 0;
+            for (int pg0 = w.pg_lo; pg0 < w.pg_hi; pg0 += PAGES_PER_STAGE, buf ^= 1) {
                 const int n = min(PAGES_PER_STAGE, w.pg_hi - pg0);
                 const uint8_t* st = cs.stage_wait(ok);
-                if (ok) {
-                    for (int kk = 8 * cw; kk < 8 * cw + 8; ++kk) {
-                        const int pi = kk / QW_PAGE_SIZE, slot = kk % QW_PAGE_SIZE;
-                        const int kpos = (pg0 + pi) * QW_PAGE_SIZE + slot;
-                        if (pi >= n || kpos >= pos) continue;      // warp-uniform
-                        const int pgid = p.bt[pg0 + pi];
-                        if (pgid < 0 || pgid >= p.n_pages) continue;
-                        const uint2 kw = *(const uint2*)(st + pi * 2 * PAGE_B + slot * HD * 2 + 8 * lane);
-                        const uint2 vw = *(const uint2*)(st + pi * 2 * PAGE_B + PAGE_B + slot * HD * 2 + 8 * lane);
-                        const float kk4[4] = {bf16_lo(kw.x), bf16_hi(kw.x), bf16_lo(kw.y), bf16_hi(kw.y)};
-                        const float vv4[4] = {bf16_lo(vw.x), bf16_hi(vw.x), bf16_lo(vw.y), bf16_hi(vw.y)};
-                        attend(kk4, vv4, true);
+                if (tid == 0 && pg0 == w.pg_lo) {
+                    stamp(p, l, 20);
+                    if (p.trace) p.trace[((size_t)blockIdx.x * (p.n_layers + 1) + l) * TRACE_SLOTS + 22] = clock64();
+                }
+                {
+                    const int pi = cw >> 1, slot = 8 * (cw & 1) + kg;
+                    const int kpos = (pg0 + pi) * QW_PAGE_SIZE + slot;
+                    const bool vis = ok && pi < n && kpos <= pos && sm.spg[cs.slot()][pi] >= 0;
+                    // the new token's key comes from the bf16 copy made above, not the (older) stage
+                    const uint8_t* krow = kpos == pos ? (const uint8_t*)sm.kn_b
+                                                      : st + (pi < n ? pi : 0) * 2 * PAGE_B + slot * HD * 2;
+                    float sc[2] = {0.f, 0.f};
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int u = 4 * (c ^ (kg & 1)) + dq;
+                        float kf[8];
+                        unpack8(((const uint4*)krow)[u], kf);
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const float4 qa = *(const float4*)sm.q[hh][0][u];
+                            const float4 qb = *(const float4*)sm.q[hh][1][u];
+                            sc[hh] += qa.x * kf[0] + qa.y * kf[1] + qa.z * kf[2] + qa.w * kf[3] + qb.x * kf[4] +
+                                      qb.y * kf[5] + qb.z * kf[6] + qb.w * kf[7];
+                        }
                     }
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        sc[hh] += __shfl_xor_sync(0xffffffffu, sc[hh], 1);
+                        sc[hh] += __shfl_xor_sync(0xffffffffu, sc[hh], 2);
+                        float mw = vis ? sc[hh] : -INFINITY;
+#pragma unroll
+                        for (int o = 4; o < 32; o <<= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
+                        const float pe = vis ? exp2f(sc[hh] - mw) : 0.f;
+                        float lw = pe;
+#pragma unroll
+                        for (int o = 4; o < 32; o <<= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
+                        if (dq == 0) sm.pp[buf][hh][8 * cw + kg] = pe;
+                        if (lane == 0) {
+                            sm.am[buf][cw][hh] = mw;
+                            sm.al[buf][cw][hh] = lw;
+                        }
+                    }
+                }
+                bar_consumers();
+                if (tid == 0 && pg0 == w.pg_lo) {
+                    if (p.trace) p.trace[((size_t)blockIdx.x * (p.n_layers + 1) + l) * TRACE_SLOTS + 23] = clock64();
+                    stamp(p, l, 21);
+                }
+                // P.V over page vpi; the buffers of this stage are not rewritten before the
+                // barrier of the next stage, which every thread reaches only after this part.
+                float Ms[2];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    Ms[hh] = Mr[hh];
+#pragma unroll
+                    for (int i = 0; i < NCW; ++i) Ms[hh] = fmaxf(Ms[hh], sm.am[buf][i][hh]);
+                }
+                float fa[2], fb[2];
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (Ms[hh] == -INFINITY) {  // nothing visible yet for this head
+                        fa[hh] = fb[hh] = 0.f;
+                        continue;
+                    }
+                    const float ma = sm.am[buf][2 * vpi][hh], mb = sm.am[buf][2 * vpi + 1][hh];
+                    const float alpha = Mr[hh] == -INFINITY ? 0.f : exp2f(Mr[hh] - Ms[hh]);
+                    fa[hh] = ma == -INFINITY ? 0.f : exp2f(ma - Ms[hh]);
+                    fb[hh] = mb == -INFINITY ? 0.f : exp2f(mb - Ms[hh]);
+                    lq[hh] = lq[hh] * alpha + fa[hh] * sm.al[buf][2 * vpi][hh] + fb[hh] * sm.al[buf][2 * vpi + 1][hh];
+                    oq[hh][0] *= alpha;
+                    oq[hh][1] *= alpha;
+                    Mr[hh] = Ms[hh];
+                }
+                if (fa[0] + fb[0] + fa[1] + fb[1] > 0.f) {  // page vpi has a visible key
+                    const uint8_t* vpage = st + vpi * 2 * PAGE_B + PAGE_B + 4 * dp;
+                    const int knew = pos - (pg0 + vpi) * QW_PAGE_SIZE;  // slot of the new token, if here
+                    float s0[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, s1[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const float4* pa = (const float4*)&sm.pp[buf][0][16 * vpi + 8 * half];
+                        const float4* pb = (const float4*)&sm.pp[buf][1][16 * vpi + 8 * half];
+                        const float4 pa0 = pa[0], pa1 = pa[1], pb0 = pb[0], pb1 = pb[1];
+                        const float p0[8] = {pa0.x, pa0.y, pa0.z, pa0.w, pa1.x, pa1.y, pa1.z, pa1.w};
+                        const float p1[8] = {pb0.x, pb0.y, pb0.z, pb0.w, pb1.x, pb1.y, pb1.z, pb1.w};
+                        float (&acc)[2][2] = half ? s1 : s0;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            const int slot = 8 * half + k;
+                            const uint32_t v = slot == knew ? *(const uint32_t*)((const uint8_t*)sm.vn_b + 4 * dp)
+                                                            : *(const uint32_t*)(vpage + slot * HD * 2);
+                            const float v0 = bf16_lo(v), v1 = bf16_hi(v);
+                            acc[0][0] = fmaf(p0[k], v0, acc[0][0]);
+                            acc[0][1] = fmaf(p0[k], v1, acc[0][1]);
+                            acc[1][0] = fmaf(p1[k], v0, acc[1][0]);
+                            acc[1][1] = fmaf(p1[k], v1, acc[1][1]);
+                        }
+                    }
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) oq[hh][e] += fa[hh] * s0[hh][e] + fb[hh] * s1[hh][e];
                 }
                 cs.stage_release();
             }
-            if (w.has_new && cw == 0) {
-                const float kk4[4] = {sm.kn[4 * lane], sm.kn[4 * lane + 1], sm.kn[4 * lane + 2], sm.kn[4 * lane + 3]};
-                const float vv4[4] = {sm.vn[4 * lane], sm.vn[4 * lane + 1], sm.vn[4 * lane + 2], sm.vn[4 * lane + 3]};
-                attend(kk4, vv4, true);
-            }
+            if (tid == 0) stamp(p, l, 19);
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                if (lane == 0) {
-                    sm.am[cw][hh] = m[hh];
-                    sm.al[cw][hh] = lsum[hh];
-                }
-#pragma unroll
-                for (int e = 0; e < 4; ++e) sm.ao[cw][hh][4 * lane + e] = o[hh][e];
+                *(float2*)&sm.ao[vpi][hh][2 * dp] = make_float2(oq[hh][0], oq[hh][1]);
+                if (dp == 0) sm.alq[vpi][hh] = lq[hh];
             }
             bar_consumers();
             {
                 const int hh = tid >> 7, d = tid & 127;
-                float M = -INFINITY;
-                for (int i = 0; i < NCW; ++i)
-                    if (sm.al[i][hh] > 0.f) M = fmaxf(M, sm.am[i][hh]);
                 float Ls = 0.f, O = 0.f;
-                for (int i = 0; i < NCW; ++i)
-                    if (sm.al[i][hh] > 0.f) {
-                        const float f = exp2f(sm.am[i][hh] - M);
-                        Ls += sm.al[i][hh] * f;
-                        O += sm.ao[i][hh][d] * f;
-                    }
+#pragma unroll
+                for (int i = 0; i < PAGES_PER_STAGE; ++i) {
+                    Ls += sm.alq[i][hh];
+                    O += sm.ao[i][hh][d];
+                }
                 float* dst = p.part + ((size_t)(2 * g + hh) * p.nsa + w.s) * PART;
                 dst[d] = O;
                 if (d == 0) {
-                    dst[HD] = M;
+                    dst[HD] = Mr[hh];
                     dst[HD + 1] = Ls;
                 }
             }
@@ -654,7 +751,7 @@ __global__ void __launch_bounds__(THREADS, 1) fused_decode_kernel(Params p) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             if (tid == 0) stamp(p, l, 15);
             ok = cs.scaled_rows(nj, acc, ok);
-            add_columns(acc, p.oacc + pb * D, cw, lane);
+            add_columns(acc, p.oacc + (pb * NSH + c % NSH) * D, cw, lane);
             bar_consumers();
             if (tid == 0) {
                 signal_add(c_o(p, l), 1u);
@@ -670,16 +767,19 @@ __global__ void __launch_bounds__(THREADS, 1) fused_decode_kernel(Params p) {
             bar_consumers();
             ok = s_ok;
             const float4 r = __ldcg((const float4*)(p.R + pb * D + k0));
-            const float4 oa = __ldcg((const float4*)(p.oacc + pb * D + k0));
+            const float4 oa = sum_shards(p.oacc + pb * NSH * D, k0);
             float xm[4] = {r.x + oa.x, r.y + oa.y, r.z + oa.z, r.w + oa.w};
             if (own && l > 0) {  // every reader of the previous layer's accumulators is done
-                *(float4*)(p.oacc + qb * D + k0) = make_float4(0.f, 0.f, 0.f, 0.f);
-                *(float4*)(p.dacc + qb * D + k0) = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int sh = 0; sh < NSH; ++sh) {
+                    *(float4*)(p.oacc + (qb * NSH + sh) * D + k0) = make_float4(0.f, 0.f, 0.f, 0.f);
+                    *(float4*)(p.dacc + (qb * NSH + sh) * D + k0) = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
             }
             norm_into_h(sm, xm, k0, L.post_norm, p.eps, tid);
             if (tid == 0) stamp(p, l, 12);
             const int np2 = w.p1 - w.p0;
-            ok = cs.dot_rows(2 * np2, ok);
+            ok = cs.dot_rows(2 * np2, ok, &p, l, 17);
             if (tid == 0) stamp(p, l, 13);
             bar_consumers();
             for (int j = tid; j < np2; j += 256) {
@@ -690,7 +790,7 @@ __global__ void __launch_bounds__(THREADS, 1) fused_decode_kernel(Params p) {
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
             ok = cs.scaled_rows(np2, acc, ok);
             if (tid == 0) stamp(p, l, 14);
-            add_columns(acc, p.dacc + pb * D, cw, lane);
+            add_columns(acc, p.dacc + (pb * NSH + c % NSH) * D, cw, lane);
             bar_consumers();
             if (tid == 0) {
                 signal_add(c_x(p, l), 1u);
@@ -709,8 +809,8 @@ __global__ void __launch_bounds__(THREADS, 1) fused_decode_kernel(Params p) {
         bar_consumers();
         ok = s_ok;
         const float4 r = __ldcg((const float4*)(p.R + pl * D + k0));
-        const float4 oa = __ldcg((const float4*)(p.oacc + pl * D + k0));
-        const float4 da = __ldcg((const float4*)(p.dacc + pl * D + k0));
+        const float4 oa = sum_shards(p.oacc + pl * NSH * D, k0);
+        const float4 da = sum_shards(p.dacc + pl * NSH * D, k0);
         float xf[4] = {r.x + oa.x + da.x, r.y + oa.y + da.y, r.z + oa.z + da.z, r.w + oa.w + da.w};
         norm_into_h(sm, xf, k0, p.final_norm, p.eps, tid);
         float hreg[4][8];
@@ -762,8 +862,9 @@ __global__ void __launch_bounds__(THREADS, 1) fused_decode_kernel(Params p) {
             p.lm_part[2 * c + 1] = __int_as_float(bidx);
             unsigned prev;
             asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(c_lm(p)) : "memory");
-            if (prev == epoch * G - 1) {
-                // last CTA: global argmax (lowest id on ties), reset the accumulators, next epoch
+            sm.last_cta = prev == epoch * G - 1;
+            if (sm.last_cta) {
+                // last CTA: global argmax (lowest id on ties); below, reset the accumulators, next epoch
                 __threadfence();
                 float bv = -INFINITY;
                 int bi = 0x7FFFFFFF;
@@ -776,13 +877,16 @@ __global__ void __launch_bounds__(THREADS, 1) fused_decode_kernel(Params p) {
                     }
                 }
                 *p.argmax = bi;
-                for (int k = 0; k < D; ++k) {
-                    p.oacc[pl * D + k] = 0.f;
-                    p.dacc[pl * D + k] = 0.f;
-                }
-                __threadfence();
-                atomicAdd(c_epoch(p), 1u);
             }
+        }
+        bar_consumers();
+        if (sm.last_cta) {  // every CTA has read the last layer's accumulators
+            for (int k = tid; k < NSH * D; k += 256) {
+                p.oacc[pl * NSH * D + k] = 0.f;
+                p.dacc[pl * NSH * D + k] = 0.f;
+            }
+            bar_consumers();
+            if (tid == 0) signal_add(c_epoch(p), 1u);
         }
     }
 }
@@ -861,7 +965,7 @@ FusedDecode* fused_create(const FusedWeights& fw, int n_layers, int V, float eps
     };
     const size_t o_w = take((woT + wdT) * 2 * n_layers);
     const size_t o_layers = take(sizeof(LayerPtrs) * n_layers);
-    const size_t o_state = take(sizeof(float) * (6 * D + QKVR));
+    const size_t o_state = take(sizeof(float) * (2 * D + 4 * NSH * D + QKVR));
     const size_t o_part = take(sizeof(float) * HQ * f->nsa * PART);
     const size_t o_lm = take(sizeof(float) * 2 * f->G + 64);
     const size_t o_sync = take(sizeof(unsigned) * CNT_STRIDE * (2 + n_layers * 18));
@@ -884,8 +988,8 @@ FusedDecode* fused_create(const FusedWeights& fw, int n_layers, int V, float eps
     float* st = (float*)(f->buf + o_state);
     f->R = st;
     f->oacc = st + 2 * D;
-    f->dacc = st + 4 * D;
-    f->qkv = st + 6 * D;
+    f->dacc = st + 2 * D + 2 * NSH * D;
+    f->qkv = st + 2 * D + 4 * NSH * D;
     f->part = (float*)(f->buf + o_part);
     f->lm_part = (float*)(f->buf + o_lm);
     f->argmax = (int*)(f->lm_part + 2 * f->G);
