@@ -62,6 +62,7 @@ struct qw_ctx {
     float *x = nullptr, *qkv = nullptr, *q = nullptr, *logits = nullptr, *part = nullptr, *hidden = nullptr;
     float* gu = nullptr;   // split-K gate/up sums of small-M calls [SPLIT_MAX_M][2 * intermediate]
     uint16_t *h = nullptr, *attn = nullptr, *act = nullptr, *q_bf16 = nullptr;
+    float2* rope_tab = nullptr;   // [rows][64] RoPE (cos, sin) of the current prefill
     int *tok_seq = nullptr, *iota = nullptr, *rows_last = nullptr, *err = nullptr;
     int4* tiles = nullptr;
     int max_rows = 0, max_splits = 128, max_tiles = 0;
@@ -265,6 +266,7 @@ int qw_init(const qw_config* cfg, const qw_weights* w, qw_ctx** out) {
     const size_t oqkv = take((size_t)T * ctx->qkv_dim * 4);
     const size_t oq = take((size_t)T * ctx->attn_dim * 4);
     const size_t oqb = take((size_t)T * ctx->attn_dim * 2);
+    const size_t orope = take((size_t)T * 64 * 8);
     const size_t ologits = take((size_t)c.max_batch * V * 4);
     const size_t ogu = take((size_t)SPLIT_MAX_M * 2 * I * 4);
     const size_t opart = take((size_t)c.max_batch * Hq * ctx->max_splits * (d + 2) * 4);
@@ -286,6 +288,7 @@ int qw_init(const qw_config* cfg, const qw_weights* w, qw_ctx** out) {
     ctx->qkv = (float*)(W + oqkv);
     ctx->q = (float*)(W + oq);
     ctx->q_bf16 = (uint16_t*)(W + oqb);
+    ctx->rope_tab = (float2*)(W + orope);
     ctx->logits = (float*)(W + ologits);
     ctx->gu = (float*)(W + ogu);
     ctx->part = (float*)(W + opart);
@@ -383,20 +386,31 @@ static int run_layers(qw_ctx* ctx, int n, const int* ids, const int* positions, 
     const int D = c.hidden, Hq = c.n_heads, Hkv = c.n_kv_heads, I = c.intermediate;
     const int split = n <= SPLIT_MAX_M;   // small-M projections take hi/lo activation pairs
     QW_TRY(launch_embed(ids, n, ctx->E, c.vocab, D, ctx->x, ctx->err, st), "embed launch");
+    const bool fused_qkv = mode == 0 && ctx->prefill_attn == 0 && !split;  // q|k|v GEMM epilogue does Steps 4-5
+    if (fused_qkv) QW_TRY(launch_rope_table(positions, n, ctx->inv_freq, ctx->rope_tab, st), "rope table launch");
     for (int l = 0; l < c.n_layers; ++l) {
         const LayerW& Lw = ctx->L[l];
         KvView kvv{kv->base + (int64_t)l * kv->layer_elems, kv->page_elems, kv->n_pages, bt, bt_stride};
         QW_TRY(launch_rmsnorm_bf16(ctx->x, nullptr, n, D, Lw.in_norm, c.rms_eps, ctx->h, split, st),
                "rmsnorm launch");
-        // small M: split-K with atomic accumulation (zeroed targets) so every SM streams weights
-        GemmEpilogue e{ctx->qkv, nullptr, ctx->qkv_dim, ctx->err, split};
-        if (split) QW_CUDA(cudaMemsetAsync(ctx->qkv, 0, (size_t)n * ctx->qkv_dim * 4, st));
-        QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_qkv, 256, n, ctx->qkv_dim, D, split ? EPI_ADD_ATOMIC : EPI_STORE_F32, e, st),
-               "qkv gemm");
         const bool tc_attn = mode == 0 && ctx->prefill_attn == 0;
-        QW_TRY(launch_qkv_post(ctx->qkv, n, positions, tok_seq, Hq, Hkv, Lw.q_norm, Lw.k_norm, ctx->inv_freq,
-                               c.rms_eps, ctx->q, tc_attn ? ctx->q_bf16 : nullptr, kvv, ctx->err, st),
-               "qk-norm/rope/kv-write launch");
+        GemmEpilogue e{ctx->qkv, nullptr, ctx->qkv_dim, ctx->err, split};
+        if (fused_qkv) {
+            // prefill: QK-Norm, RoPE, bf16 q and the cache write happen in the GEMM epilogue
+            e.rope = QkvRope{positions, tok_seq, kvv, Lw.q_norm, Lw.k_norm, ctx->rope_tab, c.rms_eps, ctx->q_bf16,
+                             Hq, Hkv};
+            QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_qkv, 256, n, ctx->qkv_dim, D, EPI_QKV_ROPE, e, st), "qkv gemm");
+        } else {
+            // small M: split-K with atomic accumulation (zeroed targets) so every SM streams weights
+            if (split) QW_CUDA(cudaMemsetAsync(ctx->qkv, 0, (size_t)n * ctx->qkv_dim * 4, st));
+            QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_qkv, 256, n, ctx->qkv_dim, D, split ? EPI_ADD_ATOMIC : EPI_STORE_F32, e,
+                             st),
+                   "qkv gemm");
+            QW_TRY(launch_qkv_post(ctx->qkv, n, positions, tok_seq, Hq, Hkv, Lw.q_norm, Lw.k_norm, ctx->inv_freq,
+                                   c.rms_eps, tc_attn ? nullptr : ctx->q, tc_attn ? ctx->q_bf16 : nullptr, kvv,
+                                   ctx->err, st),
+                   "qk-norm/rope/kv-write launch");
+        }
         if (tc_attn)
             QW_TRY(launch_attn_prefill_tc(ctx->q_bf16, n, positions, ctx->tiles, n_tiles, Hq, Hkv, kvv, ctx->attn,
                                           split, ctx->err, st),

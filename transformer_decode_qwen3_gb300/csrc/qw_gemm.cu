@@ -90,10 +90,100 @@ QW_DEV void epilogue_chunk(const float (&v)[32], int m, int n, const GemmEpilogu
 
 QW_DEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// Store 32 values as bf16 (four 16-byte stores).
+QW_DEV void store_bf16x32(uint16_t* dst, const float (&y)[32]) {
+    uint4* d = (uint4*)dst;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        d[i] = make_uint4(pack_bf16x2(y[8 * i], y[8 * i + 1]), pack_bf16x2(y[8 * i + 2], y[8 * i + 3]),
+                          pack_bf16x2(y[8 * i + 4], y[8 * i + 5]), pack_bf16x2(y[8 * i + 6], y[8 * i + 7]));
+}
+
+// EPI_QKV_ROPE on one accumulator tile: this thread's row m, columns n0 .. n0 + BN - 1 = BN / 128
+// whole heads of the fused q|k|v output (Steps 4-5 of the article).  q and k heads: RMS-normalised
+// over their 128 values (QK-Norm), scaled by the norm weight, rotated by RoPE with pairs
+// (d, d + 64) at angle float32(pos * inv_freq[d]) (cos and sin from a per-row table); q goes out as bf16, k and v enter the cache
+// page of (tok_seq[m], pos) as bf16.  TMEM loads are warp-collective, so every thread loads
+// even when its row is past M; only the stores are per row.
+template <int BN>
+QW_DEV void qkv_rope_tile(uint32_t trow, int m, int M, int n0, int N, const GemmEpilogue& ep) {
+    const QkvRope& r = ep.rope;
+    const bool live = m < M;
+    int pos = 0;  // used for the page lookup
+    uint16_t* kv_row = nullptr;  // this row's slot in its cache page (k of head 0)
+    if (live) {
+        pos = r.positions[m];
+        if (n0 + BN > r.Hq * 128) {  // the tile holds k or v heads
+            const int seq = r.tok_seq[m];
+            const int page = pos >= 0 && pos < r.kv.bt_stride * QW_PAGE_SIZE
+                                 ? r.kv.block_tables[(size_t)seq * r.kv.bt_stride + pos / QW_PAGE_SIZE]
+                                 : -1;
+            if (page < 0 || page >= r.kv.n_pages)
+                set_error(ep.err, QW_ERANGE);
+            else
+                kv_row = r.kv.base + (size_t)page * r.kv.page_stride + (size_t)(pos % QW_PAGE_SIZE) * QW_HEAD_DIM;
+        }
+    }
+#pragma unroll 1
+    for (int hd = 0; hd < BN / 128; ++hd) {
+        const int col = n0 + 128 * hd;
+        if (col >= N) break;  // uniform
+        const int head = col / 128;
+        const uint32_t t0 = trow + (uint32_t)(128 * hd);
+        // destination of the 128 values of this head in this row
+        uint16_t* dst = nullptr;
+        if (head < r.Hq)
+            dst = live ? r.q_bf16 + (size_t)m * r.Hq * 128 + (size_t)head * 128 : nullptr;
+        else if (kv_row)  // k heads Hq .. Hq+Hkv-1, then v heads: (K/V, head) rows of 16 slots
+            dst = kv_row + (size_t)(head - r.Hq) * QW_PAGE_SIZE * QW_HEAD_DIM;
+        if (head >= r.Hq + r.Hkv) {  // v: plain bf16 copy
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                float v[32];
+                tmem_ld32(t0 + 32 * c, v);
+                if (dst) store_bf16x32(dst + 32 * c, v);
+            }
+            continue;
+        }
+        float ss = 0.f;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+            float v[32];
+            tmem_ld32(t0 + 32 * c, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ss = fmaf(v[i], v[i], ss);
+        }
+        const float sc = 1.0f / sqrtf(ss / (float)QW_HEAD_DIM + r.eps);
+        const float* w = head < r.Hq ? r.q_norm : r.k_norm;
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {  // dims 32 j .. 32 j + 31 pair with 32 j + 64 ..
+            float a[32], b[32];
+            tmem_ld32(t0 + 32 * j, a);
+            tmem_ld32(t0 + 32 * j + 64, b);
+            const float4* cs4 = (const float4*)(r.rope + (size_t)(live ? m : 0) * 64 + 32 * j);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                const float4 t = __ldg(cs4 + i / 2);  // (cos, sin) of pairs d and d + 1
+                const int d = 32 * j + i;
+                const float x1 = a[i] * sc * __ldg(w + d), x2 = b[i] * sc * __ldg(w + d + 64);
+                const float y1 = a[i + 1] * sc * __ldg(w + d + 1), y2 = b[i + 1] * sc * __ldg(w + d + 65);
+                a[i] = x1 * t.x - x2 * t.y;
+                b[i] = x1 * t.y + x2 * t.x;
+                a[i + 1] = y1 * t.z - y2 * t.w;
+                b[i + 1] = y1 * t.w + y2 * t.z;
+            }
+            if (dst) {
+                store_bf16x32(dst + 32 * j, a);
+                store_bf16x32(dst + 32 * j + 64, b);
+            }
+        }
+    }
+}
+
 template <int BN, int EPI, bool SPLIT>
 __global__ void __launch_bounds__(256, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        int M, int N, int K, int tiles_m, int tiles_n, int ksplit, GemmEpilogue ep) {
+                        int M, int N, int K, int tiles_m, int tiles_n, int ksplit, int share_a, GemmEpilogue ep) {
     using C = GemmCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -133,11 +223,12 @@ __global__ void __launch_bounds__(256, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // unit t -> (m tile, n tile, K blocks [kb0, kb1)); consecutive CTAs share the B (weight) tile
+    // unit t -> (m tile, n tile, K blocks [kb0, kb1)).  Consecutive CTAs share the A tile
+    // (share_a: n tile fastest; the whole B fits in L2) or the B tile (m tile fastest).
     auto unit = [&](int t, int& tm, int& tn, int& kb0, int& kb1) {
         const int ks = t % ksplit, rest = t / ksplit;
-        tn = rest / tiles_m;
-        tm = rest % tiles_m;
+        tn = share_a ? rest % tiles_n : rest / tiles_m;
+        tm = share_a ? rest / tiles_n : rest % tiles_m;
         kb0 = ks * nk / ksplit;
         kb1 = (ks + 1) * nk / ksplit;
     };
@@ -212,8 +303,9 @@ __global__ void __launch_bounds__(256, 1)
             if (!ok) break;
             const uint32_t trow = tmem + (uint32_t)(acc * BN) + ((uint32_t)(ew * 32) << 16);
             const int n0 = tn * BN;
+            if constexpr (EPI == EPI_QKV_ROPE) qkv_rope_tile<BN>(trow, tm * C::BM + et, M, n0, N, ep);
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
+            for (int c0 = 0; c0 < BN && EPI != EPI_QKV_ROPE; c0 += 32) {
                 if (n0 + c0 >= N) break;  // uniform over the warpgroup
                 float v[32];
                 tmem_ld32(trow + c0, v);
@@ -303,8 +395,11 @@ static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N,
     }
     const int work = tiles_m * tiles_n * ksplit;
     const int grid = work < n_sm ? work : n_sm;
+    // A streams from HBM once when the CTAs running together share its tiles; that needs the
+    // weight matrix B to stay L2-resident (projection weights are 4..13 MB; the LM head is not).
+    const int share_a = (int64_t)N * K * 2 <= (int64_t)32 << 20 && tiles_m > 1;
     gemm_bf16_tc_kernel<BN, EPI, SPLIT><<<grid, C::THREADS, C::SMEM, st>>>(ta, tb, M, N, K, tiles_m, tiles_n, ksplit,
-                                                                         ep);
+                                                                         share_a, ep);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ECUDA;
 }
@@ -316,11 +411,19 @@ static int launch_split(const CUtensorMap& ta, const CUtensorMap& tb, int bn, in
         if (epi == EPI_STORE_F32) return launch_bn<256, EPI_STORE_F32, SPLIT>(ta, tb, M, N, K, ep, st);
         if (epi == EPI_RESID_ADD) return launch_bn<256, EPI_RESID_ADD, SPLIT>(ta, tb, M, N, K, ep, st);
         if (epi == EPI_ADD_ATOMIC) return launch_bn<256, EPI_ADD_ATOMIC, SPLIT>(ta, tb, M, N, K, ep, st);
+        if (epi == EPI_QKV_ROPE) {
+            if constexpr (SPLIT) return QW_EINVAL;
+            else return launch_bn<256, EPI_QKV_ROPE, false>(ta, tb, M, N, K, ep, st);
+        }
         return launch_bn<256, EPI_SWIGLU, SPLIT>(ta, tb, M, N, K, ep, st);
     }
     if (epi == EPI_STORE_F32) return launch_bn<128, EPI_STORE_F32, SPLIT>(ta, tb, M, N, K, ep, st);
     if (epi == EPI_RESID_ADD) return launch_bn<128, EPI_RESID_ADD, SPLIT>(ta, tb, M, N, K, ep, st);
     if (epi == EPI_ADD_ATOMIC) return launch_bn<128, EPI_ADD_ATOMIC, SPLIT>(ta, tb, M, N, K, ep, st);
+    if (epi == EPI_QKV_ROPE) {
+        if constexpr (SPLIT) return QW_EINVAL;
+        else return launch_bn<128, EPI_QKV_ROPE, false>(ta, tb, M, N, K, ep, st);
+    }
     return launch_bn<128, EPI_SWIGLU, SPLIT>(ta, tb, M, N, K, ep, st);
 }
 

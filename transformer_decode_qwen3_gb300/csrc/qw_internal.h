@@ -16,7 +16,30 @@ int report_error(int code, const char* msg);
 
 // EPI_ADD_ATOMIC: out += acc with fp32 atomics; the launch splits K so that every SM gets
 // work (small-M products: decode batches).
-enum { EPI_STORE_F32 = 0, EPI_RESID_ADD = 1, EPI_SWIGLU = 2, EPI_ADD_ATOMIC = 3 };
+// EPI_QKV_ROPE: the q|k|v projection of a prefill with everything that follows it up to the
+// attention: QK-Norm and half-split RoPE of the q and k heads, q stored as bf16, k and v
+// written into their cache pages (non-split products; output columns = whole heads).
+enum { EPI_STORE_F32 = 0, EPI_RESID_ADD = 1, EPI_SWIGLU = 2, EPI_ADD_ATOMIC = 3, EPI_QKV_ROPE = 4 };
+
+struct KvView {
+    uint16_t* base;        // this layer's pages: [n_pages][2][n_kv][16][128]
+    int64_t page_stride;   // elements per page (2 * n_kv * 16 * 128)
+    int n_pages;
+    const int* block_tables;
+    int bt_stride;
+};
+
+struct QkvRope {
+    const int* positions;   // [M] position of each row
+    const int* tok_seq;     // [M] sequence (block-table row) of each row
+    KvView kv;
+    const float* q_norm;    // [128] fp32
+    const float* k_norm;    // [128] fp32
+    const float2* rope;     // [M][64] (cos, sin) of float32(pos * inv_freq[i]) (launch_rope_table)
+    float eps;
+    uint16_t* q_bf16;       // [M][Hq * 128]
+    int Hq, Hkv;
+};
 
 struct GemmEpilogue {
     float* out;      // EPI_STORE_F32: out[m][n]; EPI_RESID_ADD: out[m][n] += acc
@@ -24,6 +47,7 @@ struct GemmEpilogue {
     int ldo;         // row stride (elements) of out / act
     int* err;        // device error word
     int split;       // A holds hi/lo row pairs (see split_rows); SwiGLU output is written the same way
+    QkvRope rope;    // EPI_QKV_ROPE only
 };
 
 // Rows an M-row activation occupies in the split (hi/lo) layout.
@@ -41,19 +65,13 @@ int gemm_bf16(const void* A, int lda_elems, const CUtensorMap& tmB, int bn, int 
               const GemmEpilogue& ep, cudaStream_t st);
 
 // ---------------------------------------------------------------- per-op kernels
-struct KvView {
-    uint16_t* base;        // this layer's pages: [n_pages][2][n_kv][16][128]
-    int64_t page_stride;   // elements per page (2 * n_kv * 16 * 128)
-    int n_pages;
-    const int* block_tables;
-    int bt_stride;
-};
-
+// (cos, sin) of the RoPE angles float32(positions[t] * inv_freq[i]), i < 64, for n rows.
+int launch_rope_table(const int* positions, int n, const float* inv_freq, float2* tab, cudaStream_t st);
 int launch_embed(const int* ids, int n, const uint16_t* E, int vocab, int D, float* x, int* err, cudaStream_t st);
 int launch_rmsnorm_bf16(const float* x, const int* rows /*nullable*/, int n, int D, const float* w, float eps,
                         uint16_t* out, int split, cudaStream_t st);
 int launch_qkv_post(const float* qkv, int n_tok, const int* positions, const int* tok_seq, int Hq, int Hkv,
-                    const float* q_norm, const float* k_norm, const float* inv_freq, float eps, float* q_out,
+                    const float* q_norm, const float* k_norm, const float* inv_freq, float eps, float* q_out /*nullable*/,
                     uint16_t* q_bf16 /*nullable*/, const KvView& kv, int* err, cudaStream_t st);
 int launch_attn_prefill(const float* q, const int* positions, const int4* tiles, int n_tiles, int Hq, int Hkv,
                         const KvView& kv, uint16_t* out, int split, int* err, cudaStream_t st);

@@ -120,9 +120,11 @@ __global__ void qkv_post_kernel(const float* __restrict__ qkv, const int* __rest
         }
     }
     if (hh < Hq) {
-        float* dst = q_out + ((size_t)t * Hq + hh) * QW_HEAD_DIM;
+        if (q_out) {
+            float* dst = q_out + ((size_t)t * Hq + hh) * QW_HEAD_DIM;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = y[i];
+            for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = y[i];
+        }
         if (q_bf16) {
             uint16_t* qb = q_bf16 + ((size_t)t * Hq + hh) * QW_HEAD_DIM;
 #pragma unroll
@@ -146,6 +148,20 @@ __global__ void qkv_post_kernel(const float* __restrict__ qkv, const int* __rest
                                                                (pos % QW_PAGE_SIZE)) * QW_HEAD_DIM;
 #pragma unroll
     for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = f2bf(y[i]);
+}
+
+__global__ void rope_table_kernel(const int* __restrict__ positions, int n, const float* __restrict__ inv_freq,
+                                  float2* __restrict__ tab) {
+    const int t = blockIdx.x, i = threadIdx.x;
+    float sn, cs;
+    sincosf(__fmul_rn((float)positions[t], inv_freq[i]), &sn, &cs);
+    tab[(size_t)t * 64 + i] = make_float2(cs, sn);
+}
+
+int launch_rope_table(const int* positions, int n, const float* inv_freq, float2* tab, cudaStream_t st) {
+    if (n <= 0) return QW_OK;
+    rope_table_kernel<<<n, 64, 0, st>>>(positions, n, inv_freq, tab);
+    return check_launch();
 }
 
 int launch_qkv_post(const float* qkv, int n_tok, const int* positions, const int* tok_seq, int Hq, int Hkv,
