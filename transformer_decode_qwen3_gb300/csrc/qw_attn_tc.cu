@@ -5,7 +5,8 @@
 // (rows 64..127), which share the KV head (grouped-query attention).  Keys and
 // values stream from the paged cache in tiles of 64 positions (4 pages), loaded by
 // TMA through a 4-D view of the pool ([page][K/V, head][slot][dim], 16-slot boxes,
-// 128-byte swizzle) into a 4-deep ring, so loads run three tiles ahead.
+// 128-byte swizzle) into a 2-deep ring; two CTAs share an SM so that one's softmax
+// overlaps the other's loads and MMAs.
 //
 //   warp 0      TMA producer (Q once, then K/V tiles)
 //   warp 1      MMA issuer: S_j = Q K_j^T into one of two TMEM buffers, then
@@ -26,10 +27,12 @@ constexpr int BM = 128, BN = 64, HD = 128;
 constexpr int CHUNK = 128 * 64 * 2;           // 128 rows x 64 bf16, one 128-byte-swizzle column block
 constexpr int KCHUNK = BN * 64 * 2;           // 64 keys x 64 dims: one column block of a K or V tile
 constexpr int Q_BYTES = 2 * CHUNK;            // 32 KB
-constexpr int KV_STAGES = 4;
+constexpr int KV_STAGES = 2;                  // two CTAs per SM: their softmax warps interleave
 constexpr int KV_STAGE = 4 * KCHUNK;          // K (2 blocks) + V (2 blocks) = 32 KB
 constexpr int P_BYTES = BM * BN * 2;          // 16 KB: one 64-key block
-constexpr int SMEM = Q_BYTES + KV_STAGES * KV_STAGE + P_BYTES + 1024 + 256;
+// The dynamic shared-memory window starts 1024-byte aligned (checked at run time), so no
+// alignment slack is reserved: two CTAs (2 x (112.25 + 1) KB) fit in one SM.
+constexpr int SMEM = Q_BYTES + KV_STAGES * KV_STAGE + P_BYTES + 256;
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 256;           // S0 [0,64), S1 [64,128), O [128,256)
 
@@ -97,13 +100,18 @@ QW_DEV float ex2_approx(float x) {
     return y;
 }
 
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, 2)
     attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
                            const int* __restrict__ positions, const int4* __restrict__ tiles,
                            const int* __restrict__ block_tables, int bt_stride, int n_pages, int Hq, int Hkv,
                            uint16_t* __restrict__ out, float scale_log2, int split, int* err) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = smem_raw;
+    // 128-byte-swizzled tiles need 1024-byte aligned shared memory
+    if (smem_u32(sm) & 1023) {
+        if (threadIdx.x == 0) set_error(err, QW_EINVAL);
+        return;
+    }
     uint8_t* sQ = sm;
     uint8_t* sKV = sm + Q_BYTES;                       // stage s: K blocks at s*KV_STAGE, V blocks at +2*KCHUNK
     uint8_t* sP = sm + Q_BYTES + KV_STAGES * KV_STAGE;
@@ -264,17 +272,22 @@ __global__ void __launch_bounds__(THREADS, 1)
             tmem_ld32_nowait(sbase + 0, sv + 0);
             tmem_ld32_nowait(sbase + 32, sv + 32);
             tmem_wait_ld();
-            float rmax = -INFINITY;
+            // row max over 8 independent chains (the loop is latency-bound: one or two warps per SMSP)
+            float mx[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) mx[c] = -INFINITY;
             if (full_tile) {
 #pragma unroll
-                for (int i = 0; i < BN; ++i) rmax = fmaxf(rmax, sv[i]);
+                for (int i = 0; i < BN; ++i) mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
             } else {
 #pragma unroll
                 for (int i = 0; i < BN; ++i) {
                     if (kbase + i > qp) sv[i] = -INFINITY;
-                    rmax = fmaxf(rmax, sv[i]);
+                    mx[i & 7] = fmaxf(mx[i & 7], sv[i]);
                 }
             }
+            const float rmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             // Lazy reference max: m moves (and O is rescaled) only when the tile's max exceeds it by
             // more than 8 (log2 units), so P <= 2^8; O and l share the reference, so O / l is exact.
             const float cand = rmax * scale_log2;
@@ -284,6 +297,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                 m = cand;
             }
             const float neg = m == -INFINITY ? 0.f : -m;
+            // p = 2^(s * scale - m) (masked keys: 2^-inf = 0), row sum, P row r packed as bf16;
+            // all before waiting for the previous P V, which this work overlaps
+            float sums[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) sums[c] = 0.f;
+            uint32_t pk[BN / 2];
+#pragma unroll
+            for (int i = 0; i < BN; i += 2) {
+                const float p0 = ex2_approx(fmaf(sv[i], scale_log2, neg));
+                const float p1 = ex2_approx(fmaf(sv[i + 1], scale_log2, neg));
+                sums[(i >> 1) & 7] += p0 + p1;
+                pk[i >> 1] = pack_bf16x2(p0, p1);
+            }
+            const float sum = ((sums[0] + sums[1]) + (sums[2] + sums[3])) + ((sums[4] + sums[5]) + (sums[6] + sums[7]));
             // P_j may overwrite P_{j-1} and O may be rescaled once P_{j-1} V_{j-1} is done
             if (j > 0) {
                 if (!mbar_wait(o_done, (j - 1) & 1, err) || *abort_flag) break;
@@ -291,7 +318,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // tcgen05.ld/st are warp-collective: rescale when any row of the warp needs it
                 if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-                    for (int half = 0; half < 2; ++half) {  // 64 columns at a time (registers: S is live)
+                    for (int half = 0; half < 2; ++half) {  // 64 columns at a time
                         float o[64];
                         const uint32_t ob = tmem + 2 * BN + lane_off + 64 * half;
                         tmem_ld32_nowait(ob + 0, o + 0);
@@ -305,20 +332,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
             }
-            // p = 2^(s * scale - m), row sum, P row r as bf16 in the 128-byte-swizzled layout
-            float sum = 0.f;
 #pragma unroll
-            for (int i = 0; i < BN; ++i) {
-                sv[i] = sv[i] == -INFINITY ? 0.f : ex2_approx(fmaf(sv[i], scale_log2, neg));
-                sum += sv[i];
-            }
-#pragma unroll
-            for (int unit = 0; unit < BN / 8; ++unit) {   // 16-byte units of the row's 128 bytes
-                const float* p8 = sv + 8 * unit;
-                const uint4 w = make_uint4(pack_bf16x2(p8[0], p8[1]), pack_bf16x2(p8[2], p8[3]),
-                                           pack_bf16x2(p8[4], p8[5]), pack_bf16x2(p8[6], p8[7]));
-                *(uint4*)(sP + r * 128 + ((unit ^ (r & 7)) << 4)) = w;
-            }
+            for (int unit = 0; unit < BN / 8; ++unit)   // 16-byte units of the row's 128 bytes
+                *(uint4*)(sP + r * 128 + ((unit ^ (r & 7)) << 4)) =
+                    make_uint4(pk[4 * unit], pk[4 * unit + 1], pk[4 * unit + 2], pk[4 * unit + 3]);
             l = l * alpha + sum;
             fence_proxy_async();   // the MMA reads P through the async proxy
             tc_fence_before();
