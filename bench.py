@@ -25,6 +25,7 @@ over ranks and value counts the tokens of all ranks.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -59,6 +60,26 @@ WORKLOAD_NAMES = {
     "decode_bs64": "decode bs64, ragged paged caches 128..4096, T 0.7 / top-k 50 / top-p 0.9 (configs[3])",
     "prefill": "prefill 8 x 2048, causal GQA (configs[2])",
 }
+
+
+# DRAM bytes (read + write) per launch of each workload's roofline kernel, from one ncu
+# capture summarised under profiles/; reported only while the kernel's source file is the
+# one that was captured (its sha256 below), else null.
+NCU_TRAFFIC = {
+    "decode_bs1": ("transformer_decode_qwen3_gb300/csrc/qw_fused.cu",
+                   "221b54e4d04fc1a5462d056882278a7913ff6eedbca007d92db2ce57b28af590", 1.253211e9 + 4.761856e6),
+    "decode_bs64": ("transformer_decode_qwen3_gb300/csrc/qw_kernels.cu",
+                    "ad37983cb9ec0814d89b38714d83f34560ae61255ed7761e9014616ae8f7e335", 552.45e6 + 3.01e6),
+}
+
+
+def ncu_traffic(name):
+    ent = NCU_TRAFFIC.get(name)
+    if ent is None:
+        return None
+    path, sha, nbytes = ent
+    with open(os.path.join(ROOT, path), "rb") as f:
+        return nbytes if hashlib.sha256(f.read()).hexdigest() == sha else None
 
 
 def peaks():
@@ -404,13 +425,13 @@ def measure(name, bd, model, K, W, world, hbm, tf_burst):
         kms, _ = timed(wl.kernel_only, K, world)
         ach = wl.bytes_per_step(K) / (kms / K / 1e3) / 1e9
         out["roofline"] = {"bound": "hbm", "kernel": "decode step (the fused batch-1 kernel)", "achieved": ach,
-                           "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": None,
+                           "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": ncu_traffic(name),
                            "algorithmic_bytes": wl.bytes_per_step(K), "kernel_ms": kms / K}
     elif name == "decode_bs64":
         kms, _ = timed(wl.attention_only, K, world)
         ach = wl.attention_bytes() / (kms / K / 1e3) / 1e9
         out["roofline"] = {"bound": "hbm", "kernel": "split-KV decode attention (one layer)", "achieved": ach,
-                           "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": None,
+                           "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": ncu_traffic(name),
                            "algorithmic_bytes": wl.attention_bytes(), "kernel_ms": kms / K,
                            "step_hbm_frac": wl.bytes_per_step() / (ms / K / 1e3) / 1e9 / hbm}
     else:

@@ -32,11 +32,13 @@ def test_gemm_store(bd, M, N, K, bn):
     assert torch.isfinite(C).all() and err < 1e-5, f"rel err {err:.3e}"
 
 
-def test_gemm_residual_add(bd):
-    A, B, ref = _operands(200, 1024, 2048, 3)
-    X = torch.randn(200, 1024, device="cuda")
+@pytest.mark.parametrize("M,N,K,bn", [(200, 1024, 2048, 128), (200, 1024, 2048, 256), (1, 1024, 3072, 256),
+                                      (513, 1024, 3072, 256), (300, 192, 1024, 256)])
+def test_gemm_residual_add(bd, M, N, K, bn):
+    A, B, ref = _operands(M, N, K, 3 + M)
+    X = torch.randn(M, N, device="cuda")
     C = X.clone()
-    bd.debug_gemm(A, B, C, epi=1, bn=128)
+    bd.debug_gemm(A, B, C, epi=1, bn=bn)
     torch.cuda.synchronize()
     torch.testing.assert_close(C, X + ref, rtol=1e-4, atol=1e-4)
 

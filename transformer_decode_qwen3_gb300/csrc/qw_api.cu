@@ -45,6 +45,7 @@ struct LayerW {
     uint16_t *wqkv, *wo, *wgu, *wd;  // [qkv_dim][D], [D][Hq*d], [2I][D] (gate, up rows interleaved), [D][I]
     float *in_norm, *post_norm, *q_norm, *k_norm;
     CUtensorMap tm_qkv, tm_o, tm_gu, tm_d;
+    CUtensorMap tm_o256, tm_d256;   // o_proj / down_proj with 256-row boxes (large-M products)
 };
 
 struct qw_ctx {
@@ -246,7 +247,9 @@ int qw_init(const qw_config* cfg, const qw_weights* w, qw_ctx** out) {
         if (make_tmap_bf16(&Lw.tm_qkv, Lw.wqkv, D, ctx->qkv_dim, rowb, 64, 256) ||
             make_tmap_bf16(&Lw.tm_o, Lw.wo, ctx->attn_dim, D, (size_t)ctx->attn_dim * 2, 64, 128) ||
             make_tmap_bf16(&Lw.tm_gu, Lw.wgu, D, 2 * I, rowb, 64, 256) ||
-            make_tmap_bf16(&Lw.tm_d, Lw.wd, I, D, (size_t)I * 2, 64, 128)) {
+            make_tmap_bf16(&Lw.tm_d, Lw.wd, I, D, (size_t)I * 2, 64, 128) ||
+            make_tmap_bf16(&Lw.tm_o256, Lw.wo, ctx->attn_dim, D, (size_t)ctx->attn_dim * 2, 64, 256) ||
+            make_tmap_bf16(&Lw.tm_d256, Lw.wd, I, D, (size_t)I * 2, 64, 256)) {
             free_ctx(ctx);
             return fail(QW_ECUDA, "cuTensorMapEncodeTiled failed for a weight");
         }
@@ -424,9 +427,14 @@ static int run_layers(qw_ctx* ctx, int n, const int* ids, const int* positions, 
                                       split, ctx->err, ctx->n_sm, st),
                    "decode attention launch");
         e = GemmEpilogue{ctx->x, nullptr, D, ctx->err, split};
-        QW_TRY(gemm_bf16(ctx->attn, ctx->attn_dim, Lw.tm_o, 128, n, D, ctx->attn_dim,
-                         split ? EPI_ADD_ATOMIC : EPI_RESID_ADD, e, st),
-               "o_proj gemm");
+        // N = hidden is narrow: 128-wide tiles give split-K decode batches more units,
+        // 256-wide tiles halve the activation re-reads of a prefill
+        if (split)
+            QW_TRY(gemm_bf16(ctx->attn, ctx->attn_dim, Lw.tm_o, 128, n, D, ctx->attn_dim, EPI_ADD_ATOMIC, e, st),
+                   "o_proj gemm");
+        else
+            QW_TRY(gemm_bf16(ctx->attn, ctx->attn_dim, Lw.tm_o256, 256, n, D, ctx->attn_dim, EPI_RESID_ADD, e, st),
+                   "o_proj gemm");
         QW_TRY(launch_rmsnorm_bf16(ctx->x, nullptr, n, D, Lw.post_norm, c.rms_eps, ctx->h, split, st),
                "rmsnorm launch");
         if (split) {
@@ -439,8 +447,10 @@ static int run_layers(qw_ctx* ctx, int n, const int* ids, const int* positions, 
             QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_gu, 256, n, 2 * I, D, EPI_SWIGLU, e, st), "gate/up gemm");
         }
         e = GemmEpilogue{ctx->x, nullptr, D, ctx->err, split};
-        QW_TRY(gemm_bf16(ctx->act, I, Lw.tm_d, 128, n, D, I, split ? EPI_ADD_ATOMIC : EPI_RESID_ADD, e, st),
-               "down gemm");
+        if (split)
+            QW_TRY(gemm_bf16(ctx->act, I, Lw.tm_d, 128, n, D, I, EPI_ADD_ATOMIC, e, st), "down gemm");
+        else
+            QW_TRY(gemm_bf16(ctx->act, I, Lw.tm_d256, 256, n, D, I, EPI_RESID_ADD, e, st), "down gemm");
         if (ctx->hidden)
             QW_CUDA(cudaMemcpyAsync(ctx->hidden + (size_t)l * ctx->max_rows * D, ctx->x, (size_t)n * D * 4,
                                     cudaMemcpyDeviceToDevice, st));
