@@ -229,7 +229,9 @@ int qw_debug_hidden(qw_ctx* ctx, int32_t layer, float* out, int32_t n_rows, void
  * split = 1: A holds ceil(M/64) blocks of 128 rows, rows 0..63 of a block the bf16 "hi"
  *   parts of 64 activation rows and rows 64..127 their "lo" remainders; the product uses
  *   hi + lo (the layout decode batches use), and with epi = 2 the output is written in the
- *   same hi/lo layout.  split = 0: plain A[M][K]. */
+ *   same hi/lo layout.  split = 0: plain A[M][K].  split = 2: plain A, and with bn = 256,
+ *   M > 128 and epi != 3 the product runs in clusters of two CTAs that share (multicast)
+ *   each weight tile (the prefill configuration). */
 int qw_debug_gemm(const uint16_t* A, const uint16_t* B, void* C, int32_t M, int32_t N, int32_t K, int32_t epi,
                   int32_t bn, int32_t split, void* stream);
 

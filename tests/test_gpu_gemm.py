@@ -96,3 +96,25 @@ def test_gemm_split_k_atomic(bd, M, N, K, bn):
     ref = a @ B.float().T
     err = (C - X - ref).norm() / ref.norm()
     assert err < 2e-5, f"rel err {err:.3e}"
+
+
+@pytest.mark.parametrize("M,N,K,epi", [(300, 6144, 1024, 0), (257, 384, 1024, 0), (384, 256, 64, 0),
+                                       (129, 512, 128, 0), (513, 1024, 3072, 1), (300, 256, 1024, 1),
+                                       (1000, 768, 256, 2), (2048, 4096, 1024, 0)])
+def test_gemm_cta_pairs(bd, M, N, K, epi):
+    """Large-M mode: CTA pairs multicast the shared weight tile (odd tile counts included)."""
+    A, B, ref = _operands(M, N, K, 11 * M + N)
+    if epi == 2:
+        C = torch.zeros(M, N // 2, dtype=torch.bfloat16, device="cuda")
+        bd.debug_gemm(A, B, C, epi=2, bn=256, split=2)
+        torch.cuda.synchronize()
+        g, u = ref[:, 0::2], ref[:, 1::2]
+        torch.testing.assert_close(C.float(), g * torch.sigmoid(g) * u, rtol=1e-2, atol=1e-3)
+        return
+    X = torch.randn(M, N, device="cuda") if epi == 1 else torch.full((M, N), float("nan"), device="cuda")
+    C = X.clone()
+    bd.debug_gemm(A, B, C, epi=epi, bn=256, split=2)
+    torch.cuda.synchronize()
+    expect = X + ref if epi == 1 else ref
+    err = (C - expect).norm() / expect.norm()
+    assert torch.isfinite(C).all() and err < 1e-5, f"rel err {err:.3e}"

@@ -294,10 +294,11 @@ def kernel_launches() -> int:
     return int(load().qw_kernel_launches())
 
 
-def debug_gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, epi: int = 0, bn: int = 256, split: bool = False,
+def debug_gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, epi: int = 0, bn: int = 256, split: int = 0,
                M: int | None = None, stream=None):
     """C (epilogue) = A B^T on the tensor-core projection kernel (see qw_debug_gemm).
-    With split, A is the hi/lo layout and M the number of activation rows."""
+    split = 1: A is the hi/lo layout and M the number of activation rows; split = 2: plain A on
+    the CTA-pair (weight tile multicast) path."""
     lib = load()
     K = A.shape[1]
     M = A.shape[0] if M is None else M

@@ -46,6 +46,7 @@ struct LayerW {
     float *in_norm, *post_norm, *q_norm, *k_norm;
     CUtensorMap tm_qkv, tm_o, tm_gu, tm_d;
     CUtensorMap tm_o256, tm_d256;   // o_proj / down_proj with 256-row boxes (large-M products)
+    CUtensorMap tm_qkv128, tm_gu128;  // q|k|v and gate/up with 128-row boxes (CTA-pair halves)
 };
 
 struct qw_ctx {
@@ -249,7 +250,9 @@ int qw_init(const qw_config* cfg, const qw_weights* w, qw_ctx** out) {
             make_tmap_bf16(&Lw.tm_gu, Lw.wgu, D, 2 * I, rowb, 64, 256) ||
             make_tmap_bf16(&Lw.tm_d, Lw.wd, I, D, (size_t)I * 2, 64, 128) ||
             make_tmap_bf16(&Lw.tm_o256, Lw.wo, ctx->attn_dim, D, (size_t)ctx->attn_dim * 2, 64, 256) ||
-            make_tmap_bf16(&Lw.tm_d256, Lw.wd, I, D, (size_t)I * 2, 64, 256)) {
+            make_tmap_bf16(&Lw.tm_d256, Lw.wd, I, D, (size_t)I * 2, 64, 256) ||
+            make_tmap_bf16(&Lw.tm_qkv128, Lw.wqkv, D, ctx->qkv_dim, rowb, 64, 128) ||
+            make_tmap_bf16(&Lw.tm_gu128, Lw.wgu, D, 2 * I, rowb, 64, 128)) {
             free_ctx(ctx);
             return fail(QW_ECUDA, "cuTensorMapEncodeTiled failed for a weight");
         }
@@ -402,7 +405,8 @@ static int run_layers(qw_ctx* ctx, int n, const int* ids, const int* positions, 
             // prefill: QK-Norm, RoPE, bf16 q and the cache write happen in the GEMM epilogue
             e.rope = QkvRope{positions, tok_seq, kvv, Lw.q_norm, Lw.k_norm, ctx->rope_tab, c.rms_eps, ctx->q_bf16,
                              Hq, Hkv};
-            QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_qkv, 256, n, ctx->qkv_dim, D, EPI_QKV_ROPE, e, st), "qkv gemm");
+            QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_qkv, 256, n, ctx->qkv_dim, D, EPI_QKV_ROPE, e, st, &Lw.tm_qkv128),
+                   "qkv gemm");
         } else {
             // small M: split-K with atomic accumulation (zeroed targets) so every SM streams weights
             if (split) QW_CUDA(cudaMemsetAsync(ctx->qkv, 0, (size_t)n * ctx->qkv_dim * 4, st));
@@ -433,7 +437,8 @@ static int run_layers(qw_ctx* ctx, int n, const int* ids, const int* positions, 
             QW_TRY(gemm_bf16(ctx->attn, ctx->attn_dim, Lw.tm_o, 128, n, D, ctx->attn_dim, EPI_ADD_ATOMIC, e, st),
                    "o_proj gemm");
         else
-            QW_TRY(gemm_bf16(ctx->attn, ctx->attn_dim, Lw.tm_o256, 256, n, D, ctx->attn_dim, EPI_RESID_ADD, e, st),
+            QW_TRY(gemm_bf16(ctx->attn, ctx->attn_dim, Lw.tm_o256, 256, n, D, ctx->attn_dim, EPI_RESID_ADD, e, st,
+                             &Lw.tm_o),
                    "o_proj gemm");
         QW_TRY(launch_rmsnorm_bf16(ctx->x, nullptr, n, D, Lw.post_norm, c.rms_eps, ctx->h, split, st),
                "rmsnorm launch");
@@ -444,13 +449,13 @@ static int run_layers(qw_ctx* ctx, int n, const int* ids, const int* positions, 
             QW_TRY(launch_swiglu_split(ctx->gu, n, I, ctx->act, st), "swiglu launch");
         } else {
             e = GemmEpilogue{nullptr, ctx->act, I, ctx->err, split};
-            QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_gu, 256, n, 2 * I, D, EPI_SWIGLU, e, st), "gate/up gemm");
+            QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_gu, 256, n, 2 * I, D, EPI_SWIGLU, e, st, &Lw.tm_gu128), "gate/up gemm");
         }
         e = GemmEpilogue{ctx->x, nullptr, D, ctx->err, split};
         if (split)
             QW_TRY(gemm_bf16(ctx->act, I, Lw.tm_d, 128, n, D, I, EPI_ADD_ATOMIC, e, st), "down gemm");
         else
-            QW_TRY(gemm_bf16(ctx->act, I, Lw.tm_d256, 256, n, D, I, EPI_RESID_ADD, e, st), "down gemm");
+            QW_TRY(gemm_bf16(ctx->act, I, Lw.tm_d256, 256, n, D, I, EPI_RESID_ADD, e, st, &Lw.tm_d), "down gemm");
         if (ctx->hidden)
             QW_CUDA(cudaMemcpyAsync(ctx->hidden + (size_t)l * ctx->max_rows * D, ctx->x, (size_t)n * D * 4,
                                     cudaMemcpyDeviceToDevice, st));
@@ -597,11 +602,14 @@ int qw_debug_gemm(const uint16_t* A, const uint16_t* B, void* C, int32_t M, int3
     if (!A || !B || !C || M < 1 || N < 32 || K < 64 || K % 64 || N % 32 || epi < 0 || epi > 3 ||
         (bn != 128 && bn != 256))
         return fail(QW_EINVAL, "qw_debug_gemm: bad argument");
-    CUtensorMap tb;
+    if (split < 0 || split > 2) return fail(QW_EINVAL, "qw_debug_gemm: bad split");
+    CUtensorMap tb, tb_half;
     QW_TRY(make_tmap_bf16(&tb, B, (uint64_t)K, (uint64_t)N, (uint64_t)K * 2, 64, (uint32_t)bn), "tensor map for B");
+    QW_TRY(make_tmap_bf16(&tb_half, B, (uint64_t)K, (uint64_t)N, (uint64_t)K * 2, 64, 128), "tensor map for B");
     GemmEpilogue e{epi == 2 ? nullptr : (float*)C, epi == 2 ? (uint16_t*)C : nullptr, epi == 2 ? N / 2 : N, nullptr,
-                   split ? 1 : 0};
-    QW_TRY(gemm_bf16(A, K, tb, bn, M, N, K, epi, e, (cudaStream_t)stream), "gemm launch");
+                   split == 1 ? 1 : 0};
+    QW_TRY(gemm_bf16(A, K, tb, bn, M, N, K, epi, e, (cudaStream_t)stream, split == 2 ? &tb_half : nullptr),
+           "gemm launch");
     return QW_OK;
 }
 

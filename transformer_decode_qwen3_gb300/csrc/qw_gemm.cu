@@ -12,6 +12,12 @@
 // read the other accumulator with tcgen05.ld (thread t owns output row t) and
 // apply the fused epilogue, so a tile's epilogue overlaps the next tile's MMAs.
 //
+// Multicast mode (large M): CTAs run in clusters of two that take vertically adjacent
+// output tiles with the same weight tile; each CTA fetches half of that B tile and TMA
+// multicasts it into both CTAs' shared memory, so each CTA pulls 32 KB instead of 48 KB
+// from L2 per 64-wide K block.  A stage is refilled only once both CTAs' MMAs are done
+// with it (their commits arrive on both CTAs' empty barriers).
+//
 // Split-operand mode (small M, e.g. decode batches): every activation row a is
 // stored as two bf16 rows, hi = bf16(a) in tile rows 0..63 and lo = bf16(a - hi)
 // in rows 64..127, so one M=128 MMA yields hi.W and lo.W side by side and the
@@ -40,7 +46,9 @@ struct GemmCfg {
     static constexpr int THREADS = 256;                 // warps 0-3: TMA, MMA, TMEM owner, idle; 4-7: epilogue
 };
 
-QW_DEV float silu_f(float g) { return g / (1.0f + expf(-g)); }
+// SiLU on the special-function unit (2^x and 1/x approximations, relative error ~1e-6; the
+// result is rounded to bf16 next).  Large negative g: 2^x overflows to +inf and 1/inf = 0.
+QW_DEV float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // Destination row of activation row m in the split layout (hi copy; lo is 64 rows further).
 QW_DEV int split_row(int m) { return (m >> 6) * 128 + (m & 63); }
@@ -89,6 +97,41 @@ QW_DEV void epilogue_chunk(const float (&v)[32], int m, int n, const GemmEpilogu
 }
 
 QW_DEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+QW_DEV uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+QW_DEV uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+QW_DEV uint32_t n_clusters_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+// All threads of both CTAs of the cluster.
+QW_DEV void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// TMA load delivered to the same shared-memory offset (data and mbarrier) in every CTA of mask.
+QW_DEV void tma_load_2d_mc(void* smem_dst, const CUtensorMap* m, int x, int y, uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"((uint64_t)m), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
+        : "memory");
+}
+// Arrive on the mbarrier at this offset in every CTA of mask once this thread's MMAs are done.
+QW_DEV void umma_commit_mc(uint64_t* bar, uint16_t mask) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::
+                     "r"(smem_u32(bar)),
+                 "h"(mask)
+                 : "memory");
+}
 
 // Store 32 values as bf16 (four 16-byte stores).
 QW_DEV void store_bf16x32(uint16_t* dst, const float (&y)[32]) {
@@ -180,10 +223,11 @@ QW_DEV void qkv_rope_tile(uint32_t trow, int m, int M, int n0, int N, const Gemm
     }
 }
 
-template <int BN, int EPI, bool SPLIT>
+template <int BN, int EPI, bool SPLIT, bool MC>
 __global__ void __launch_bounds__(256, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         int M, int N, int K, int tiles_m, int tiles_n, int ksplit, int share_a, GemmEpilogue ep) {
+    // MC: tmB has boxes of BN / 2 rows (each CTA of the pair loads one half)
     using C = GemmCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -198,21 +242,27 @@ __global__ void __launch_bounds__(256, 1)
     volatile uint32_t* abort_flag = tmem_slot + 1;
 
     // a CTA of this launch already gave up on a wait: end quickly instead of timing out again
-    if (ep.err && *(volatile int*)ep.err == QW_ETIMEOUT) return;
+    // (in a cluster the CTA still meets its peer at the cluster barriers, with no work)
+    const bool gave_up = ep.err && *(volatile int*)ep.err == QW_ETIMEOUT;
+    if (!MC && gave_up) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = K / C::BK;
-    const int n_tiles = tiles_m * tiles_n * ksplit;   // work units: (m tile, n tile, K slice)
+    const uint32_t crank = MC ? cluster_ctarank() : 0u;
+    const int tiles_mu = MC ? (tiles_m + 1) / 2 : tiles_m;   // m units (pairs of m tiles in MC)
+    const int n_tiles = tiles_mu * tiles_n * ksplit;           // work units: (m unit, n tile, K slice)
+    const int first = MC ? (int)cluster_id_x() : (int)blockIdx.x;
+    const int stride = MC ? (int)n_clusters_x() : (int)gridDim.x;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], MC ? 2 : 1);   // MC: both CTAs' MMAs release a stage
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], 4);      // one arrival per epilogue warp
         }
-        *abort_flag = 0;
+        *abort_flag = gave_up ? 1u : 0u;
         fence_mbar_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
@@ -220,6 +270,7 @@ __global__ void __launch_bounds__(256, 1)
     if (warp == 2) tmem_alloc(tmem_slot, C::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
+    if (MC) cluster_sync();   // the peer's barriers are initialised before any multicast reaches them
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
@@ -227,8 +278,9 @@ __global__ void __launch_bounds__(256, 1)
     // (share_a: n tile fastest; the whole B fits in L2) or the B tile (m tile fastest).
     auto unit = [&](int t, int& tm, int& tn, int& kb0, int& kb1) {
         const int ks = t % ksplit, rest = t / ksplit;
-        tn = share_a ? rest % tiles_n : rest / tiles_m;
-        tm = share_a ? rest / tiles_n : rest % tiles_m;
+        tn = share_a ? rest % tiles_n : rest / tiles_mu;
+        tm = share_a ? rest / tiles_n : rest % tiles_mu;
+        if (MC) tm = 2 * tm + (int)crank;   // past the last m tile for an odd count: zero rows, no stores
         kb0 = ks * nk / ksplit;
         kb1 = (ks + 1) * nk / ksplit;
     };
@@ -236,7 +288,7 @@ __global__ void __launch_bounds__(256, 1)
     if (warp == 0) {
         if (lane == 0) {  // TMA producer
             uint32_t kb_all = 0;
-            for (int t = blockIdx.x; t < n_tiles && !*abort_flag; t += gridDim.x) {
+            for (int t = first; t < n_tiles && !*abort_flag; t += stride) {
                 int tm, tn, kb0, kb1;
                 unit(t, tm, tn, kb0, kb1);
                 for (int kb = kb0; kb < kb1; ++kb, ++kb_all) {
@@ -246,10 +298,19 @@ __global__ void __launch_bounds__(256, 1)
                         *abort_flag = 1;
                         break;
                     }
-                    mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);
+                    mbar_arrive_expect_tx(&full[s], C::STAGE_BYTES);   // MC: half of B comes from the peer
                     tma_load_2d(sA + s * C::A_BYTES, &tmA, kb * C::BK, tm * C::BM, &full[s]);
-                    tma_load_2d(sB + s * C::B_BYTES, &tmB, kb * C::BK, tn * BN, &full[s]);
+                    if (MC)
+                        tma_load_2d_mc(sB + s * C::B_BYTES + crank * (C::B_BYTES / 2), &tmB, kb * C::BK,
+                                       tn * BN + (int)crank * (BN / 2), &full[s], (uint16_t)0x3);
+                    else
+                        tma_load_2d(sB + s * C::B_BYTES, &tmB, kb * C::BK, tn * BN, &full[s]);
                 }
+            }
+            if (MC) {
+                // every commit of both CTAs aimed at this CTA's empty barriers has landed before the exit
+                const uint32_t from = kb_all > (uint32_t)C::STAGES ? kb_all - C::STAGES : 0u;
+                for (uint32_t i = from; i < kb_all; ++i) mbar_wait(&empty[i % C::STAGES], (i / C::STAGES) & 1, ep.err);
             }
         }
     } else if (warp == 1) {
@@ -257,7 +318,7 @@ __global__ void __launch_bounds__(256, 1)
             constexpr uint32_t idesc = umma_idesc_bf16(C::BM, BN);
             uint32_t kb_all = 0;
             int local = 0;
-            for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++local) {
+            for (int t = first; t < n_tiles; t += stride, ++local) {
                 const int acc = local & 1;
                 const uint32_t use = (uint32_t)(local >> 1);
                 bool ok = !*abort_flag && mbar_wait(&tempty[acc], (use & 1) ^ 1, ep.err);
@@ -278,7 +339,10 @@ __global__ void __launch_bounds__(256, 1)
                     for (int k = 0; k < C::BK / 16; ++k)
                         umma_bf16(dtm, umma_desc_sw128(a0 + k * 32), umma_desc_sw128(b0 + k * 32), idesc,
                                   (kb != kb0) || k != 0);
-                    umma_commit(&empty[s]);
+                    if (MC)
+                        umma_commit_mc(&empty[s], (uint16_t)0x3);
+                    else
+                        umma_commit(&empty[s]);
                 }
                 if (!ok) {
                     *abort_flag = 1;
@@ -293,7 +357,7 @@ __global__ void __launch_bounds__(256, 1)
         const int ew = warp - 4;
         const int et = threadIdx.x - 128;
         int local = 0;
-        for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++local) {
+        for (int t = first; t < n_tiles; t += stride, ++local) {
             int tm, tn, kb0, kb1;
             unit(t, tm, tn, kb0, kb1);
             const int acc = local & 1;
@@ -334,6 +398,7 @@ __global__ void __launch_bounds__(256, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (MC) cluster_sync();   // no multicast or remote arrive can still target this CTA
     if (warp == 2) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
@@ -366,22 +431,35 @@ int make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t 
     return r == CUDA_SUCCESS ? QW_OK : QW_ECUDA;
 }
 
-template <int BN, int EPI, bool SPLIT>
+template <int BN, int EPI, bool SPLIT, bool MC>
 static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, const GemmEpilogue& ep,
                      cudaStream_t st) {
     using C = GemmCfg<BN>;
+    auto kern = gemm_bf16_tc_kernel<BN, EPI, SPLIT, MC>;
     static bool attr_set = false;
+    static int n_sm = 0, max_clusters = 0;
     if (!attr_set) {
-        if (cudaFuncSetAttribute(gemm_bf16_tc_kernel<BN, EPI, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 C::SMEM) != cudaSuccess)
-            return QW_ECUDA;
-        attr_set = true;
-    }
-    static int n_sm = 0;
-    if (!n_sm) {
         int dev = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+            return QW_ECUDA;
+        if (MC) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = 2;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(2 * (n_sm / 2));
+            cfg.blockDim = dim3(C::THREADS);
+            cfg.dynamicSmemBytes = C::SMEM;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess || max_clusters < 1)
+                return QW_ECUDA;
+        }
+        attr_set = true;
     }
     const int tiles_m = SPLIT ? (M + 63) / 64 : (M + C::BM - 1) / C::BM;
     const int tiles_n = (N + BN - 1) / BN;
@@ -393,13 +471,31 @@ static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N,
         if (ksplit > nk) ksplit = nk;
         if (ksplit < 1) ksplit = 1;
     }
-    const int work = tiles_m * tiles_n * ksplit;
-    const int grid = work < n_sm ? work : n_sm;
     // A streams from HBM once when the CTAs running together share its tiles; that needs the
     // weight matrix B to stay L2-resident (projection weights are 4..13 MB; the LM head is not).
     const int share_a = (int64_t)N * K * 2 <= (int64_t)32 << 20 && tiles_m > 1;
-    gemm_bf16_tc_kernel<BN, EPI, SPLIT><<<grid, C::THREADS, C::SMEM, st>>>(ta, tb, M, N, K, tiles_m, tiles_n, ksplit,
-                                                                         share_a, ep);
+    if (MC) {
+        const int units = (tiles_m + 1) / 2 * tiles_n;
+        const int nc = units < max_clusters ? units : max_clusters;
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeClusterDimension;
+        at[0].val.clusterDim.x = 2;
+        at[0].val.clusterDim.y = 1;
+        at[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * nc);
+        cfg.blockDim = dim3(C::THREADS);
+        cfg.dynamicSmemBytes = C::SMEM;
+        cfg.stream = st;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, M, N, K, tiles_m, tiles_n, 1, share_a, ep);
+        count_launches(1);
+        return e == cudaSuccess ? QW_OK : QW_ECUDA;
+    }
+    const int work = tiles_m * tiles_n * ksplit;
+    const int grid = work < n_sm ? work : n_sm;
+    kern<<<grid, C::THREADS, C::SMEM, st>>>(ta, tb, M, N, K, tiles_m, tiles_n, ksplit, share_a, ep);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ECUDA;
 }
@@ -408,27 +504,38 @@ template <bool SPLIT>
 static int launch_split(const CUtensorMap& ta, const CUtensorMap& tb, int bn, int M, int N, int K, int epi,
                         const GemmEpilogue& ep, cudaStream_t st) {
     if (bn == 256) {
-        if (epi == EPI_STORE_F32) return launch_bn<256, EPI_STORE_F32, SPLIT>(ta, tb, M, N, K, ep, st);
-        if (epi == EPI_RESID_ADD) return launch_bn<256, EPI_RESID_ADD, SPLIT>(ta, tb, M, N, K, ep, st);
-        if (epi == EPI_ADD_ATOMIC) return launch_bn<256, EPI_ADD_ATOMIC, SPLIT>(ta, tb, M, N, K, ep, st);
+        if (epi == EPI_STORE_F32) return launch_bn<256, EPI_STORE_F32, SPLIT, false>(ta, tb, M, N, K, ep, st);
+        if (epi == EPI_RESID_ADD) return launch_bn<256, EPI_RESID_ADD, SPLIT, false>(ta, tb, M, N, K, ep, st);
+        if (epi == EPI_ADD_ATOMIC) return launch_bn<256, EPI_ADD_ATOMIC, SPLIT, false>(ta, tb, M, N, K, ep, st);
         if (epi == EPI_QKV_ROPE) {
             if constexpr (SPLIT) return QW_EINVAL;
-            else return launch_bn<256, EPI_QKV_ROPE, false>(ta, tb, M, N, K, ep, st);
+            else return launch_bn<256, EPI_QKV_ROPE, false, false>(ta, tb, M, N, K, ep, st);
         }
-        return launch_bn<256, EPI_SWIGLU, SPLIT>(ta, tb, M, N, K, ep, st);
+        return launch_bn<256, EPI_SWIGLU, SPLIT, false>(ta, tb, M, N, K, ep, st);
     }
-    if (epi == EPI_STORE_F32) return launch_bn<128, EPI_STORE_F32, SPLIT>(ta, tb, M, N, K, ep, st);
-    if (epi == EPI_RESID_ADD) return launch_bn<128, EPI_RESID_ADD, SPLIT>(ta, tb, M, N, K, ep, st);
-    if (epi == EPI_ADD_ATOMIC) return launch_bn<128, EPI_ADD_ATOMIC, SPLIT>(ta, tb, M, N, K, ep, st);
+    if (epi == EPI_STORE_F32) return launch_bn<128, EPI_STORE_F32, SPLIT, false>(ta, tb, M, N, K, ep, st);
+    if (epi == EPI_RESID_ADD) return launch_bn<128, EPI_RESID_ADD, SPLIT, false>(ta, tb, M, N, K, ep, st);
+    if (epi == EPI_ADD_ATOMIC) return launch_bn<128, EPI_ADD_ATOMIC, SPLIT, false>(ta, tb, M, N, K, ep, st);
     if (epi == EPI_QKV_ROPE) {
         if constexpr (SPLIT) return QW_EINVAL;
-        else return launch_bn<128, EPI_QKV_ROPE, false>(ta, tb, M, N, K, ep, st);
+        else return launch_bn<128, EPI_QKV_ROPE, false, false>(ta, tb, M, N, K, ep, st);
     }
-    return launch_bn<128, EPI_SWIGLU, SPLIT>(ta, tb, M, N, K, ep, st);
+    return launch_bn<128, EPI_SWIGLU, SPLIT, false>(ta, tb, M, N, K, ep, st);
+}
+
+// Large-M products on 256-wide tiles in CTA pairs sharing the weight tile (tb_half: the same
+// weight with 128-row boxes).
+static int launch_mc(const CUtensorMap& ta, const CUtensorMap& tb_half, int M, int N, int K, int epi,
+                     const GemmEpilogue& ep, cudaStream_t st) {
+    if (epi == EPI_STORE_F32) return launch_bn<256, EPI_STORE_F32, false, true>(ta, tb_half, M, N, K, ep, st);
+    if (epi == EPI_RESID_ADD) return launch_bn<256, EPI_RESID_ADD, false, true>(ta, tb_half, M, N, K, ep, st);
+    if (epi == EPI_QKV_ROPE) return launch_bn<256, EPI_QKV_ROPE, false, true>(ta, tb_half, M, N, K, ep, st);
+    if (epi == EPI_SWIGLU) return launch_bn<256, EPI_SWIGLU, false, true>(ta, tb_half, M, N, K, ep, st);
+    return QW_EINVAL;
 }
 
 int gemm_bf16(const void* A, int lda_elems, const CUtensorMap& tmB, int bn, int M, int N, int K, int epi,
-              const GemmEpilogue& ep, cudaStream_t st) {
+              const GemmEpilogue& ep, cudaStream_t st, const CUtensorMap* tmB_half) {
     if (M <= 0) return QW_OK;
     if (K % 64 || N % 32 || (bn != 128 && bn != 256)) return QW_EINVAL;
     // split layout: ceil(M/64) tiles of 128 rows (64 hi rows, then their 64 lo rows)
@@ -436,6 +543,8 @@ int gemm_bf16(const void* A, int lda_elems, const CUtensorMap& tmB, int bn, int 
     CUtensorMap ta;
     int rc = make_tmap_bf16(&ta, A, (uint64_t)K, rows, (uint64_t)lda_elems * 2, 64, 128);
     if (rc) return rc;
+    if (tmB_half && !ep.split && bn == 256 && M > 128 && epi != EPI_ADD_ATOMIC)
+        return launch_mc(ta, *tmB_half, M, N, K, epi, ep, st);
     return ep.split ? launch_split<true>(ta, tmB, bn, M, N, K, epi, ep, st)
                     : launch_split<false>(ta, tmB, bn, M, N, K, epi, ep, st);
 }

@@ -60,9 +60,11 @@ constexpr int SPLIT_MAX_M = 256;
 int make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t row_stride_bytes,
                    uint32_t box_inner, uint32_t box_rows);
 
-// C[M][N] (epilogue) = A[M][K] . B[N][K]^T; tmB must have box {64, bn}.
+// C[M][N] (epilogue) = A[M][K] . B[N][K]^T; tmB must have box {64, bn}.  tmB_half (nullable):
+// the same B with box {64, 128}; given with bn = 256 and M > 128 (not split, not split-K), the
+// product runs in CTA pairs that multicast the shared weight tile.
 int gemm_bf16(const void* A, int lda_elems, const CUtensorMap& tmB, int bn, int M, int N, int K, int epi,
-              const GemmEpilogue& ep, cudaStream_t st);
+              const GemmEpilogue& ep, cudaStream_t st, const CUtensorMap* tmB_half = nullptr);
 
 // ---------------------------------------------------------------- per-op kernels
 // (cos, sin) of the RoPE angles float32(positions[t] * inv_freq[i]), i < 64, for n rows.
