@@ -145,79 +145,94 @@ QW_DEV void store_bf16x32(uint16_t* dst, const float (&y)[32]) {
 // EPI_QKV_ROPE on one accumulator tile: this thread's row m, columns n0 .. n0 + BN - 1 = BN / 128
 // whole heads of the fused q|k|v output (Steps 4-5 of the article).  q and k heads: RMS-normalised
 // over their 128 values (QK-Norm), scaled by the norm weight, rotated by RoPE with pairs
-// (d, d + 64) at angle float32(pos * inv_freq[d]) (cos and sin from a per-row table); q goes out as bf16, k and v enter the cache
-// page of (tok_seq[m], pos) as bf16.  TMEM loads are warp-collective, so every thread loads
-// even when its row is past M; only the stores are per row.
+// (d, d + 64) at angle float32(pos * inv_freq[d]) (cos and sin from a per-row table, read once
+// for all heads of the tile); q goes out as bf16, k and v enter the cache page of (tok_seq[m],
+// pos) as bf16.  nw: the q and k norm weights in shared memory (nw[0..127] q, nw[128..255] k).
+// TMEM loads are warp-collective, so every thread loads even when its row is past M; only the
+// stores are per row.
 template <int BN>
-QW_DEV void qkv_rope_tile(uint32_t trow, int m, int M, int n0, int N, const GemmEpilogue& ep) {
+QW_DEV void qkv_rope_tile(uint32_t trow, int m, int M, int n0, int N, const GemmEpilogue& ep, const float* nw) {
+    constexpr int NH = BN / 128;
     const QkvRope& r = ep.rope;
     const bool live = m < M;
-    int pos = 0;  // used for the page lookup
     uint16_t* kv_row = nullptr;  // this row's slot in its cache page (k of head 0)
-    if (live) {
-        pos = r.positions[m];
-        if (n0 + BN > r.Hq * 128) {  // the tile holds k or v heads
-            const int seq = r.tok_seq[m];
-            const int page = pos >= 0 && pos < r.kv.bt_stride * QW_PAGE_SIZE
-                                 ? r.kv.block_tables[(size_t)seq * r.kv.bt_stride + pos / QW_PAGE_SIZE]
-                                 : -1;
-            if (page < 0 || page >= r.kv.n_pages)
-                set_error(ep.err, QW_ERANGE);
-            else
-                kv_row = r.kv.base + (size_t)page * r.kv.page_stride + (size_t)(pos % QW_PAGE_SIZE) * QW_HEAD_DIM;
-        }
+    if (live && n0 + BN > r.Hq * 128) {  // the tile holds k or v heads
+        const int pos = r.positions[m];
+        const int seq = r.tok_seq[m];
+        const int page = pos >= 0 && pos < r.kv.bt_stride * QW_PAGE_SIZE
+                             ? r.kv.block_tables[(size_t)seq * r.kv.bt_stride + pos / QW_PAGE_SIZE]
+                             : -1;
+        if (page < 0 || page >= r.kv.n_pages)
+            set_error(ep.err, QW_ERANGE);
+        else
+            kv_row = r.kv.base + (size_t)page * r.kv.page_stride + (size_t)(pos % QW_PAGE_SIZE) * QW_HEAD_DIM;
     }
-#pragma unroll 1
-    for (int hd = 0; hd < BN / 128; ++hd) {
+    uint16_t* dst[NH];
+    bool rope[NH], valid[NH];
+    float sc[NH];
+#pragma unroll
+    for (int hd = 0; hd < NH; ++hd) {
         const int col = n0 + 128 * hd;
-        if (col >= N) break;  // uniform
         const int head = col / 128;
+        valid[hd] = col < N;
+        rope[hd] = valid[hd] && head < r.Hq + r.Hkv;
+        dst[hd] = nullptr;
+        if (valid[hd] && head < r.Hq)
+            dst[hd] = live ? r.q_bf16 + (size_t)m * r.Hq * 128 + (size_t)head * 128 : nullptr;
+        else if (valid[hd] && kv_row)  // k heads Hq .. Hq+Hkv-1, then v heads: (K/V, head) rows of 16 slots
+            dst[hd] = kv_row + (size_t)(head - r.Hq) * QW_PAGE_SIZE * QW_HEAD_DIM;
+        sc[hd] = 1.f;
+    }
+    // v heads: plain bf16 copy; q and k heads: sum of squares
+#pragma unroll
+    for (int hd = 0; hd < NH; ++hd) {
+        if (!valid[hd]) continue;  // uniform
         const uint32_t t0 = trow + (uint32_t)(128 * hd);
-        // destination of the 128 values of this head in this row
-        uint16_t* dst = nullptr;
-        if (head < r.Hq)
-            dst = live ? r.q_bf16 + (size_t)m * r.Hq * 128 + (size_t)head * 128 : nullptr;
-        else if (kv_row)  // k heads Hq .. Hq+Hkv-1, then v heads: (K/V, head) rows of 16 slots
-            dst = kv_row + (size_t)(head - r.Hq) * QW_PAGE_SIZE * QW_HEAD_DIM;
-        if (head >= r.Hq + r.Hkv) {  // v: plain bf16 copy
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                float v[32];
-                tmem_ld32(t0 + 32 * c, v);
-                if (dst) store_bf16x32(dst + 32 * c, v);
-            }
-            continue;
-        }
         float ss = 0.f;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
             float v[32];
             tmem_ld32(t0 + 32 * c, v);
+            if (rope[hd]) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) ss = fmaf(v[i], v[i], ss);
+                for (int i = 0; i < 32; ++i) ss = fmaf(v[i], v[i], ss);
+            } else if (dst[hd]) {
+                store_bf16x32(dst[hd] + 32 * c, v);
+            }
         }
-        const float sc = 1.0f / sqrtf(ss / (float)QW_HEAD_DIM + r.eps);
-        const float* w = head < r.Hq ? r.q_norm : r.k_norm;
+        sc[hd] = 1.0f / sqrtf(ss / (float)QW_HEAD_DIM + r.eps);
+    }
+    if (!(rope[0] || (NH > 1 && rope[NH - 1]))) return;  // uniform
 #pragma unroll 1
-        for (int j = 0; j < 2; ++j) {  // dims 32 j .. 32 j + 31 pair with 32 j + 64 ..
+    for (int j = 0; j < 2; ++j) {  // dims 32 j .. 32 j + 31 pair with 32 j + 64 ..
+        float4 t[16];              // (cos, sin) of pairs 32 j + 2 i and + 1
+        const float4* cs4 = (const float4*)(r.rope + (size_t)(live ? m : 0) * 64 + 32 * j);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) t[i] = __ldg(cs4 + i);
+#pragma unroll
+        for (int hd = 0; hd < NH; ++hd) {
+            if (!rope[hd]) continue;  // uniform
+            const int head = (n0 + 128 * hd) / 128;
+            const float* w = nw + (head < r.Hq ? 0 : 128);
+            const uint32_t t0 = trow + (uint32_t)(128 * hd);
             float a[32], b[32];
-            tmem_ld32(t0 + 32 * j, a);
-            tmem_ld32(t0 + 32 * j + 64, b);
-            const float4* cs4 = (const float4*)(r.rope + (size_t)(live ? m : 0) * 64 + 32 * j);
+            tmem_ld32_nowait(t0 + 32 * j, a);
+            tmem_ld32_nowait(t0 + 32 * j + 64, b);
+            tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; i += 2) {
-                const float4 t = __ldg(cs4 + i / 2);  // (cos, sin) of pairs d and d + 1
+                const float4 tt = t[i / 2];
                 const int d = 32 * j + i;
-                const float x1 = a[i] * sc * __ldg(w + d), x2 = b[i] * sc * __ldg(w + d + 64);
-                const float y1 = a[i + 1] * sc * __ldg(w + d + 1), y2 = b[i + 1] * sc * __ldg(w + d + 65);
-                a[i] = x1 * t.x - x2 * t.y;
-                b[i] = x1 * t.y + x2 * t.x;
-                a[i + 1] = y1 * t.z - y2 * t.w;
-                b[i + 1] = y1 * t.w + y2 * t.z;
+                const float x1 = a[i] * sc[hd] * w[d], x2 = b[i] * sc[hd] * w[d + 64];
+                const float y1 = a[i + 1] * sc[hd] * w[d + 1], y2 = b[i + 1] * sc[hd] * w[d + 65];
+                a[i] = x1 * tt.x - x2 * tt.y;
+                b[i] = x1 * tt.y + x2 * tt.x;
+                a[i + 1] = y1 * tt.z - y2 * tt.w;
+                b[i + 1] = y1 * tt.w + y2 * tt.z;
             }
-            if (dst) {
-                store_bf16x32(dst + 32 * j, a);
-                store_bf16x32(dst + 32 * j + 64, b);
+            if (dst[hd]) {
+                store_bf16x32(dst[hd] + 32 * j, a);
+                store_bf16x32(dst[hd] + 32 * j + 64, b);
             }
         }
     }
@@ -356,6 +371,11 @@ __global__ void __launch_bounds__(256, 1)
         // Epilogue warpgroup: warp 4 + i reads TMEM lanes 32 i .. 32 i + 31.
         const int ew = warp - 4;
         const int et = threadIdx.x - 128;
+        if constexpr (EPI == EPI_QKV_ROPE) {  // q and k norm weights into shared memory
+            xch[et] = ep.rope.q_norm[et];
+            xch[128 + et] = ep.rope.k_norm[et];
+            epi_bar();
+        }
         int local = 0;
         for (int t = first; t < n_tiles; t += stride, ++local) {
             int tm, tn, kb0, kb1;
@@ -367,7 +387,7 @@ __global__ void __launch_bounds__(256, 1)
             if (!ok) break;
             const uint32_t trow = tmem + (uint32_t)(acc * BN) + ((uint32_t)(ew * 32) << 16);
             const int n0 = tn * BN;
-            if constexpr (EPI == EPI_QKV_ROPE) qkv_rope_tile<BN>(trow, tm * C::BM + et, M, n0, N, ep);
+            if constexpr (EPI == EPI_QKV_ROPE) qkv_rope_tile<BN>(trow, tm * C::BM + et, M, n0, N, ep, xch);
 #pragma unroll 1
             for (int c0 = 0; c0 < BN && EPI != EPI_QKV_ROPE; c0 += 32) {
                 if (n0 + c0 >= N) break;  // uniform over the warpgroup
