@@ -87,9 +87,13 @@ __global__ void __launch_bounds__(THREADS, 2)
     uint8_t* sP = sm + Q_BYTES + KV_STAGES * KV_STAGE;
     uint64_t* bars = (uint64_t*)(sP + P_BYTES);
     uint64_t* q_full = bars;
-    uint64_t* kv_full = bars + 1;                  // [KV_STAGES]
-    uint64_t* kv_empty = kv_full + KV_STAGES;      // [KV_STAGES]
-    uint64_t* s_full = kv_empty + KV_STAGES;       // [2]
+    // K and V of a stage are filled and released separately: a K slot frees as soon as its
+    // S = Q K^T is done, so the next K loads start well before their tile is needed
+    uint64_t* k_full = bars + 1;                   // [KV_STAGES]
+    uint64_t* v_full = k_full + KV_STAGES;         // [KV_STAGES]
+    uint64_t* k_empty = v_full + KV_STAGES;        // [KV_STAGES]
+    uint64_t* v_empty = k_empty + KV_STAGES;       // [KV_STAGES]
+    uint64_t* s_full = v_empty + KV_STAGES;        // [2]
     uint64_t* p_full = s_full + 2;
     uint64_t* o_done = p_full + 1;
     uint32_t* tmem_slot = (uint32_t*)(o_done + 1);
@@ -108,8 +112,10 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         for (int s = 0; s < KV_STAGES; ++s) {
-            mbar_init(&kv_full[s], 1);
-            mbar_init(&kv_empty[s], 1);
+            mbar_init(&k_full[s], 1);
+            mbar_init(&v_full[s], 1);
+            mbar_init(&k_empty[s], 1);
+            mbar_init(&v_empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) mbar_init(&s_full[s], 1);
         mbar_init(p_full, 4);
@@ -146,31 +152,36 @@ __global__ void __launch_bounds__(THREADS, 2)
                         tma_load_2d(sQ + c * CHUNK + hh * (CHUNK / 2), &tmQ, (2 * g + hh) * HD + 64 * c, row0,
                                     q_full);
             }
-            int next_page = page_of(0);
-            for (int j = 0; j < nt; ++j) {
-                const int s = j % KV_STAGES;
-                const int my_page = next_page;
-                if (j + 1 < nt) next_page = page_of(j + 1);   // in flight while this tile waits
+            // issue order K_0, then K_{j+1}, V_j for j = 0, 1, ...: K runs one tile ahead of V
+            auto issue = [&](int j, int page_lane, bool is_v) -> bool {
+                const int st_i = j % KV_STAGES;
+                uint64_t* emp = is_v ? &v_empty[st_i] : &k_empty[st_i];
+                uint64_t* ful = is_v ? &v_full[st_i] : &k_full[st_i];
                 bool ok = true;
-                if (lane == 0) ok = mbar_wait(&kv_empty[s], ((j / KV_STAGES) & 1) ^ 1, err) && !*abort_flag;
+                if (lane == 0) ok = mbar_wait(emp, ((j / KV_STAGES) & 1) ^ 1, err) && !*abort_flag;
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) {
                     if (lane == 0) *abort_flag = 1;
-                    break;
+                    return false;
                 }
-                uint8_t* st = sKV + s * KV_STAGE;
-                if (lane == 0) mbar_arrive_expect_tx(&kv_full[s], KV_STAGE);
+                uint8_t* st = sKV + st_i * KV_STAGE + (is_v ? 2 * KCHUNK : 0);
+                if (lane == 0) mbar_arrive_expect_tx(ful, 2 * KCHUNK);
                 for (int pi = 0; pi < PPT; ++pi) {
-                    const int page = __shfl_sync(0xffffffffu, my_page, pi);
-                    if (lane == 0) {
-                        for (int c = 0; c < 2; ++c) {
-                            tma_load_4d(st + c * KCHUNK + pi * QW_PAGE_SIZE * 128, &tmKV, 64 * c, 0, g, page,
-                                        &kv_full[s]);
-                            tma_load_4d(st + (2 + c) * KCHUNK + pi * QW_PAGE_SIZE * 128, &tmKV, 64 * c, 0, Hkv + g,
-                                        page, &kv_full[s]);
-                        }
-                    }
+                    const int page = __shfl_sync(0xffffffffu, page_lane, pi);
+                    if (lane == 0)
+                        for (int c = 0; c < 2; ++c)
+                            tma_load_4d(st + c * KCHUNK + pi * QW_PAGE_SIZE * 128, &tmKV, 64 * c, 0,
+                                        is_v ? Hkv + g : g, page, ful);
                 }
+                return true;
+            };
+            int page_j = page_of(0);
+            bool go = issue(0, page_j, false);
+            for (int j = 0; j < nt && go; ++j) {
+                const int page_next = j + 1 < nt ? page_of(j + 1) : 0;
+                if (j + 1 < nt) go = issue(j + 1, page_next, false);
+                if (go) go = issue(j, page_j, true);
+                page_j = page_next;
             }
         }
     } else if (warp == 1) {
@@ -187,22 +198,23 @@ __global__ void __launch_bounds__(THREADS, 2)
                               kk != 0);
                 }
                 umma_commit(&s_full[j & 1]);
+                umma_commit(&k_empty[j % KV_STAGES]);   // the K slot is free once S_j is computed
             };
-            if (ok) ok = mbar_wait(&kv_full[0], 0, err);
+            if (ok) ok = mbar_wait(&k_full[0], 0, err);
             if (ok) {
                 tc_fence_after();
                 issue_s(0);
             }
             for (int j = 0; j < nt && ok; ++j) {
                 if (j + 1 < nt) {
-                    if (!mbar_wait(&kv_full[(j + 1) % KV_STAGES], ((j + 1) / KV_STAGES) & 1, err)) {
+                    if (!mbar_wait(&k_full[(j + 1) % KV_STAGES], ((j + 1) / KV_STAGES) & 1, err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     issue_s(j + 1);
                 }
-                if (!mbar_wait(p_full, j & 1, err)) {
+                if (!mbar_wait(p_full, j & 1, err) || !mbar_wait(&v_full[j % KV_STAGES], (j / KV_STAGES) & 1, err)) {
                     ok = false;
                     break;
                 }
@@ -215,7 +227,7 @@ __global__ void __launch_bounds__(THREADS, 2)
                               IDESC_PV, (j | kk) != 0);
                 }
                 umma_commit(o_done);
-                umma_commit(&kv_empty[j % KV_STAGES]);
+                umma_commit(&v_empty[j % KV_STAGES]);
             }
             if (!ok) {
                 *abort_flag = 1;
