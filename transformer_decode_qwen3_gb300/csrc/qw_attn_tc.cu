@@ -10,10 +10,11 @@
 //
 //   warp 0      TMA producer (Q once, then K/V tiles)
 //   warp 1      MMA issuer: S_j = Q K_j^T into one of two TMEM buffers, then
-//               O += P_j V_j (V as an MN-major operand) into a TMEM accumulator
+//               O += P_j V_j (P from TMEM, V as an MN-major shared-memory operand)
+//               into a TMEM accumulator
 //   warps 2..5  softmax: thread = row; reads S_j from TMEM, masks keys beyond the
 //               row's position, keeps the running max m and sum l, rescales O in
-//               TMEM when m grows, writes P_j (bf16) to shared memory
+//               TMEM when m grows, writes P_j (bf16) back over its S buffer
 // Scores are in log2 units (scale 1/sqrt(128) * log2 e); the output is O / l.
 #include <cudaTypedefs.h>
 
@@ -29,10 +30,9 @@ constexpr int KCHUNK = BN * 64 * 2;           // 64 keys x 64 dims: one column b
 constexpr int Q_BYTES = 2 * CHUNK;            // 32 KB
 constexpr int KV_STAGES = 2;                  // two CTAs per SM: their softmax warps interleave
 constexpr int KV_STAGE = 4 * KCHUNK;          // K (2 blocks) + V (2 blocks) = 32 KB
-constexpr int P_BYTES = BM * BN * 2;          // 16 KB: one 64-key block
 // The dynamic shared-memory window starts 1024-byte aligned (checked at run time), so no
 // alignment slack is reserved: two CTAs (2 x (112.25 + 1) KB) fit in one SM.
-constexpr int SMEM = Q_BYTES + KV_STAGES * KV_STAGE + P_BYTES + 256;
+constexpr int SMEM = Q_BYTES + KV_STAGES * KV_STAGE + 256;
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 256;           // S0 [0,64), S1 [64,128), O [128,256)
 
@@ -84,8 +84,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     }
     uint8_t* sQ = sm;
     uint8_t* sKV = sm + Q_BYTES;                       // stage s: K blocks at s*KV_STAGE, V blocks at +2*KCHUNK
-    uint8_t* sP = sm + Q_BYTES + KV_STAGES * KV_STAGE;
-    uint64_t* bars = (uint64_t*)(sP + P_BYTES);
+    uint64_t* bars = (uint64_t*)(sm + Q_BYTES + KV_STAGES * KV_STAGE);
     uint64_t* q_full = bars;
     // K and V of a stage are filled and released separately: a K slot frees as soon as its
     // S = Q K^T is done, so the next K loads start well before their tile is needed
@@ -186,7 +185,7 @@ __global__ void __launch_bounds__(THREADS, 2)
         }
     } else if (warp == 1) {
         if (lane == 0 && nt > 0) {
-            const uint32_t aq = smem_u32(sQ), ap = smem_u32(sP);
+            const uint32_t aq = smem_u32(sQ);
             bool ok = mbar_wait(q_full, 0, err);
             auto issue_s = [&](int j) {
                 const uint32_t k0 = smem_u32(sKV + (j % KV_STAGES) * KV_STAGE);
@@ -223,8 +222,8 @@ __global__ void __launch_bounds__(THREADS, 2)
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
                     // A = P (K-major, keys 16 kk ..), B = V (MN-major: keys 16 kk .. are rows 16 kk ..)
-                    umma_bf16(tmem + 2 * BN, umma_desc_sw128(ap + kk * 32), desc_mn_sw128(v0 + kk * 16 * 128, KCHUNK),
-                              IDESC_PV, (j | kk) != 0);
+                    umma_bf16_ts(tmem + 2 * BN, tmem + (uint32_t)((j & 1) * BN + kk * 8),
+                                 desc_mn_sw128(v0 + kk * 16 * 128, KCHUNK), IDESC_PV, (j | kk) != 0);
                 }
                 umma_commit(o_done);
                 umma_commit(&v_empty[j % KV_STAGES]);
@@ -293,12 +292,12 @@ __global__ void __launch_bounds__(THREADS, 2)
                 pk[i >> 1] = pack_bf16x2(p0, p1);
             }
             const float sum = ((sums[0] + sums[1]) + (sums[2] + sums[3])) + ((sums[4] + sums[5]) + (sums[6] + sums[7]));
-            // P_j may overwrite P_{j-1} and O may be rescaled once P_{j-1} V_{j-1} is done
-            if (j > 0) {
+            // O may be rescaled once P_{j-1} V_{j-1} is done; tcgen05.ld/st are warp-collective, so
+            // the warp rescales when any of its rows needs it (rare: the reference max is lazy)
+            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
                 if (!mbar_wait(o_done, (j - 1) & 1, err) || *abort_flag) break;
                 tc_fence_after();
-                // tcgen05.ld/st are warp-collective: rescale when any row of the warp needs it
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                {
 #pragma unroll 1
                     for (int half = 0; half < 2; ++half) {  // 64 columns at a time
                         float o[64];
@@ -314,12 +313,11 @@ __global__ void __launch_bounds__(THREADS, 2)
                     }
                 }
             }
-#pragma unroll
-            for (int unit = 0; unit < BN / 8; ++unit)   // 16-byte units of the row's 128 bytes
-                *(uint4*)(sP + r * 128 + ((unit ^ (r & 7)) << 4)) =
-                    make_uint4(pk[4 * unit], pk[4 * unit + 1], pk[4 * unit + 2], pk[4 * unit + 3]);
+            // P_j (bf16 pairs) over the first 32 columns of its own S buffer: the P V MMA reads A
+            // from tensor memory, and buffer j & 1 is not written again before P_j V_j is done
+            tmem_st32_nowait(sbase, (const float*)pk);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             l = l * alpha + sum;
-            fence_proxy_async();   // the MMA reads P through the async proxy
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
