@@ -155,6 +155,11 @@ def test_config3_prefill_8x2048(full):
     last = torch.empty(B, V, device="cuda")
     model.prefill(ids.cuda(), pos.cuda(), cu, kv, bt, last)
     model.check()
+    # the kernels are deterministic: a second prefill reproduces every logit bit for bit
+    again = torch.empty(B, V, device="cuda")
+    model.prefill(ids.cuda(), pos.cuda(), cu, kv, bt, again)
+    model.check()
+    assert torch.equal(again, last), "prefill is not deterministic"
     probe = [0, 1, 63, 64, 1000, T - 1]
     for s in (0, B - 1):
         rows = [s * T + r for r in probe]

@@ -5,16 +5,15 @@
 // (rows 64..127), which share the KV head (grouped-query attention).  Keys and
 // values stream from the paged cache in tiles of 64 positions (4 pages), loaded by
 // TMA through a 4-D view of the pool ([page][K/V, head][slot][dim], 16-slot boxes,
-// 128-byte swizzle) into rings of 3 K tiles and 2 V tiles; two CTAs share an SM so that
-// one's softmax overlaps the other's loads and MMAs.
+// 128-byte swizzle) into a 2-deep ring; two CTAs share an SM so that one's softmax
+// overlaps the other's loads and MMAs.
 //
 //   warp 0      TMA producer (Q once, then K/V tiles)
 //   warp 1      MMA issuer: S_j = Q K_j^T into one of two TMEM buffers, then
-//               O += P_j V_j (P from TMEM, V as an MN-major shared-memory operand)
-//               into a TMEM accumulator
+//               O += P_j V_j (V as an MN-major operand) into a TMEM accumulator
 //   warps 2..5  softmax: thread = row; reads S_j from TMEM, masks keys beyond the
 //               row's position, keeps the running max m and sum l, rescales O in
-//               TMEM when m grows, writes P_j (bf16) back over its S buffer
+//               TMEM when m grows, writes P_j (bf16) to shared memory
 // Scores are in log2 units (scale 1/sqrt(128) * log2 e); the output is O / l.
 #include <cudaTypedefs.h>
 
@@ -28,11 +27,12 @@ constexpr int BM = 128, BN = 64, HD = 128;
 constexpr int CHUNK = 128 * 64 * 2;           // 128 rows x 64 bf16, one 128-byte-swizzle column block
 constexpr int KCHUNK = BN * 64 * 2;           // 64 keys x 64 dims: one column block of a K or V tile
 constexpr int Q_BYTES = 2 * CHUNK;            // 32 KB
-constexpr int K_STAGES = 3, V_STAGES = 2;     // rings of 16 KB K and V tiles (K runs ahead)
-constexpr int KV_TILE = 2 * KCHUNK;           // 64 keys x 128 dims of K or of V
+constexpr int KV_STAGES = 2;                  // two CTAs per SM: their softmax warps interleave
+constexpr int KV_STAGE = 4 * KCHUNK;          // K (2 blocks) + V (2 blocks) = 32 KB
+constexpr int P_BYTES = BM * BN * 2;          // 16 KB: one 64-key block
 // The dynamic shared-memory window starts 1024-byte aligned (checked at run time), so no
 // alignment slack is reserved: two CTAs (2 x (112.25 + 1) KB) fit in one SM.
-constexpr int SMEM = Q_BYTES + (K_STAGES + V_STAGES) * KV_TILE + 256;
+constexpr int SMEM = Q_BYTES + KV_STAGES * KV_STAGE + P_BYTES + 256;
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 256;           // S0 [0,64), S1 [64,128), O [128,256)
 
@@ -83,17 +83,17 @@ __global__ void __launch_bounds__(THREADS, 2)
         return;
     }
     uint8_t* sQ = sm;
-    uint8_t* sK = sm + Q_BYTES;                     // [K_STAGES] K tiles
-    uint8_t* sV = sK + K_STAGES * KV_TILE;          // [V_STAGES] V tiles
-    uint64_t* bars = (uint64_t*)(sV + V_STAGES * KV_TILE);
+    uint8_t* sKV = sm + Q_BYTES;                       // stage s: K blocks at s*KV_STAGE, V blocks at +2*KCHUNK
+    uint8_t* sP = sm + Q_BYTES + KV_STAGES * KV_STAGE;
+    uint64_t* bars = (uint64_t*)(sP + P_BYTES);
     uint64_t* q_full = bars;
     // K and V of a stage are filled and released separately: a K slot frees as soon as its
     // S = Q K^T is done, so the next K loads start well before their tile is needed
-    uint64_t* k_full = bars + 1;                   // [K_STAGES]
-    uint64_t* v_full = k_full + K_STAGES;          // [V_STAGES]
-    uint64_t* k_empty = v_full + V_STAGES;         // [K_STAGES]
-    uint64_t* v_empty = k_empty + K_STAGES;        // [V_STAGES]
-    uint64_t* s_full = v_empty + V_STAGES;         // [2]
+    uint64_t* k_full = bars + 1;                   // [KV_STAGES]
+    uint64_t* v_full = k_full + KV_STAGES;         // [KV_STAGES]
+    uint64_t* k_empty = v_full + KV_STAGES;        // [KV_STAGES]
+    uint64_t* v_empty = k_empty + KV_STAGES;       // [KV_STAGES]
+    uint64_t* s_full = v_empty + KV_STAGES;        // [2]
     uint64_t* p_full = s_full + 2;
     uint64_t* o_done = p_full + 1;
     uint32_t* tmem_slot = (uint32_t*)(o_done + 1);
@@ -111,12 +111,10 @@ __global__ void __launch_bounds__(THREADS, 2)
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < K_STAGES; ++s) {
+        for (int s = 0; s < KV_STAGES; ++s) {
             mbar_init(&k_full[s], 1);
-            mbar_init(&k_empty[s], 1);
-        }
-        for (int s = 0; s < V_STAGES; ++s) {
             mbar_init(&v_full[s], 1);
+            mbar_init(&k_empty[s], 1);
             mbar_init(&v_empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) mbar_init(&s_full[s], 1);
@@ -156,18 +154,17 @@ __global__ void __launch_bounds__(THREADS, 2)
             }
             // issue order K_0, then K_{j+1}, V_j for j = 0, 1, ...: K runs one tile ahead of V
             auto issue = [&](int j, int page_lane, bool is_v) -> bool {
-                const int ns = is_v ? V_STAGES : K_STAGES;
-                const int st_i = j % ns;
+                const int st_i = j % KV_STAGES;
                 uint64_t* emp = is_v ? &v_empty[st_i] : &k_empty[st_i];
                 uint64_t* ful = is_v ? &v_full[st_i] : &k_full[st_i];
                 bool ok = true;
-                if (lane == 0) ok = mbar_wait(emp, ((j / ns) & 1) ^ 1, err) && !*abort_flag;
+                if (lane == 0) ok = mbar_wait(emp, ((j / KV_STAGES) & 1) ^ 1, err) && !*abort_flag;
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) {
                     if (lane == 0) *abort_flag = 1;
                     return false;
                 }
-                uint8_t* st = (is_v ? sV : sK) + st_i * KV_TILE;
+                uint8_t* st = sKV + st_i * KV_STAGE + (is_v ? 2 * KCHUNK : 0);
                 if (lane == 0) mbar_arrive_expect_tx(ful, 2 * KCHUNK);
                 for (int pi = 0; pi < PPT; ++pi) {
                     const int page = __shfl_sync(0xffffffffu, page_lane, pi);
@@ -189,10 +186,10 @@ __global__ void __launch_bounds__(THREADS, 2)
         }
     } else if (warp == 1) {
         if (lane == 0 && nt > 0) {
-            const uint32_t aq = smem_u32(sQ);
+            const uint32_t aq = smem_u32(sQ), ap = smem_u32(sP);
             bool ok = mbar_wait(q_full, 0, err);
             auto issue_s = [&](int j) {
-                const uint32_t k0 = smem_u32(sK + (j % K_STAGES) * KV_TILE);
+                const uint32_t k0 = smem_u32(sKV + (j % KV_STAGES) * KV_STAGE);
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t qoff = (kk >> 2) * CHUNK + (kk & 3) * 32;
@@ -201,7 +198,7 @@ __global__ void __launch_bounds__(THREADS, 2)
                               kk != 0);
                 }
                 umma_commit(&s_full[j & 1]);
-                umma_commit(&k_empty[j % K_STAGES]);   // the K slot is free once S_j is computed
+                umma_commit(&k_empty[j % KV_STAGES]);   // the K slot is free once S_j is computed
             };
             if (ok) ok = mbar_wait(&k_full[0], 0, err);
             if (ok) {
@@ -210,27 +207,27 @@ __global__ void __launch_bounds__(THREADS, 2)
             }
             for (int j = 0; j < nt && ok; ++j) {
                 if (j + 1 < nt) {
-                    if (!mbar_wait(&k_full[(j + 1) % K_STAGES], ((j + 1) / K_STAGES) & 1, err)) {
+                    if (!mbar_wait(&k_full[(j + 1) % KV_STAGES], ((j + 1) / KV_STAGES) & 1, err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
                     issue_s(j + 1);
                 }
-                if (!mbar_wait(p_full, j & 1, err) || !mbar_wait(&v_full[j % V_STAGES], (j / V_STAGES) & 1, err)) {
+                if (!mbar_wait(p_full, j & 1, err) || !mbar_wait(&v_full[j % KV_STAGES], (j / KV_STAGES) & 1, err)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t v0 = smem_u32(sV + (j % V_STAGES) * KV_TILE);
+                const uint32_t v0 = smem_u32(sKV + (j % KV_STAGES) * KV_STAGE + 2 * KCHUNK);
 #pragma unroll
                 for (int kk = 0; kk < BN / 16; ++kk) {
                     // A = P (K-major, keys 16 kk ..), B = V (MN-major: keys 16 kk .. are rows 16 kk ..)
-                    umma_bf16_ts(tmem + 2 * BN, tmem + (uint32_t)((j & 1) * BN + kk * 8),
-                                 desc_mn_sw128(v0 + kk * 16 * 128, KCHUNK), IDESC_PV, (j | kk) != 0);
+                    umma_bf16(tmem + 2 * BN, umma_desc_sw128(ap + kk * 32), desc_mn_sw128(v0 + kk * 16 * 128, KCHUNK),
+                              IDESC_PV, (j | kk) != 0);
                 }
                 umma_commit(o_done);
-                umma_commit(&v_empty[j % V_STAGES]);
+                umma_commit(&v_empty[j % KV_STAGES]);
             }
             if (!ok) {
                 *abort_flag = 1;
@@ -296,12 +293,12 @@ __global__ void __launch_bounds__(THREADS, 2)
                 pk[i >> 1] = pack_bf16x2(p0, p1);
             }
             const float sum = ((sums[0] + sums[1]) + (sums[2] + sums[3])) + ((sums[4] + sums[5]) + (sums[6] + sums[7]));
-            // O may be rescaled once P_{j-1} V_{j-1} is done; tcgen05.ld/st are warp-collective, so
-            // the warp rescales when any of its rows needs it (rare: the reference max is lazy)
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            // P_j may overwrite P_{j-1} and O may be rescaled once P_{j-1} V_{j-1} is done
+            if (j > 0) {
                 if (!mbar_wait(o_done, (j - 1) & 1, err) || *abort_flag) break;
                 tc_fence_after();
-                {
+                // tcgen05.ld/st are warp-collective: rescale when any row of the warp needs it
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
                     for (int half = 0; half < 2; ++half) {  // 64 columns at a time
                         float o[64];
@@ -317,11 +314,12 @@ __global__ void __launch_bounds__(THREADS, 2)
                     }
                 }
             }
-            // P_j (bf16 pairs) over the first 32 columns of its own S buffer: the P V MMA reads A
-            // from tensor memory, and buffer j & 1 is not written again before P_j V_j is done
-            tmem_st32_nowait(sbase, (const float*)pk);
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+#pragma unroll
+            for (int unit = 0; unit < BN / 8; ++unit)   // 16-byte units of the row's 128 bytes
+                *(uint4*)(sP + r * 128 + ((unit ^ (r & 7)) << 4)) =
+                    make_uint4(pk[4 * unit], pk[4 * unit + 1], pk[4 * unit + 2], pk[4 * unit + 3]);
             l = l * alpha + sum;
+            fence_proxy_async();   // the MMA reads P through the async proxy
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
