@@ -163,9 +163,16 @@ def max_over_ranks(world, v: float) -> float:
     if world == 1:
         return v
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate(world, ms_local: float, units_per_step: int, K: int):
+    """Whole-job timing of K steps on every rank: (slowest rank's ms, units of all ranks per second)."""
+    ms = max_over_ranks(world, ms_local)
+    return ms, world * units_per_step * K / (ms / 1e3)
 
 
 def timed(fn, K, world):
@@ -419,8 +426,8 @@ def measure(name, bd, model, K, W, world, hbm, tf_burst):
     for i in range(W):
         wl.step(i)
     ms, launches = timed(wl.step, K, world)
-    ms = max_over_ranks(world, ms)
-    out = {"ms_per_step": ms / K, "value": world * wl.units_per_step * K / (ms / 1e3), "gpu_launches": launches}
+    ms, value = aggregate(world, ms, wl.units_per_step, K)
+    out = {"ms_per_step": ms / K, "value": value, "gpu_launches": launches}
     if name == "decode_bs1":
         kms, _ = timed(wl.kernel_only, K, world)
         ach = wl.bytes_per_step(K) / (kms / K / 1e3) / 1e9
