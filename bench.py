@@ -243,6 +243,22 @@ class DecodeBs1:
             h_tok[0] = int(h_out[0])
         return time.perf_counter() - t0, 8, 4
 
+    def generate_e2e(self, K):
+        """qw_generate: the first token in from pinned host memory, K steps decoded, sampled and fed
+        back on the device, the K ids out to the host; wall-clock seconds."""
+        h_tok = torch.empty(1, dtype=torch.int32).pin_memory()
+        h_out = torch.empty(K, dtype=torch.int32).pin_memory()
+        d_tok = torch.empty(1, dtype=torch.int32, device="cuda")
+        d_out = torch.empty(K, dtype=torch.int32, device="cuda")
+        h_tok[0] = int(self.toks[0])
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        d_tok.copy_(h_tok, non_blocking=True)
+        self.model.generate(d_tok, PROMPT, K, self.params, 1, d_out, self.kv, self.bt)
+        h_out.copy_(d_out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return time.perf_counter() - t0
+
     def close(self):
         self.kv.close()
 
@@ -451,6 +467,9 @@ def measure(name, bd, model, K, W, world, hbm, tf_burst):
     e2e_s, h2d, d2h = wl.e2e(K)
     out["e2e"] = {"value": world * wl.units_per_step * K / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": h2d,
                   "d2h_bytes_per_step": d2h}
+    if name == "decode_bs1":  # the whole loop on the device (qw_generate), host copies at the ends only
+        out["generate"] = {"value": world * K / wl.generate_e2e(K), "unit": "tok/s",
+                           "h2d_bytes": 4, "d2h_bytes": 4 * K}
     wl.close()
     return out
 
@@ -491,6 +510,8 @@ def main():
                        "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2 (1.19 GB of weights streamed per step)"},
             "roofline": m["roofline"], "e2e": m["e2e"], "gpu_launches": m["gpu_launches"], "clocks": clk.summary()}
+    if "generate" in m:
+        line["generate"] = m["generate"]
     if not args.no_secondary and rank == 0:
         sec = {}
         for name in METRICS:

@@ -165,6 +165,21 @@ int qw_decode_step(qw_ctx* ctx, const int32_t* tokens, const int32_t* positions,
 int qw_sample(qw_ctx* ctx, const float* logits, int32_t batch, const qw_sample_params* params,
               uint64_t rng_counter, int32_t* out_ids, void* stream);
 
+/* Generate n_steps tokens of one sequence with the article's Step 9 loop run entirely on
+ * the device: step i runs qw_decode_step on the token fed back by step i - 1 at position
+ * start_pos + i, then qw_sample with rng_counter + i, and writes the id to out_ids[i]; the
+ * host never waits on the device.  The same kernels as a host loop of qw_decode_step +
+ * qw_sample, so the ids are identical.
+ *   block_tables  DEVICE int32[1][bt_stride]: pages for positions up to start_pos + n_steps - 1.
+ *   first_token   DEVICE int32[1]: the token at start_pos (e.g. sampled from the prefill).
+ *   params        DEVICE qw_sample_params[1].
+ *   out_ids       DEVICE int32[n_steps]: out_ids[i] is the token for position start_pos + i + 1.
+ * Errors: QW_EINVAL for bad arguments (n_steps < 1, start_pos < 0, or positions beyond
+ * bt_stride * QW_PAGE_SIZE); device-side range errors as for qw_decode_step. */
+int qw_generate(qw_ctx* ctx, qw_kv* kv, const int32_t* block_tables, int32_t bt_stride,
+                const int32_t* first_token, int32_t start_pos, int32_t n_steps,
+                const qw_sample_params* params, uint64_t rng_counter, int32_t* out_ids, void* stream);
+
 /* Decode attention of one layer over the paged cache (Step 5 for one new token per
  * sequence): out[b][h] = softmax(q[b][h] . K^T / sqrt(128)) V over the cached positions
  * 0 .. positions[b] of sequence b, with query head h reading KV head

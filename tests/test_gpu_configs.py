@@ -142,6 +142,44 @@ def test_fused_greedy_hint_and_paths_agree(full):
         model.set_decode_path(0)
 
 
+def test_generate_on_device_equals_host_loop(full):
+    """qw_generate (decode + sample + feedback on the device, no host sync) returns the ids of
+    the host loop of qw_decode_step + qw_sample; both run the same kernels.  The fused kernel
+    adds with float atomics, so ids may part only at a near-tie (top-2 margin < 1e-3); the
+    comparison stops there."""
+    bd, model, orc = full
+    T, n = 40, 24
+    params = bd.sample_params([(0.0, 1, 1.0, 0)])
+    runs = []
+    for r in range(2):
+        kv = bd.KVPool(model, 8)
+        bt = torch.arange(8, dtype=torch.int32, device="cuda").view(1, 8)
+        ids = synth.token_ids(0, 7, T, V).cuda()
+        model.prefill(ids, torch.arange(T, dtype=torch.int32, device="cuda"), [0, T], kv, bt, None)
+        tok0 = torch.tensor([17], dtype=torch.int32, device="cuda")
+        out = torch.empty(n, dtype=torch.int32, device="cuda")
+        margins = []
+        if r == 0:
+            model.generate(tok0, T, n, params, 100, out, kv, bt)
+        else:
+            tok = tok0
+            for i in range(n):
+                lg = torch.empty(1, V, device="cuda")
+                model.decode_step(tok, torch.tensor([T + i], dtype=torch.int32, device="cuda"), kv, bt, lg)
+                top2 = torch.topk(lg[0], 2).values
+                margins.append(float(top2[0] - top2[1]))
+                model.sample(params, 100 + i, out[i:i + 1], logits=lg)
+                tok = out[i:i + 1]
+        model.check()
+        runs.append((out.cpu().tolist(), margins))
+        kv.close()
+    dev, (host, margins) = runs[0][0], runs[1]
+    for i in range(n):
+        if dev[i] != host[i]:
+            assert margins[i] < 1e-3, f"step {i}: {dev[i]} vs {host[i]} with margin {margins[i]:.3e}"
+            break
+
+
 def test_config3_prefill_8x2048(full):
     bd, model, orc = full
     B, T = 8, 2048

@@ -28,7 +28,7 @@ QW_TRACE_SLOTS = 24
 EXPORTED = ["qw_config_default", "qw_init", "qw_destroy", "qw_kv_create", "qw_kv_destroy", "qw_kv_layout",
             "qw_prefill", "qw_decode_step", "qw_sample", "qw_check", "qw_last_error_message",
             "qw_debug_hidden", "qw_set_decode_path", "qw_debug_gemm", "qw_kernel_launches", "qw_attn_decode", "qw_attn_decode_noalloc", "qw_debug_trace",
-            "qw_set_prefill_attention"]
+            "qw_set_prefill_attention", "qw_generate"]
 
 
 class QwConfig(ctypes.Structure):
@@ -84,6 +84,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qw_prefill.argtypes = [vp, vp, vp, ctypes.POINTER(i32), i32, vp, vp, i32, vp, vp]
     lib.qw_decode_step.argtypes = [vp, vp, vp, i32, vp, vp, i32, vp, vp]
     lib.qw_sample.argtypes = [vp, vp, i32, vp, ctypes.c_uint64, vp, vp]
+    lib.qw_generate.argtypes = [vp, vp, vp, i32, vp, i32, i32, vp, ctypes.c_uint64, vp, vp]
     lib.qw_check.argtypes = [vp, vp]
     lib.qw_last_error_message.argtypes = []
     lib.qw_last_error_message.restype = ctypes.c_char_p
@@ -209,6 +210,13 @@ class Model:
         batch = out_ids.numel() if batch is None else batch
         _check(_lib.qw_sample(self.handle, _ptr(logits), batch, _ptr(params), ctypes.c_uint64(rng_counter),
                               _ptr(out_ids), _stream(stream)), "qw_sample")
+
+    def generate(self, first_token, start_pos: int, n_steps: int, params: torch.Tensor, rng_counter: int, out_ids,
+                 kv: "KVPool", block_tables, stream=None):
+        """n_steps decode + sample steps of one sequence with the ids fed back on the device."""
+        _check(_lib.qw_generate(self.handle, kv.handle, _ptr(block_tables), block_tables.shape[-1], _ptr(first_token),
+                                start_pos, n_steps, _ptr(params), ctypes.c_uint64(rng_counter), _ptr(out_ids),
+                                _stream(stream)), "qw_generate")
 
     def attn_decode(self, q, positions, kv: "KVPool", layer: int, block_tables, out, stream=None):
         _check(_lib.qw_attn_decode(self.handle, _ptr(q), _ptr(positions), positions.numel(), kv.handle, layer,

@@ -65,6 +65,7 @@ struct qw_ctx {
     float* gu = nullptr;   // split-K gate/up sums of small-M calls [SPLIT_MAX_M][2 * intermediate]
     uint16_t *h = nullptr, *attn = nullptr, *act = nullptr, *q_bf16 = nullptr;
     float2* rope_tab = nullptr;   // [rows][64] RoPE (cos, sin) of the current prefill
+    int* gen_pos = nullptr;       // [GEN_CHUNK] positions of a qw_generate chunk
     int *tok_seq = nullptr, *iota = nullptr, *rows_last = nullptr, *err = nullptr;
     int4* tiles = nullptr;
     int max_rows = 0, max_splits = 128, max_tiles = 0;
@@ -273,6 +274,7 @@ int qw_init(const qw_config* cfg, const qw_weights* w, qw_ctx** out) {
     const size_t oq = take((size_t)T * ctx->attn_dim * 4);
     const size_t oqb = take((size_t)T * ctx->attn_dim * 2);
     const size_t orope = take((size_t)T * 64 * 8);
+    const size_t ogen = take((size_t)GEN_CHUNK * 4);
     const size_t ologits = take((size_t)c.max_batch * V * 4);
     const size_t ogu = take((size_t)SPLIT_MAX_M * 2 * I * 4);
     const size_t opart = take((size_t)c.max_batch * Hq * ctx->max_splits * (d + 2) * 4);
@@ -295,6 +297,7 @@ int qw_init(const qw_config* cfg, const qw_weights* w, qw_ctx** out) {
     ctx->q = (float*)(W + oq);
     ctx->q_bf16 = (uint16_t*)(W + oqb);
     ctx->rope_tab = (float2*)(W + orope);
+    ctx->gen_pos = (int*)(W + ogen);
     ctx->logits = (float*)(W + ologits);
     ctx->gu = (float*)(W + ogu);
     ctx->part = (float*)(W + opart);
@@ -552,6 +555,27 @@ int qw_sample(qw_ctx* ctx, const float* logits, int32_t batch, const qw_sample_p
     QW_TRY(launch_sample(logits, batch, ctx->cfg.vocab, params, rng_counter, out_ids, hint, ctx->err,
                          (cudaStream_t)stream),
            "sample launch");
+    return QW_OK;
+}
+
+int qw_generate(qw_ctx* ctx, qw_kv* kv, const int32_t* bt, int32_t bt_stride, const int32_t* first_token,
+                int32_t start_pos, int32_t n_steps, const qw_sample_params* params, uint64_t rng_counter,
+                int32_t* out_ids, void* stream) {
+    if (!ctx || !kv || !bt || !first_token || !params || !out_ids) return fail(QW_EINVAL, "qw_generate: null argument");
+    if (n_steps < 1 || start_pos < 0 || bt_stride < 1 ||
+        (int64_t)start_pos + n_steps > (int64_t)bt_stride * QW_PAGE_SIZE)
+        return fail(QW_EINVAL, "qw_generate: n_steps < 1, start_pos < 0 or positions beyond the block table");
+    cudaStream_t st = (cudaStream_t)stream;
+    for (int32_t i = 0; i < n_steps; ++i) {
+        if (i % GEN_CHUNK == 0)  // positions of the next chunk (stream-ordered after the previous steps)
+            QW_TRY(launch_positions(ctx->gen_pos, start_pos + i, std::min<int32_t>(GEN_CHUNK, n_steps - i), st),
+                   "positions launch");
+        const int32_t* tok = i == 0 ? first_token : out_ids + i - 1;
+        int rc = qw_decode_step(ctx, tok, ctx->gen_pos + i % GEN_CHUNK, 1, kv, bt, bt_stride, nullptr, stream);
+        if (rc) return rc;
+        rc = qw_sample(ctx, nullptr, 1, params, rng_counter + (uint64_t)i, out_ids + i, stream);
+        if (rc) return rc;
+    }
     return QW_OK;
 }
 

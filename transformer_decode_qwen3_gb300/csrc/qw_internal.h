@@ -54,6 +54,8 @@ struct GemmEpilogue {
 inline int split_rows(int M) { return (M + 63) / 64 * 128; }
 // Small-M GEMMs (decode batches) take their activations as hi/lo bf16 pairs.
 constexpr int SPLIT_MAX_M = 256;
+// qw_generate writes the positions of this many steps at a time.
+constexpr int GEN_CHUNK = 4096;
 
 // Tensor map of a row-major bf16 matrix [rows][inner] with a (box_rows x box_inner)
 // box and 128-byte swizzling (box_inner * 2 must be 128).
@@ -67,6 +69,8 @@ int gemm_bf16(const void* A, int lda_elems, const CUtensorMap& tmB, int bn, int 
               const GemmEpilogue& ep, cudaStream_t st, const CUtensorMap* tmB_half = nullptr);
 
 // ---------------------------------------------------------------- per-op kernels
+// out[i] = start + i, i < n.
+int launch_positions(int* out, int start, int n, cudaStream_t st);
 // (cos, sin) of the RoPE angles float32(positions[t] * inv_freq[i]), i < 64, for n rows.
 int launch_rope_table(const int* positions, int n, const float* inv_freq, float2* tab, cudaStream_t st);
 int launch_embed(const int* ids, int n, const uint16_t* E, int vocab, int D, float* x, int* err, cudaStream_t st);

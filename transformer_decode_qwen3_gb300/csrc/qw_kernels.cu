@@ -150,6 +150,17 @@ __global__ void qkv_post_kernel(const float* __restrict__ qkv, const int* __rest
     for (int i = 0; i < 4; ++i) dst[lane + 32 * i] = f2bf(y[i]);
 }
 
+__global__ void positions_kernel(int* __restrict__ out, int start, int n) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) out[i] = start + i;
+}
+
+int launch_positions(int* out, int start, int n, cudaStream_t st) {
+    if (n <= 0) return QW_OK;
+    positions_kernel<<<(n + 255) / 256, 256, 0, st>>>(out, start, n);
+    return check_launch();
+}
+
 __global__ void rope_table_kernel(const int* __restrict__ positions, int n, const float* __restrict__ inv_freq,
                                   float2* __restrict__ tab) {
     const int t = blockIdx.x, i = threadIdx.x;
