@@ -25,6 +25,8 @@
 // at no extra tensor-core work (the tile would otherwise be half empty).
 #include <cudaTypedefs.h>
 
+#include <string.h>
+
 #include <vector>
 
 #include "qw_common.cuh"
@@ -41,7 +43,9 @@ struct GemmCfg {
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TMEM_COLS = 2 * BN;            // two accumulators; power of two >= 32
-    static constexpr int XCH_BYTES = 64 * 33 * 4;       // split-mode hand-over of the lo rows
+    // split mode: hand-over of the lo rows (64 x 33 floats); residual add: one 4 KB staging
+    // block (32 rows x 32 fp32, 128-byte swizzled) per epilogue warp for the TMA reduce-add
+    static constexpr int XCH_BYTES = 4 * 4096;
     static constexpr int SMEM = STAGES * STAGE_BYTES + XCH_BYTES + 1024 /*align*/ + 256 /*barriers*/;
     static constexpr int THREADS = 256;                 // warps 0-3: TMA, MMA, TMEM owner, idle; 4-7: epilogue
 };
@@ -97,6 +101,17 @@ QW_DEV void epilogue_chunk(const float (&v)[32], int m, int n, const GemmEpilogu
 }
 
 QW_DEV void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// global[tile at (x, y)] += shared tile, element-wise in L2 (the tensor map's fp32 type).
+QW_DEV void tma_reduce_add_2d(const CUtensorMap* m, const void* smem_src, int x, int y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     (uint64_t)m),
+                 "r"(x), "r"(y), "r"(smem_u32(smem_src))
+                 : "memory");
+}
+QW_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+QW_DEV void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+QW_DEV void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 QW_DEV uint32_t cluster_ctarank() {
     uint32_t r;
@@ -241,7 +256,9 @@ QW_DEV void qkv_rope_tile(uint32_t trow, int m, int M, int n0, int N, const Gemm
 template <int BN, int EPI, bool SPLIT, bool MC>
 __global__ void __launch_bounds__(256, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        int M, int N, int K, int tiles_m, int tiles_n, int ksplit, int share_a, GemmEpilogue ep) {
+                        const __grid_constant__ CUtensorMap tmC, int M, int N, int K, int tiles_m, int tiles_n,
+                        int ksplit, int share_a, GemmEpilogue ep) {
+    // tmC (residual add, not split): ep.out as fp32 [M][N], boxes of 32 x 32, 128-byte swizzle
     // MC: tmB has boxes of BN / 2 rows (each CTA of the pair loads one half)
     using C = GemmCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
@@ -388,8 +405,33 @@ __global__ void __launch_bounds__(256, 1)
             const uint32_t trow = tmem + (uint32_t)(acc * BN) + ((uint32_t)(ew * 32) << 16);
             const int n0 = tn * BN;
             if constexpr (EPI == EPI_QKV_ROPE) qkv_rope_tile<BN>(trow, tm * C::BM + et, M, n0, N, ep, xch);
+            if constexpr (EPI == EPI_RESID_ADD && !SPLIT) {
+                // Each warp stages its 32 rows x 32 columns in shared memory (row = lane, 16-byte
+                // units swizzled by row & 7) and one lane adds the block into the output with a
+                // TMA reduce-add: the residual is never read by the SM, and rows past M are
+                // clipped by the tensor map.
+                uint8_t* xw = (uint8_t*)xch + ew * 4096;
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN && EPI != EPI_QKV_ROPE; c0 += 32) {
+                for (int c0 = 0; c0 < BN; c0 += 32) {
+                    if (n0 + c0 >= N) break;  // uniform
+                    float v[32];
+                    tmem_ld32(trow + c0, v);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        *(float4*)(xw + lane * 128 + ((u ^ (lane & 7)) << 4)) =
+                            make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+                    fence_proxy_async();  // the TMA reads the block through the async proxy
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_reduce_add_2d(&tmC, xw, n0 + c0, tm * C::BM + ew * 32);
+                        bulk_commit();
+                        bulk_wait_read0();  // the block may be overwritten once the TMA has read it
+                    }
+                    __syncwarp();
+                }
+            }
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN && EPI != EPI_QKV_ROPE && !(EPI == EPI_RESID_ADD && !SPLIT); c0 += 32) {
                 if (n0 + c0 >= N) break;  // uniform over the warpgroup
                 float v[32];
                 tmem_ld32(trow + c0, v);
@@ -415,6 +457,7 @@ __global__ void __launch_bounds__(256, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
         }
+        if (EPI == EPI_RESID_ADD && !SPLIT && lane == 0) bulk_wait0();  // the reduce-adds are done
     }
     tc_fence_before();
     __syncthreads();
@@ -451,9 +494,30 @@ int make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t inner, uint64_t 
     return r == CUDA_SUCCESS ? QW_OK : QW_ECUDA;
 }
 
+// fp32 [rows][inner] with 32 x 32 boxes and 128-byte swizzling (the reduce-add target).
+static int make_tmap_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                         uint64_t row_stride_bytes) {
+    if (!load_encode_fn()) return QW_ECUDA;
+    if (((uintptr_t)base & 15) || (row_stride_bytes & 15)) return QW_EINVAL;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? QW_OK : QW_ECUDA;
+}
+
 template <int BN, int EPI, bool SPLIT, bool MC>
 static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N, int K, const GemmEpilogue& ep,
                      cudaStream_t st) {
+    CUtensorMap tc;
+    memset(&tc, 0, sizeof(tc));
+    if (EPI == EPI_RESID_ADD && !SPLIT) {
+        const int rc = make_tmap_f32(&tc, ep.out, (uint64_t)N, (uint64_t)M, (uint64_t)ep.ldo * 4);
+        if (rc) return rc;
+    }
     using C = GemmCfg<BN>;
     auto kern = gemm_bf16_tc_kernel<BN, EPI, SPLIT, MC>;
     static bool attr_set = false;
@@ -509,13 +573,13 @@ static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N,
         cfg.stream = st;
         cfg.attrs = at;
         cfg.numAttrs = 1;
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, M, N, K, tiles_m, tiles_n, 1, share_a, ep);
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, M, N, K, tiles_m, tiles_n, 1, share_a, ep);
         count_launches(1);
         return e == cudaSuccess ? QW_OK : QW_ECUDA;
     }
     const int work = tiles_m * tiles_n * ksplit;
     const int grid = work < n_sm ? work : n_sm;
-    kern<<<grid, C::THREADS, C::SMEM, st>>>(ta, tb, M, N, K, tiles_m, tiles_n, ksplit, share_a, ep);
+    kern<<<grid, C::THREADS, C::SMEM, st>>>(ta, tb, tc, M, N, K, tiles_m, tiles_n, ksplit, share_a, ep);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ECUDA;
 }
