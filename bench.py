@@ -69,7 +69,7 @@ NCU_TRAFFIC = {
     "decode_bs1": ("transformer_decode_qwen3_gb300/csrc/qw_fused.cu",
                    "221b54e4d04fc1a5462d056882278a7913ff6eedbca007d92db2ce57b28af590", 1.253211e9 + 4.761856e6),
     "decode_bs64": ("transformer_decode_qwen3_gb300/csrc/qw_kernels.cu",
-                    "ad37983cb9ec0814d89b38714d83f34560ae61255ed7761e9014616ae8f7e335", 552.45e6 + 3.01e6),
+                    "0d958305b814a36b36a99ccc10f4aaf42dd9c0da01dd41efdc072bf6feef8d0b", 552.44e6 + 3.01e6),
 }
 
 
