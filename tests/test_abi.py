@@ -64,6 +64,26 @@ def test_init_rejects_bad_config_without_touching_the_gpu(lib, field, value):
     assert lib.qw_last_error_message()
 
 
+@pytest.mark.parametrize("shape", [dict(hidden=2560, n_heads=32, n_kv_heads=8, intermediate=9728),    # 4B
+                                   dict(hidden=4096, n_heads=32, n_kv_heads=8, intermediate=12288)])  # 8B
+def test_init_names_the_unsupported_group_size(lib, shape):
+    """Qwen3 sizes with four query heads per KV head are refused with a message (the attention
+    kernels implement groups of two: 0.6B and 1.7B)."""
+    from transformer_decode_qwen3_gb300 import binding
+    cfg = binding.QwConfig()
+    lib.qw_config_default(ctypes.byref(cfg))
+    for k, v in shape.items():
+        setattr(cfg, k, v)
+    h = ctypes.c_void_p()
+    assert lib.qw_init(ctypes.byref(cfg), ctypes.byref(binding.QwWeights()), ctypes.byref(h)) == binding.QW_EINVAL
+    assert b"n_heads == 2 * n_kv_heads" in lib.qw_last_error_message()
+
+
+def test_generate_rejects_bad_arguments(lib):
+    from transformer_decode_qwen3_gb300 import binding
+    assert lib.qw_generate(None, None, None, 1, None, 0, 1, None, ctypes.c_uint64(0), None, None) == binding.QW_EINVAL
+
+
 def test_null_arguments_are_rejected(lib):
     from transformer_decode_qwen3_gb300 import binding
     assert lib.qw_init(None, None, None) == binding.QW_EINVAL
