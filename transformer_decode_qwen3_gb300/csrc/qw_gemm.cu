@@ -18,6 +18,10 @@
 // from L2 per 64-wide K block.  A stage is refilled only once both CTAs' MMAs are done
 // with it (their commits arrive on both CTAs' empty barriers).
 //
+// Residual add (large M): each epilogue warp stages its 32 x 32 fp32 block in shared
+// memory and adds it into the output with a TMA reduce-add, so the SM never reads the
+// residual stream and writes it only in bulk.
+//
 // Split-operand mode (small M, e.g. decode batches): every activation row a is
 // stored as two bf16 rows, hi = bf16(a) in tile rows 0..63 and lo = bf16(a - hi)
 // in rows 64..127, so one M=128 MMA yields hi.W and lo.W side by side and the
