@@ -56,9 +56,9 @@ METRICS = {
     "prefill": "prefill tok/s (Qwen3-0.6B shape, 8 x 2048 causal)",
 }
 WORKLOAD_NAMES = {
-    "decode_bs1": "decode bs1, prompt 512, cache 512->768, greedy (configs[1])",
-    "decode_bs64": "decode bs64, ragged paged caches 128..4096, T 0.7 / top-k 50 / top-p 0.9 (configs[3])",
-    "prefill": "prefill 8 x 2048, causal GQA (configs[2])",
+    "decode_bs1": "decode bs1, prompt 512, cache 512->768, greedy",
+    "decode_bs64": "decode bs64, ragged paged caches 128..4096, T 0.7 / top-k 50 / top-p 0.9",
+    "prefill": "prefill 8 x 2048, causal GQA",
 }
 
 
@@ -194,7 +194,7 @@ def timed(fn, K, world):
 
 # ------------------------------------------------------------------ workloads
 class DecodeBs1:
-    """configs[1]: prompt of 512 random ids, then greedy decode steps."""
+    """Batch 1: a prompt of 512 random ids, then greedy decode steps."""
     units_per_step = 1
 
     def __init__(self, bd, model, n_steps):
@@ -264,7 +264,7 @@ class DecodeBs1:
 
 
 class DecodeBs64:
-    """configs[3]: 64 sequences over ragged synthetic caches, one sampled step each."""
+    """Batch 64: sequences over ragged synthetic caches, one sampled step each."""
     units_per_step = BS64
 
     def __init__(self, bd, model):
@@ -323,7 +323,7 @@ class DecodeBs64:
 
 
 class Prefill:
-    """configs[2]: prefill only, 8 x 2048 random prompts, last-token logits."""
+    """Prefill only: 8 x 2048 random prompts, last-token logits."""
     units_per_step = PREFILL_B * PREFILL_T
 
     def __init__(self, bd, model):

@@ -97,20 +97,20 @@ def _decode_loop(model, bd, orc, kv, bt, cache, T, steps, logits, errs, gpu_ids,
         ref_ids.append(int(np.argmax(ref[0])))
 
 
-def test_config1_prompt5_greedy8(full):
+def test_prompt5_greedy8(full):
     _prompt_then_greedy(full, 5, 8, call=0)
 
 
-def test_config2_prompt512_greedy256(full):
+def test_prompt512_greedy256(full):
     _prompt_then_greedy(full, 512, 256, call=1)
 
 
-def test_config1_fused_decode(full):
+def test_prompt5_greedy8_fused(full):
     """The same workload through the fused persistent decode kernel."""
     _prompt_then_greedy(full, 5, 8, call=0, path=2)
 
 
-def test_config2_fused_decode(full):
+def test_prompt512_greedy256_fused(full):
     _prompt_then_greedy(full, 512, 256, call=1, path=2)
 
 
@@ -180,7 +180,7 @@ def test_generate_on_device_equals_host_loop(full):
             break
 
 
-def test_config3_prefill_8x2048(full):
+def test_prefill_8x2048(full):
     bd, model, orc = full
     B, T = 8, 2048
     n_pages = B * T // Q.PAGE
@@ -211,7 +211,7 @@ def test_config3_prefill_8x2048(full):
         assert Q.rel_l2_rows(last[s:s + 1].cpu().numpy(), ref).max() < Q.LOGIT_TOL
 
 
-def test_config4_batch64_ragged_sampled(full):
+def test_decode_batch64_ragged_sampled(full):
     bd, model, orc = full
     B = 64
     lens = synth.uniform_ints(0, synth.STREAM_LENGTHS, B, 128, 4096).tolist()
@@ -260,7 +260,7 @@ def test_config4_batch64_ragged_sampled(full):
     assert strict >= 1
 
 
-def test_config5_batch16_context32k(full):
+def test_decode_batch16_context32k(full):
     bd, model, orc = full
     B, L, steps = 16, 32768, 32
     per = (L + steps) // Q.PAGE + 1
