@@ -91,7 +91,5 @@ int launch_attn_decode(const float* q, const int* positions, int batch, int Hq, 
 int launch_sample(const float* logits, int batch, int vocab, const qw_sample_params* params, uint64_t rng_counter,
                   int32_t* out_ids, const int* argmax_hint, int* err, cudaStream_t st);
 int launch_bf16_to_f32(const uint16_t* src, float* dst, int n, cudaStream_t st);
-// act (split hi/lo layout) = silu(gu[m][2j]) * gu[m][2j+1] for m < n, j < I.
-int launch_swiglu_split(const float* gu, int n, int I, uint16_t* act, cudaStream_t st);
 
 }  // namespace qw

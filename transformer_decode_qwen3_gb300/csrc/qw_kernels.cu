@@ -800,24 +800,6 @@ int launch_sample(const float* logits, int batch, int vocab, const qw_sample_par
     return check_launch();
 }
 
-// ---------------------------------------------------------------- Step 6: SwiGLU of split-K sums
-__global__ void swiglu_split_kernel(const float* __restrict__ gu, int I, uint16_t* __restrict__ act) {
-    const int m = blockIdx.x;
-    const float* row = gu + (size_t)m * 2 * I;
-    for (int j = 2 * threadIdx.x; j < I; j += 2 * blockDim.x) {
-        const float4 v = *(const float4*)(row + 2 * j);   // gate j, up j, gate j+1, up j+1
-        const float a0 = v.x / (1.0f + expf(-v.x)) * v.y;
-        const float a1 = v.z / (1.0f + expf(-v.z)) * v.w;
-        store_bf16x2(act, I, m, j, a0, a1, 1);
-    }
-}
-
-int launch_swiglu_split(const float* gu, int n, int I, uint16_t* act, cudaStream_t st) {
-    if (n <= 0) return QW_OK;
-    swiglu_split_kernel<<<n, 256, 0, st>>>(gu, I, act);
-    return check_launch();
-}
-
 // ---------------------------------------------------------------- weight staging
 __global__ void bf16_to_f32_kernel(const uint16_t* __restrict__ src, float* __restrict__ dst, int n) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
