@@ -69,7 +69,7 @@ NCU_TRAFFIC = {
     "decode_bs1": ("transformer_decode_qwen3_gb300/csrc/qw_fused.cu",
                    "221b54e4d04fc1a5462d056882278a7913ff6eedbca007d92db2ce57b28af590", 1.253211e9 + 4.761856e6),
     "decode_bs64": ("transformer_decode_qwen3_gb300/csrc/qw_kernels.cu",
-                    "0d958305b814a36b36a99ccc10f4aaf42dd9c0da01dd41efdc072bf6feef8d0b", 552.44e6 + 3.01e6),
+                    "115eff790f8dd54e9f6cec1876bd424e7e359315496e49d14195ae057d64775a", 552.48e6 + 3.01e6),
 }
 
 
