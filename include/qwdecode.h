@@ -62,7 +62,7 @@ typedef struct qw_config {
     int32_t n_layers;
     int32_t hidden;        /* multiple of 256, at most 4096 */
     int32_t n_heads;       /* query heads; n_heads * head_dim is a multiple of 256 */
-    int32_t n_kv_heads;    /* divides n_heads */
+    int32_t n_kv_heads;    /* n_heads / 2: the kernels implement groups of two query heads per KV head */
     int32_t head_dim;      /* must be QW_HEAD_DIM */
     int32_t intermediate;  /* multiple of 128 */
     int32_t vocab;         /* multiple of 32 */
