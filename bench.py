@@ -1,26 +1,28 @@
-"""Benchmark of the Qwen3-0.6B-shaped decoder pass on GB300.
+"""Benchmark of the Qwen3-0.6B-shaped decoder pass on one GB300.
 
 Workloads (--workload; the default is the headline):
-  decode_bs1   batch-1 greedy decode after a 512-token random prompt, the cache
-               growing from 512 to 512 + K positions (K = 256 covers 512 -> 768).
-               One step = embedding, 28 blocks, final norm, tied LM head and the
-               greedy sampler, the sampled id fed back on the device.
-  decode_bs64  64 sequences over ragged synthetic caches of 128..4096 positions
-               (16-token pages), one decode step + sampling (T 0.7, top-k 50,
-               top-p 0.9, Philox seeded by sequence id) per timed step.
-  prefill      prefill of 8 x 2048 random tokens (causal), last-token logits.
-The other two workloads are also measured briefly and reported under "secondary".
+  decode_bs1       batch-1 greedy decode after a 512-token random prompt; the timed steps
+                   run at cache positions 512 .. 512 + K - 1 (K = 256 covers 512 -> 768).
+                   One step = embedding, 28 blocks, final norm, tied LM head and the
+                   greedy sampler, the sampled id fed back on the device.
+  decode_bs64      64 sequences over ragged synthetic caches of 128..4096 positions
+                   (16-token pages), one decode step + sampling (T 0.7, top-k 50,
+                   top-p 0.9, Philox seeded by sequence id) per timed step.
+  prefill          prefill of 8 x 2048 random tokens (causal), last-token logits.
+  decode_bs16_32k  16 sequences at cache length 32768 (synthetic caches, ~60 GB of
+                   bf16 KV), greedy decode steps at positions 32768 .. 32768 + K - 1.
+The other workloads are also measured briefly and reported under "secondary".
 
 Random-init weights (seeded, N(0, 0.02)-shaped) and random token ids: no dataset,
-no checkpoint.  Every step streams 1.19 GB of weights, more than the 129 MB L2,
-so no flush is needed between steps.
+no checkpoint.  Every step streams 1.19 GB of weights (and up to 60 GB of cache),
+more than the 129 MB L2, so no flush is needed between steps.
 
---impl reference times the CPU oracle (numpy float64) on the host cores on the
-same workload and metric.
+The library is single-GPU: it runs on the current CUDA device only and this
+script measures one GPU.  Asked for more (--gpus N > 1, or a torchrun launch
+with WORLD_SIZE > 1), rank 0 prints one line saying so and nothing runs.
 
-Run with several GPUs through torch.distributed.run: every rank runs an
-independent replica (the path has no cross-GPU exchange), the timing is the max
-over ranks and value counts the tokens of all ranks.
+--impl reference times the CPU oracle on the host cores on the same workload,
+metric and config.
 """
 from __future__ import annotations
 
@@ -49,17 +51,29 @@ NORM_BYTES = 2 * (2 * S.hidden + 2 * S.head_dim)
 WEIGHT_BYTES = S.n_layers * (2 * LAYER_PARAMS + NORM_BYTES) + 2 * S.hidden + 2 * S.vocab * S.hidden
 KV_BYTES_PER_POS = S.n_layers * 2 * S.n_kv_heads * S.head_dim * 2          # 114,688 B per cached position
 KV_LAYER_BYTES_PER_POS = KV_BYTES_PER_POS // S.n_layers                     # 4,096 B
-PROMPT, PREFILL_B, PREFILL_T, BS64 = 512, 8, 2048, 64
+PROMPT, PREFILL_B, PREFILL_T, BS64, LONG_B, LONG_L = 512, 8, 2048, 64, 16, 32768
 METRICS = {
     "decode_bs1": "decode tok/s @bs1 (Qwen3-0.6B shape, 512-token prompt, greedy)",
     "decode_bs64": "decode tok/s @bs64 (Qwen3-0.6B shape, ragged caches 128..4096, sampled)",
     "prefill": "prefill tok/s (Qwen3-0.6B shape, 8 x 2048 causal)",
+    "decode_bs16_32k": "decode tok/s @bs16 (Qwen3-0.6B shape, caches at 32768, greedy)",
 }
-WORKLOAD_NAMES = {
-    "decode_bs1": "decode bs1, prompt 512, cache 512->768, greedy",
-    "decode_bs64": "decode bs64, ragged paged caches 128..4096, T 0.7 / top-k 50 / top-p 0.9",
-    "prefill": "prefill 8 x 2048, causal GQA",
-}
+
+
+def config_of(name: str, K: int) -> dict:
+    """The workload description both arms print (no model keys: the shape is in the metric)."""
+    l2 = "inputs larger than L2 (1.19 GB of weights streamed per step), no flush"
+    if name == "decode_bs1":
+        return {"workload": f"decode bs1, prompt {PROMPT}, timed cache positions {PROMPT}..{PROMPT + K - 1}, greedy",
+                "global_batch": 1, "prompt": PROMPT, "cache_start": PROMPT, "cache_end": PROMPT + K, "l2": l2}
+    if name == "decode_bs64":
+        return {"workload": "decode bs64, ragged paged caches 128..4096, T 0.7 / top-k 50 / top-p 0.9",
+                "global_batch": BS64, "page": PAGE, "l2": l2}
+    if name == "prefill":
+        return {"workload": f"prefill {PREFILL_B} x {PREFILL_T}, causal GQA", "global_batch": PREFILL_B,
+                "seq_len": PREFILL_T, "l2": l2}
+    return {"workload": f"decode bs{LONG_B}, caches at {LONG_L}, timed positions {LONG_L}..{LONG_L + K - 1}, greedy",
+            "global_batch": LONG_B, "cache_start": LONG_L, "cache_end": LONG_L + K, "page": PAGE, "l2": l2}
 
 
 # DRAM bytes (read + write) per launch of each workload's roofline kernel, from one ncu
@@ -142,44 +156,10 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def dist_setup():
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    return world, rank, local
-
-
-def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
-
-
-def max_over_ranks(world, v: float) -> float:
-    if world == 1:
-        return v
-    import torch.distributed as dist
-    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
-    t = torch.tensor([v], dtype=torch.float64, device=dev)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def aggregate(world, ms_local: float, units_per_step: int, K: int):
-    """Whole-job timing of K steps on every rank: (slowest rank's ms, units of all ranks per second)."""
-    ms = max_over_ranks(world, ms_local)
-    return ms, world * units_per_step * K / (ms / 1e3)
-
-
-def timed(fn, K, world):
-    """Run fn(i) for i < K between barriers and synchronizes; CUDA-event milliseconds and launches."""
+def timed(fn, K):
+    """Run fn(i) for i < K between synchronizes; CUDA-event milliseconds and kernel launches."""
     from transformer_decode_qwen3_gb300 import binding as bd
     torch.cuda.synchronize()
-    barrier(world)
     launches0 = bd.kernel_launches()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -188,14 +168,43 @@ def timed(fn, K, world):
         fn(i)
     e1.record()
     torch.cuda.synchronize()
-    barrier(world)
     return e0.elapsed_time(e1), bd.kernel_launches() - launches0
 
 
+def profiled(model, fn, K):
+    """Per-kernel-class device milliseconds per step over K more steps (library CUDA events)."""
+    torch.cuda.synchronize()
+    model.profile(True)
+    for i in range(K):
+        fn(i)
+    prof = model.profile(False, fetch=True)
+    return {k: {"ms_per_step": v[0] / K, "launches_per_step": v[1] / K} for k, v in prof.items() if v[1]}
+
+
 # ------------------------------------------------------------------ workloads
+def synth_caches(bd, model, lens, cap):
+    """A KV pool holding the synthetic caches of sequences with lengths `lens` (room for `cap`
+    positions each), pages assigned in order; returns (pool, block tables)."""
+    per = math.ceil(cap / PAGE) + 1
+    kv = bd.KVPool(model, len(lens) * per)
+    pool = kv.view()
+    bt = torch.arange(len(lens) * per, dtype=torch.int32, device="cuda").view(len(lens), per)
+    for s, L in enumerate(lens):
+        n_p = math.ceil(L / PAGE)
+        for layer in range(S.n_layers):
+            for which, std in ((0, 1.0), (1, 0.64)):
+                v = synth.kv_values(0, layer, which, s * (1 << 15) * 1024, L * 1024, std, "cuda")
+                if n_p * PAGE > L:
+                    v = torch.cat([v.view(L, 8, 128), torch.zeros(n_p * PAGE - L, 8, 128, dtype=torch.bfloat16,
+                                                                  device="cuda")])
+                pool[layer, s * per:s * per + n_p, which] = v.view(n_p, PAGE, 8, 128).permute(0, 2, 1, 3)
+    return kv, bt
+
+
 class DecodeBs1:
     """Batch 1: a prompt of 512 random ids, then greedy decode steps."""
     units_per_step = 1
+    roofline_class = "fused"
 
     def __init__(self, bd, model, n_steps):
         self.bd, self.model = bd, model
@@ -215,11 +224,11 @@ class DecodeBs1:
         self.model.decode_step(self.toks[i:i + 1], self.pos[i:i + 1], self.kv, self.bt, None)
         self.model.sample(self.params, i + 1, self.toks[i + 1:i + 2])
 
-    def kernel_only(self, i):  # the forward pass alone (the fused kernel when it is taken)
-        self.model.decode_step(self.toks[i:i + 1], self.pos[i:i + 1], self.kv, self.bt, None)
-
     def bytes_per_step(self, K):
         return WEIGHT_BYTES + sum((PROMPT + i + 1) * KV_BYTES_PER_POS for i in range(K)) / K
+
+    def roofline_bytes(self, K):
+        return self.bytes_per_step(K)
 
     def e2e(self, K):
         """Token and position from pinned host memory in, sampled id out, every step."""
@@ -263,70 +272,88 @@ class DecodeBs1:
         self.kv.close()
 
 
-class DecodeBs64:
-    """Batch 64: sequences over ragged synthetic caches, one sampled step each."""
-    units_per_step = BS64
+class BatchDecode:
+    """Batched decode over synthetic paged caches, one step per sequence per timed step."""
+    roofline_class = "attn"
 
-    def __init__(self, bd, model):
+    def __init__(self, bd, model, lens, params, cap):
         self.bd, self.model = bd, model
-        self.lens = synth.uniform_ints(0, synth.STREAM_LENGTHS, BS64, 128, 4096).tolist()
-        per = 4096 // PAGE + 2
-        self.kv = bd.KVPool(model, BS64 * per)
-        pool = self.kv.view()
-        self.bt = torch.arange(BS64 * per, dtype=torch.int32, device="cuda").view(BS64, per)
-        for s, L in enumerate(self.lens):
-            n_p = math.ceil(L / PAGE)
-            for layer in range(S.n_layers):
-                for which, std in ((0, 1.0), (1, 0.64)):
-                    v = synth.kv_values(0, layer, which, s * (1 << 15) * 1024, L * 1024, std, "cuda")
-                    v = torch.cat([v.view(L, 8, 128), torch.zeros(n_p * PAGE - L, 8, 128, dtype=torch.bfloat16,
-                                                                  device="cuda")])
-                    pool[layer, s * per:s * per + n_p, which] = v.view(n_p, PAGE, 8, 128).permute(0, 2, 1, 3)
-        self.toks = synth.token_ids(0, 3, BS64, S.vocab, device="cuda")
-        self.pos = torch.tensor(self.lens, dtype=torch.int32, device="cuda")
-        self.params = bd.sample_params([(0.7, 50, 0.9, s) for s in range(BS64)])
-        self.out = torch.empty(BS64, dtype=torch.int32, device="cuda")
-        self.q = torch.randn(BS64, S.n_heads, 128, device="cuda")
-        self.attn_out = torch.empty(BS64, S.n_heads * 128, dtype=torch.bfloat16, device="cuda")
+        self.lens = lens
+        self.B = len(lens)
+        self.units_per_step = self.B
+        self.kv, self.bt = synth_caches(bd, model, lens, cap)
+        self.toks = synth.token_ids(0, 3, self.B, S.vocab, device="cuda")
+        self.base = torch.tensor(lens, dtype=torch.int32, device="cuda")
+        self.params = bd.sample_params(params)
+        self.out = torch.empty(self.B, dtype=torch.int32, device="cuda")
+
+    def positions(self, i):
+        return self.base
 
     def step(self, i):
-        self.model.decode_step(self.toks, self.pos, self.kv, self.bt, None)
+        self.model.decode_step(self.toks, self.positions(i), self.kv, self.bt, None)
         self.model.sample(self.params, i, self.out)
 
-    def attention_only(self, i):  # the dominant kernel alone: one layer's split-KV attention
-        self.model.attn_decode(self.q, self.pos, self.kv, i % S.n_layers, self.bt, self.attn_out)
+    def attention_bytes(self, i=0):
+        return sum((L + 1) * KV_LAYER_BYTES_PER_POS for L in self.lens) * S.n_layers
 
-    def bytes_per_step(self, K=None):
-        return WEIGHT_BYTES + sum((L + 1) * KV_BYTES_PER_POS for L in self.lens)
+    def bytes_per_step(self, K=1):
+        return WEIGHT_BYTES + self.attention_bytes()
 
-    def attention_bytes(self):
-        return sum((L + 1) * KV_LAYER_BYTES_PER_POS for L in self.lens)
+    def roofline_bytes(self, K):
+        return self.attention_bytes()
 
     def e2e(self, K):
-        h_in = torch.empty(2, BS64, dtype=torch.int32).pin_memory()
-        h_in[0] = self.toks.cpu()
-        h_in[1] = self.pos.cpu()
-        h_out = torch.empty(BS64, dtype=torch.int32).pin_memory()
-        d_in = torch.empty(2, BS64, dtype=torch.int32, device="cuda")
+        """Tokens and positions from pinned host memory in, sampled ids out, every step."""
+        h_in = torch.empty(K, 2, self.B, dtype=torch.int32).pin_memory()
+        for i in range(K):
+            h_in[i, 0] = self.toks.cpu()
+            h_in[i, 1] = self.positions(i).cpu()
+        h_out = torch.empty(self.B, dtype=torch.int32).pin_memory()
+        d_in = torch.empty(2, self.B, dtype=torch.int32, device="cuda")
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         for i in range(K):
-            d_in.copy_(h_in, non_blocking=True)
+            d_in.copy_(h_in[i], non_blocking=True)
             self.model.decode_step(d_in[0], d_in[1], self.kv, self.bt, None)
             self.model.sample(self.params, i, self.out)
             h_out.copy_(self.out, non_blocking=True)
             torch.cuda.current_stream().synchronize()
-        return time.perf_counter() - t0, 2 * BS64 * 4, BS64 * 4
+        return time.perf_counter() - t0, 2 * self.B * 4, self.B * 4
 
     def close(self):
         self.kv.close()
 
 
+class DecodeBs64(BatchDecode):
+    """Batch 64: ragged synthetic caches 128..4096, one sampled step each (the same step repeated)."""
+
+    def __init__(self, bd, model, K):
+        lens = synth.uniform_ints(0, synth.STREAM_LENGTHS, BS64, 128, 4096).tolist()
+        super().__init__(bd, model, lens, [(0.7, 50, 0.9, s) for s in range(BS64)], 4096 + PAGE)
+
+
+class DecodeBs16Long(BatchDecode):
+    """Batch 16 at cache length 32768: greedy steps at positions 32768 + i (the cache grows)."""
+
+    def __init__(self, bd, model, K):
+        super().__init__(bd, model, [LONG_L] * LONG_B, [(0.0, 1, 1.0, s) for s in range(LONG_B)], LONG_L + K + 8)
+        self.K = K
+        self.pos = self.base.view(1, -1) + torch.arange(K + 8, dtype=torch.int32, device="cuda").view(-1, 1)
+
+    def positions(self, i):
+        return self.pos[i % (self.K + 8)]
+
+    def attention_bytes(self, i=None):
+        return self.B * (LONG_L + 1 + (self.K - 1) / 2) * KV_LAYER_BYTES_PER_POS * S.n_layers
+
+
 class Prefill:
     """Prefill only: 8 x 2048 random prompts, last-token logits."""
     units_per_step = PREFILL_B * PREFILL_T
+    roofline_class = "gemm"
 
-    def __init__(self, bd, model):
+    def __init__(self, bd, model, K):
         self.bd, self.model = bd, model
         B, T = PREFILL_B, PREFILL_T
         self.kv = bd.KVPool(model, B * T // PAGE)
@@ -371,37 +398,44 @@ class Prefill:
 
 # ------------------------------------------------------------------ CPU oracle
 def oracle_rate(workload: str, max_seconds=15.0):
-    """The oracle, unmodified, on a bounded sample of the workload; (units/s, sample text)."""
+    """The oracle, unmodified, on a bounded sample of the workload; (units/s, sample text, threads)."""
     import numpy as np
     from oracle import qwen3_ref as R
     w = synth.make_weights(S)
     orc = R.Qwen3Oracle(w, S)
+    threads = os.cpu_count()
     if workload == "prefill":
         T = 256                         # a 256-token prefix of sequence 0
         ids = synth.token_ids(0, 2, T, S.vocab).numpy()
         t0 = time.perf_counter()
         orc.forward(ids, np.arange(T), orc.new_cache(), last_only=True)
         dt = time.perf_counter() - t0
-        return T / dt, f"prefill of the first {T} tokens of one 2048-token sequence ({dt:.1f} s)"
-    if workload == "decode_bs64":
-        lens = synth.uniform_ints(0, synth.STREAM_LENGTHS, BS64, 128, 4096).tolist()
-        toks = synth.token_ids(0, 3, BS64, S.vocab)
-        t0 = time.perf_counter()
-        n = 0
-        while n < 2 or (time.perf_counter() - t0 < max_seconds and n < BS64):
+        return T / dt, f"prefill of the first {T} tokens of one 2048-token sequence ({dt:.1f} s)", threads
+    if workload in ("decode_bs64", "decode_bs16_32k"):
+        if workload == "decode_bs64":
+            lens = synth.uniform_ints(0, synth.STREAM_LENGTHS, BS64, 128, 4096).tolist()
+            params = (0.7, 50, 0.9)
+        else:
+            lens = [LONG_L] * LONG_B
+            params = (0.0, 1, 1.0)
+        toks = synth.token_ids(0, 3, len(lens), S.vocab)
+        per_tok = S.n_kv_heads * 128
+        elapsed, n = 0.0, 0
+        while n < 1 or (elapsed < max_seconds and n < len(lens)):
             cache = [None] * S.n_layers
-            for layer in range(S.n_layers):
-                per_tok = S.n_kv_heads * 128
+            for layer in range(S.n_layers):        # cache set-up, not timed
                 k = synth.kv_values(0, layer, 0, n * (1 << 15) * per_tok, lens[n] * per_tok, 1.0)
                 v = synth.kv_values(0, layer, 1, n * (1 << 15) * per_tok, lens[n] * per_tok, 0.64)
                 cache[layer] = R.LayerCache(R.bf16_to_f64(k).reshape(lens[n], 8, 128).transpose(1, 0, 2),
                                             R.bf16_to_f64(v).reshape(lens[n], 8, 128).transpose(1, 0, 2),
                                             np.arange(lens[n]))
+            t0 = time.perf_counter()
             logits = orc.forward([int(toks[n])], [lens[n]], cache, last_only=True)
-            R.sample(logits[0], 0.7, 50, 0.9, R.sampling_uniform(n, 0))
+            R.sample(logits[0], *params, R.sampling_uniform(n, 0))
+            elapsed += time.perf_counter() - t0
             n += 1
-        dt = time.perf_counter() - t0
-        return n / dt, f"{n} of the 64 sequences, one sampled decode step each ({dt:.1f} s, cache set-up included)"
+        return n / elapsed, (f"{n} of the {len(lens)} sequences, one decode step each ({elapsed:.1f} s timed; "
+                             f"cache set-up untimed)"), threads
     ids = synth.token_ids(0, 1, PROMPT, S.vocab).numpy()
     cache = orc.new_cache()
     logits = orc.forward(ids, np.arange(PROMPT), cache, last_only=True)
@@ -413,63 +447,67 @@ def oracle_rate(workload: str, max_seconds=15.0):
         tok = int(np.argmax(logits[0]))
         n += 1
     dt = time.perf_counter() - t0
-    return n / dt, f"{n} batch-1 decode steps after the 512-token prompt ({dt:.1f} s; prefill untimed)"
+    return n / dt, f"{n} batch-1 decode steps after the 512-token prompt ({dt:.1f} s; prefill untimed)", threads
 
 
-def run_reference(args, world, rank):
-    if rank != 0:
-        return
-    v, sample = oracle_rate(args.workload, max_seconds=max(5.0, min(60.0, 0.25 * args.steps)))
+def run_reference(args):
+    v, sample, threads = oracle_rate(args.workload, max_seconds=max(5.0, min(60.0, 0.25 * args.steps)))
     unit = "tok/s"
     line = {"metric": METRICS[args.workload], "value": v, "unit": unit, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded random-init weights and token ids)",
-            "impl": "reference", "config": {"workload": WORKLOAD_NAMES[args.workload]},
-            "cpu_baseline": {"value": v, "unit": unit, "cores": os.cpu_count(), "kind": "oracle", "sample": sample},
+            "impl": "reference", "config": config_of(args.workload, args.steps),
+            "cpu_baseline": {"value": v, "unit": unit, "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
 # ------------------------------------------------------------------ main
-def measure(name, bd, model, K, W, world, hbm, tf_burst):
-    """Returns the JSON fields of one workload measured with K timed steps after W warm-ups."""
+def make_workload(name, bd, model, K, W):
     if name == "decode_bs1":
-        wl = DecodeBs1(bd, model, max(K, W))
-    elif name == "decode_bs64":
-        wl = DecodeBs64(bd, model)
-    else:
-        wl = Prefill(bd, model)
+        return DecodeBs1(bd, model, max(K, W))
+    if name == "decode_bs64":
+        return DecodeBs64(bd, model, max(K, W))
+    if name == "decode_bs16_32k":
+        return DecodeBs16Long(bd, model, max(K, W))
+    return Prefill(bd, model, max(K, W))
+
+
+def measure(name, bd, model, K, W, hbm, tf_burst):
+    """Returns the JSON fields of one workload measured with K timed steps after W warm-ups."""
+    wl = make_workload(name, bd, model, K, W)
     for i in range(W):
         wl.step(i)
-    ms, launches = timed(wl.step, K, world)
-    ms, value = aggregate(world, ms, wl.units_per_step, K)
-    out = {"ms_per_step": ms / K, "value": value, "gpu_launches": launches}
-    if name == "decode_bs1":
-        kms, _ = timed(wl.kernel_only, K, world)
-        ach = wl.bytes_per_step(K) / (kms / K / 1e3) / 1e9
-        out["roofline"] = {"bound": "hbm", "kernel": "decode step (the fused batch-1 kernel)", "achieved": ach,
-                           "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": ncu_traffic(name),
-                           "algorithmic_bytes": wl.bytes_per_step(K), "kernel_ms": kms / K}
-    elif name == "decode_bs64":
-        kms, _ = timed(wl.attention_only, K, world)
-        ach = wl.attention_bytes() / (kms / K / 1e3) / 1e9
-        out["roofline"] = {"bound": "hbm", "kernel": "split-KV decode attention (one layer)", "achieved": ach,
-                           "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": ncu_traffic(name),
-                           "algorithmic_bytes": wl.attention_bytes(), "kernel_ms": kms / K,
-                           "step_hbm_frac": wl.bytes_per_step() / (ms / K / 1e3) / 1e9 / hbm}
-    else:
+    ms, launches = timed(wl.step, K)
+    out = {"ms_per_step": ms / K, "value": wl.units_per_step * K / (ms / 1e3), "gpu_launches": launches}
+    # per-kernel-class device time over K more steps, CUDA events on the launching stream
+    kern = profiled(model, wl.step, K)
+    out["kernels"] = kern
+    cls_ms = kern.get(wl.roofline_class, {}).get("ms_per_step")
+    if name == "prefill":
         lin, attn, head = wl.flops()
-        ach = (lin + attn + head) / (ms / K / 1e3) / 1e12
-        out["roofline"] = {"bound": "tensor", "kernel": "prefill step (GEMMs + attention)", "achieved": ach,
-                           "peak": tf_burst, "unit": "TFLOP/s", "frac": ach / tf_burst, "traffic": None,
-                           "algorithmic_flop": lin + attn + head,
-                           "linear_frac_of_peak": lin / (ms / K / 1e3) / 1e12 / tf_burst}
+        ach = lin / (cls_ms / 1e3) / 1e12
+        attn_ms = kern["attn"]["ms_per_step"]
+        out["roofline"] = {"bound": "tensor", "kernel": "prefill projections (tcgen05 GEMMs, all 4 x 28 per step)",
+                           "achieved": ach, "peak": tf_burst, "unit": "TFLOP/s", "frac": ach / tf_burst,
+                           "traffic": None, "algorithmic_flop": lin, "kernel_ms": cls_ms,
+                           "gemm_frac": ach / tf_burst,
+                           "attention_frac": attn / (attn_ms / 1e3) / 1e12 / tf_burst,
+                           "step_frac": (lin + attn + head) / (ms / K / 1e3) / 1e12 / tf_burst}
+    else:
+        nbytes = wl.roofline_bytes(K)
+        ach = nbytes / (cls_ms / 1e3) / 1e9
+        what = ("decode step (the fused batch-1 kernel)" if name == "decode_bs1"
+                else "split-KV decode attention + merge (all 28 layers of a step)")
+        out["roofline"] = {"bound": "hbm", "kernel": what, "achieved": ach, "peak": hbm, "unit": "GB/s",
+                           "frac": ach / hbm, "traffic": ncu_traffic(name), "algorithmic_bytes": nbytes,
+                           "kernel_ms": cls_ms,
+                           "step_hbm_frac": wl.bytes_per_step(K) / (ms / K / 1e3) / 1e9 / hbm}
     e2e_s, h2d, d2h = wl.e2e(K)
-    out["e2e"] = {"value": world * wl.units_per_step * K / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": h2d,
+    out["e2e"] = {"value": wl.units_per_step * K / e2e_s, "unit": "tok/s", "h2d_bytes_per_step": h2d,
                   "d2h_bytes_per_step": d2h}
     if name == "decode_bs1":  # the whole loop on the device (qw_generate), host copies at the ends only
-        out["generate"] = {"value": world * K / wl.generate_e2e(K), "unit": "tok/s",
-                           "h2d_bytes": 4, "d2h_bytes": 4 * K}
+        out["generate"] = {"value": K / wl.generate_e2e(K), "unit": "tok/s", "h2d_bytes": 4, "d2h_bytes": 4 * K}
     wl.close()
     return out
 
@@ -481,16 +519,20 @@ def main():
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--workload", default="decode_bs1", choices=list(METRICS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--no-secondary", action="store_true", help="skip the other two workloads")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the other workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    world, rank, local = dist_setup()
-    if args.impl == "reference":
-        run_reference(args, world, rank)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.gpus > 1 or world > 1:
+        if int(os.environ.get("RANK", "0")) == 0:
+            print(json.dumps({"metric": METRICS[args.workload], "impl": args.impl, "n_gpus": max(args.gpus, world),
+                              "unavailable": "single-GPU library: it measures one GPU only"}), flush=True)
         return
-    torch.cuda.set_device(local)
+    if args.impl == "reference":
+        run_reference(args)
+        return
     from transformer_decode_qwen3_gb300 import binding as bd
     bd.load()
     hbm, tf_burst, tf_sust, peak_kind = peaks()
@@ -499,38 +541,32 @@ def main():
     del w
     torch.cuda.empty_cache()
     with ClockSampler(torch.cuda.current_device()) as clk:
-        m = measure(args.workload, bd, model, args.steps, args.warmup, world, hbm, tf_burst)
+        m = measure(args.workload, bd, model, args.steps, args.warmup, hbm, tf_burst)
     m["roofline"]["peak_kind"] = f"{peak_kind} ({'copy bandwidth' if m['roofline']['unit'] == 'GB/s' else 'bf16 burst'})"
-    line = {"metric": METRICS[args.workload], "value": m["value"], "unit": "tok/s", "n_gpus": world,
+    line = {"metric": METRICS[args.workload], "value": m["value"], "unit": "tok/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded random-init bf16 weights and token ids)",
-            "config": {"workload": WORKLOAD_NAMES[args.workload], "global_batch": world *
-                       {"decode_bs1": 1, "decode_bs64": BS64, "prefill": PREFILL_B}[args.workload],
-                       "parallelism": f"replicas x{world}",
-                       "l2": "inputs larger than L2 (1.19 GB of weights streamed per step)"},
-            "roofline": m["roofline"], "e2e": m["e2e"], "gpu_launches": m["gpu_launches"], "clocks": clk.summary()}
+            "config": config_of(args.workload, args.steps), "roofline": m["roofline"], "e2e": m["e2e"],
+            "gpu_launches": m["gpu_launches"], "kernels": m["kernels"], "clocks": clk.summary()}
     if "generate" in m:
         line["generate"] = m["generate"]
-    if not args.no_secondary and rank == 0:
+    if not args.no_secondary:
         sec = {}
         for name in METRICS:
             if name == args.workload:
                 continue
-            r = measure(name, bd, model, 5 if name != "decode_bs1" else 64, 3, 1, hbm, tf_burst)
+            K2 = 64 if name == "decode_bs1" else (16 if name == "decode_bs16_32k" else 5)
+            r = measure(name, bd, model, K2, 3, hbm, tf_burst)
             sec[name] = {"tok_s": r["value"], "ms_per_step": r["ms_per_step"], "roofline": r["roofline"],
-                         "e2e_tok_s": r["e2e"]["value"]}
+                         "e2e_tok_s": r["e2e"]["value"], "kernels": r["kernels"], "config": config_of(name, K2)}
+            torch.cuda.empty_cache()
         line["secondary"] = sec
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, sample = oracle_rate(args.workload)
-        line["cpu_baseline"] = {"value": v, "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
-                                "sample": sample}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    if not args.no_cpu_baseline:
+        v, sample, threads = oracle_rate(args.workload)
+        line["cpu_baseline"] = {"value": v, "unit": "tok/s", "cores": threads, "kind": "oracle", "sample": sample}
+    print(json.dumps(line), flush=True)
     model.close()
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
 
 
 if __name__ == "__main__":

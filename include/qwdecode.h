@@ -51,6 +51,15 @@ extern "C" {
 #define QW_NOALLOC_SCRATCH_FLOATS (1 << 20) /* fixed scratch of qw_attn_decode_noalloc: 4 MiB */
 #define QW_TRACE_SLOTS 24  /* timestamps per CTA and layer in qw_debug_trace */
 
+/* Kernel classes of qw_debug_profile. */
+#define QW_PROF_GEMM 0     /* tensor-core projections (q|k|v, o_proj, gate/up, down) */
+#define QW_PROF_ATTN 1     /* attention (prefill flash kernel, split-KV decode + merge) */
+#define QW_PROF_OTHER 2    /* embedding, RMSNorm, QK-Norm/RoPE/cache write, RoPE table */
+#define QW_PROF_LMHEAD 3   /* final norm + LM head */
+#define QW_PROF_SAMPLE 4   /* sampler */
+#define QW_PROF_FUSED 5    /* the fused batch-1 decode kernel */
+#define QW_PROF_CLASSES 6
+
 typedef struct qw_ctx qw_ctx;
 typedef struct qw_kv qw_kv;
 
@@ -214,8 +223,10 @@ int qw_attn_decode(qw_ctx* ctx, const float* q, const int32_t* positions, int32_
  * Limits: batch * n_heads * 130 <= QW_NOALLOC_SCRATCH_FLOATS (batch * n_heads <= 8065),
  * else QW_EINVAL with nothing launched.  Page ids outside [0, n_pages) are skipped but,
  * with no context, not reported.
- * The first call on each device looks up the array's device address (once per device,
- * with that device current); make that first call before any stream capture.  All calls
+ * Every call looks up the array's address in the current device's current context (a
+ * lookup, no allocation), so a cudaDeviceReset or a change of context in between is safe;
+ * the first call on a device may also load the library's device code, so make that first
+ * call before any stream capture.  All calls
  * share the one array and nothing in it needs to start at zero: calls whose GPU work can
  * overlap (different streams, several host threads) race on it, so serialise them. */
 int qw_attn_decode_noalloc(const float* q, const int32_t* positions, int32_t batch, int32_t n_heads,
@@ -262,6 +273,14 @@ int qw_debug_gemm(const uint16_t* A, const uint16_t* B, void* C, int32_t M, int3
  * keys start / done, 20/21: first key stage arrived / its scores published, 22/23: SM
  * clock64 at 20/21 (cycles, not ns); layer n_layers: LM head wait begin/end and done).  *n_needed receives the buffer length.  Synchronous. */
 int qw_debug_trace(qw_ctx* ctx, int32_t enable, uint64_t* host_out, int64_t n, int64_t* n_needed);
+
+/* Device time per kernel class, for measurement.  enable = 1: from now on record a CUDA
+ * event pair on the launching stream around every launch (forgetting earlier records);
+ * enable = 0: stop recording.  ms_out (nullable, HOST double[QW_PROF_CLASSES]) and
+ * count_out (nullable, HOST int64[QW_PROF_CLASSES]) receive, after a device
+ * synchronisation, the summed milliseconds and the number of launches of each class
+ * (QW_PROF_*) recorded since the last enable.  Not for use inside stream capture. */
+int qw_debug_profile(qw_ctx* ctx, int32_t enable, double* ms_out, int64_t* count_out);
 
 /* Select the prefill attention kernel: 0 = tcgen05/TMEM flash kernel (default),
  * 1 = mma.sync flash kernel.  For comparisons in tests. */

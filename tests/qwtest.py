@@ -125,3 +125,17 @@ def sample_exempt(detail: dict, top_p: float, tol=1e-3) -> bool:
         return False
     return (detail["draw_gap"] < tol or abs(detail["cum_before_cutoff"] - top_p) < tol
             or abs(detail["cum_at_cutoff"] - top_p) < tol)
+
+
+def split_rows(a: torch.Tensor) -> torch.Tensor:
+    """The hi/lo bf16 layout of float rows a[M][K] that split-mode projections read."""
+    M, K = a.shape
+    tiles = (M + 63) // 64
+    out = torch.zeros(tiles * 128, K, dtype=torch.bfloat16, device=a.device)
+    hi = a.to(torch.bfloat16)
+    lo = (a - hi.float()).to(torch.bfloat16)
+    idx = torch.arange(M, device=a.device)
+    dst = (idx // 64) * 128 + idx % 64
+    out[dst] = hi
+    out[dst + 64] = lo
+    return out

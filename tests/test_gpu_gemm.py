@@ -3,6 +3,8 @@ PyTorch fp32 reference of the same contraction, through the C ABI hook."""
 import pytest
 import torch
 
+from tests import qwtest as Q
+
 pytestmark = pytest.mark.gpu
 
 
@@ -61,7 +63,7 @@ def test_gemm_split_operand(bd, M, N, K, bn, epi):
     a = (torch.randn(M, K, generator=g) * 0.5).cuda()
     B = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16).cuda()
     ref = a @ B.float().T
-    A = bd.split_rows(a)
+    A = Q.split_rows(a)
     if epi == 2:
         C = torch.zeros(A.shape[0], N // 2, dtype=torch.bfloat16, device="cuda")
         bd.debug_gemm(A, B, C, epi=2, bn=bn, split=True, M=M)
@@ -91,7 +93,7 @@ def test_gemm_split_k_atomic(bd, M, N, K, bn):
     B = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16).cuda()
     X = torch.randn(M, N, device="cuda")
     C = X.clone()
-    bd.debug_gemm(bd.split_rows(a), B, C, epi=3, bn=bn, split=True, M=M)
+    bd.debug_gemm(Q.split_rows(a), B, C, epi=3, bn=bn, split=True, M=M)
     torch.cuda.synchronize()
     ref = a @ B.float().T
     err = (C - X - ref).norm() / ref.norm()

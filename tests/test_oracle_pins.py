@@ -265,6 +265,80 @@ def test_ffn_matches_scalar_loops(tiny_shape):
             assert abs(got[r, o] - expect) < 1e-11 * (1 + abs(expect))
 
 
+def _scalar_ffn(W, prefix, x_row, S):
+    a = []
+    Wg, Wu, Wd = (W[f"{prefix}.{n}.weight"] for n in ("gate_proj", "up_proj", "down_proj"))
+    for i in range(S.intermediate):
+        g = sum(Wg[i][c] * x_row[c] for c in range(S.hidden))
+        u = sum(Wu[i][c] * x_row[c] for c in range(S.hidden))
+        a.append(g / (1 + math.exp(-g)) * u)
+    return [sum(Wd[o][i] * a[i] for i in range(S.intermediate)) for o in range(S.hidden)]
+
+
+def test_transformer_block_matches_scalar_loops(tiny_shape):
+    """Step 7 composition with every sublayer active: h = rms(x, w_in); x1 = x + Wo attn(h);
+    x2 = x1 + ffn(rms(x1, w_post)).  Distinct random norm weights catch a swapped weight, an
+    FFN fed rms(x) instead of rms(x1), or a dropped residual."""
+    S = tiny_shape
+    _, m = _tiny_model(S)
+    rng = np.random.default_rng(12)
+    pl = "model.layers.1"
+    w_in = 1.0 + 0.5 * rng.normal(size=S.hidden)
+    w_post = 1.0 + 0.5 * rng.normal(size=S.hidden)
+    m.W[f"{pl}.input_layernorm.weight"], m.W[f"{pl}.post_attention_layernorm.weight"] = w_in, w_post
+    pa = f"{pl}.self_attn"
+    args = [m.W[f"{pa}.{n}.weight"].tolist() for n in ("q_proj", "k_proj", "v_proj")]
+    args += [m.W[f"{pa}.q_norm.weight"].tolist(), m.W[f"{pa}.k_norm.weight"].tolist()]
+    Wo = m.W[f"{pa}.o_proj.weight"]
+
+    def rms(vec, w):
+        ms = sum(t * t for t in vec) / len(vec)
+        return [t / math.sqrt(ms + R.EPS) * wi for t, wi in zip(vec, w)]
+
+    cache, past = m.new_cache(), []
+    for chunk in ([0, 1, 2], [3]):                         # prefill, then one cached decode step
+        x = rng.normal(size=(len(chunk), S.hidden))
+        got = m.transformer_block(x, 1, cache, chunk)
+        h = [rms(list(row), w_in) for row in x]
+        att = _brute_attention(h, *args, chunk, past, S.n_heads, S.n_kv_heads, S.head_dim)
+        for t in range(len(chunk)):
+            x1 = [x[t][o] + sum(Wo[o][c] * att[t][c] for c in range(S.n_heads * S.head_dim))
+                  for o in range(S.hidden)]
+            f = _scalar_ffn(m.W, f"{pl}.mlp", rms(x1, w_post), S)
+            expect = [x1[o] + f[o] for o in range(S.hidden)]
+            np.testing.assert_allclose(got[t], expect, rtol=1e-10, atol=1e-12)
+
+
+def test_generate_positions_and_per_step_counter(tiny_shape):
+    """Step 9: the token chosen at step i - 1 is decoded at position T + i - 1, so every logits
+    row equals the last row of a fresh full recompute over prompt + chosen ids; step i draws
+    its uniform with rng_counter = i."""
+    _, m = _tiny_model(tiny_shape)
+    prompt = [3, 77, 200, 5]
+    T = len(prompt)
+    for temp, top_k, top_p in ((0.0, 0, 1.0), (1.3, 0, 0.9), (0.8, 5, 1.0)):
+        chosen, rows = R.generate(m, prompt, 5, temperature=temp, top_k=top_k, top_p=top_p, seed=9)
+        assert len(chosen) == len(rows) == 5
+        for i in range(5):
+            seq = prompt + chosen[:i]
+            ref = m.forward(seq, np.arange(T + i), m.new_cache())[-1]
+            np.testing.assert_allclose(rows[i], ref, rtol=1e-10, atol=1e-12)
+            assert chosen[i] == R.sample(ref, temp, top_k, top_p, R.sampling_uniform(9, i))
+    # a wrong position is visible in the logits: decoding the same token one position later differs
+    cache = m.new_cache()
+    m.forward(prompt, np.arange(T), cache)
+    a = m.forward([chosen[0]], [T], [c for c in cache])[-1]
+    cache2 = m.new_cache()
+    m.forward(prompt, np.arange(T), cache2)
+    b = m.forward([chosen[0]], [T + 1], cache2)[-1]
+    assert np.abs(a - b).max() > 1e-6
+    # teacher forcing feeds forced[i - 1] at step i
+    forced = [9, 8, 7, 6]
+    _, rows_f = R.generate(m, prompt, 5, forced=forced)
+    np.testing.assert_allclose(rows_f[4], m.forward(prompt + forced, np.arange(T + 4), m.new_cache())[-1],
+                               rtol=1e-10, atol=1e-12)
+
+
 # ------------------------------------------------------------------ sampling (Step 8)
 def test_sample_greedy_and_top1():
     rng = np.random.default_rng(10)

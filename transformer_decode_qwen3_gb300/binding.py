@@ -24,11 +24,12 @@ QW_PAGE_SIZE = 16
 QW_HEAD_DIM = 128
 QW_MAX_TOP_K = 1024
 QW_TRACE_SLOTS = 24
+PROF_CLASSES = ("gemm", "attn", "other", "lm_head", "sample", "fused")
 
 EXPORTED = ["qw_config_default", "qw_init", "qw_destroy", "qw_kv_create", "qw_kv_destroy", "qw_kv_layout",
             "qw_prefill", "qw_decode_step", "qw_sample", "qw_check", "qw_last_error_message",
             "qw_debug_hidden", "qw_set_decode_path", "qw_debug_gemm", "qw_kernel_launches", "qw_attn_decode", "qw_attn_decode_noalloc", "qw_debug_trace",
-            "qw_set_prefill_attention", "qw_generate"]
+            "qw_set_prefill_attention", "qw_generate", "qw_debug_profile"]
 
 
 class QwConfig(ctypes.Structure):
@@ -95,6 +96,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qw_attn_decode_noalloc.argtypes = [vp, vp, i32, i32, i32, vp, i32, vp, i32, vp, vp]
     lib.qw_debug_trace.argtypes = [vp, i32, vp, i64, ctypes.POINTER(i64)]
     lib.qw_set_prefill_attention.argtypes = [vp, i32]
+    lib.qw_debug_profile.argtypes = [vp, i32, vp, vp]
     lib.qw_kernel_launches.argtypes = []
     lib.qw_kernel_launches.restype = ctypes.c_uint64
     for name in EXPORTED:
@@ -234,6 +236,16 @@ class Model:
                "qw_debug_trace")
         return out.view(-1, self.shape.n_layers + 1, QW_TRACE_SLOTS)
 
+    def profile(self, enable: bool, fetch: bool = False):
+        """Per-kernel-class device time (qw_debug_profile): with fetch, a dict class -> (ms, launches)
+        over the launches recorded since profiling was last enabled."""
+        n = len(PROF_CLASSES)
+        ms = (ctypes.c_double * n)()
+        cnt = (ctypes.c_int64 * n)()
+        _check(_lib.qw_debug_profile(self.handle, int(enable), ctypes.addressof(ms) if fetch else None,
+                                     ctypes.addressof(cnt) if fetch else None), "qw_debug_profile")
+        return {k: (ms[i], cnt[i]) for i, k in enumerate(PROF_CLASSES)} if fetch else None
+
     def check(self, stream=None):
         _check(_lib.qw_check(self.handle, _stream(stream)), "qw_check")
 
@@ -313,20 +325,6 @@ def debug_gemm(A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, epi: int = 0, 
     N = B.shape[0]
     _check(lib.qw_debug_gemm(_ptr(A), _ptr(B), _ptr(C), M, N, K, epi, bn, int(split), _stream(stream)),
            "qw_debug_gemm")
-
-
-def split_rows(a: torch.Tensor) -> torch.Tensor:
-    """The hi/lo bf16 layout of float rows a[M][K] that split-mode projections read."""
-    M, K = a.shape
-    tiles = (M + 63) // 64
-    out = torch.zeros(tiles * 128, K, dtype=torch.bfloat16, device=a.device)
-    hi = a.to(torch.bfloat16)
-    lo = (a - hi.float()).to(torch.bfloat16)
-    idx = torch.arange(M, device=a.device)
-    dst = (idx // 64) * 128 + idx % 64
-    out[dst] = hi
-    out[dst + 64] = lo
-    return out
 
 
 def sample_params(rows: list[tuple[float, int, float, int]], device="cuda") -> torch.Tensor:

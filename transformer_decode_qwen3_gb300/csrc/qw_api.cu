@@ -49,6 +49,15 @@ struct LayerW {
     CUtensorMap tm_qkv128, tm_gu128;  // q|k|v and gate/up with 128-row boxes (CTA-pair halves)
 };
 
+// Per-kernel-class device time (qw_debug_profile): CUDA events recorded on the launching
+// stream around each launch of a class while enabled.
+struct Profiler {
+    bool on = false;
+    std::vector<cudaEvent_t> ev;       // pairs (start, end); reused across enables
+    std::vector<int> cls;              // class of pair i
+    size_t used = 0;                   // pairs recorded since the last enable
+};
+
 struct qw_ctx {
     qw_config cfg;
     int dev = 0, n_sm = 0;
@@ -73,7 +82,38 @@ struct qw_ctx {
     int prefill_attn = 0;   // 0: tcgen05 kernel, 1: mma.sync kernel
     FusedDecode* fused = nullptr;
     bool last_fused = false;   // the last decode step ran the fused kernel (its argmax is valid)
+    Profiler prof;
 };
+
+// Records the start of a launch of class `cls` on construction and its end on destruction
+// (nothing unless profiling is on).
+struct ProfScope {
+    qw_ctx* c;
+    int idx = -1;
+    cudaStream_t st;
+    ProfScope(qw_ctx* ctx, int cls, cudaStream_t s) : c(ctx), st(s) {
+        Profiler& p = c->prof;
+        if (!p.on) return;
+        if (p.used * 2 + 2 > p.ev.size()) {
+            cudaEvent_t a, b;
+            if (cudaEventCreate(&a) != cudaSuccess) return;
+            if (cudaEventCreate(&b) != cudaSuccess) {
+                cudaEventDestroy(a);
+                return;
+            }
+            p.ev.push_back(a);
+            p.ev.push_back(b);
+            p.cls.push_back(cls);
+        }
+        idx = (int)p.used++;
+        p.cls[idx] = cls;
+        cudaEventRecord(p.ev[2 * idx], st);
+    }
+    ~ProfScope() {
+        if (idx >= 0) cudaEventRecord(c->prof.ev[2 * idx + 1], st);
+    }
+};
+#define QW_PROF(cls) ProfScope prof_scope_(ctx, cls, st)
 
 struct qw_kv {
     qw_ctx* ctx;
@@ -137,6 +177,7 @@ static int upload_norm(float* dst, const uint16_t* src, int n, int on_device) {
 
 static void free_ctx(qw_ctx* c) {
     if (!c) return;
+    for (cudaEvent_t e : c->prof.ev) cudaEventDestroy(e);
     if (c->fused) fused_destroy(c->fused);
     if (c->wbuf) cudaFree(c->wbuf);
     if (c->wsbuf) cudaFree(c->wsbuf);
@@ -391,70 +432,70 @@ static int run_layers(qw_ctx* ctx, int n, const int* ids, const int* positions, 
     const qw_config& c = ctx->cfg;
     const int D = c.hidden, Hq = c.n_heads, Hkv = c.n_kv_heads, I = c.intermediate;
     const int split = n <= SPLIT_MAX_M;   // small-M projections take hi/lo activation pairs
-    QW_TRY(launch_embed(ids, n, ctx->E, c.vocab, D, ctx->x, ctx->err, st), "embed launch");
+    { QW_PROF(QW_PROF_OTHER); QW_TRY(launch_embed(ids, n, ctx->E, c.vocab, D, ctx->x, ctx->err, st), "embed launch"); }
     const bool fused_qkv = mode == 0 && ctx->prefill_attn == 0 && !split;  // q|k|v GEMM epilogue does Steps 4-5
-    if (fused_qkv) QW_TRY(launch_rope_table(positions, n, ctx->inv_freq, ctx->rope_tab, st), "rope table launch");
+    if (fused_qkv) { QW_PROF(QW_PROF_OTHER); QW_TRY(launch_rope_table(positions, n, ctx->inv_freq, ctx->rope_tab, st), "rope table launch"); }
     for (int l = 0; l < c.n_layers; ++l) {
         const LayerW& Lw = ctx->L[l];
         KvView kvv{kv->base + (int64_t)l * kv->layer_elems, kv->page_elems, kv->n_pages, bt, bt_stride};
-        QW_TRY(launch_rmsnorm_bf16(ctx->x, nullptr, n, D, Lw.in_norm, c.rms_eps, ctx->h, split, st),
-               "rmsnorm launch");
+        { QW_PROF(QW_PROF_OTHER); QW_TRY(launch_rmsnorm_bf16(ctx->x, nullptr, n, D, Lw.in_norm, c.rms_eps, ctx->h, split, st),
+               "rmsnorm launch"); }
         const bool tc_attn = mode == 0 && ctx->prefill_attn == 0;
         GemmEpilogue e{ctx->qkv, nullptr, ctx->qkv_dim, ctx->err, split};
         if (fused_qkv) {
             // prefill: QK-Norm, RoPE, bf16 q and the cache write happen in the GEMM epilogue
             e.rope = QkvRope{positions, tok_seq, kvv, Lw.q_norm, Lw.k_norm, ctx->rope_tab, c.rms_eps, ctx->q_bf16,
                              Hq, Hkv};
-            QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_qkv, 256, n, ctx->qkv_dim, D, EPI_QKV_ROPE, e, st, &Lw.tm_qkv128),
-                   "qkv gemm");
+            { QW_PROF(QW_PROF_GEMM); QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_qkv, 256, n, ctx->qkv_dim, D, EPI_QKV_ROPE, e, st, &Lw.tm_qkv128),
+                   "qkv gemm"); }
         } else {
             // small M: 128-wide tiles (32 CTAs stream the weight for a 4096-wide q|k|v), measured
             // faster than split-K with atomic accumulation into a zeroed target
-            QW_TRY(gemm_bf16(ctx->h, D, split ? Lw.tm_qkv128 : Lw.tm_qkv, split ? 128 : 256, n, ctx->qkv_dim, D,
+            { QW_PROF(QW_PROF_GEMM); QW_TRY(gemm_bf16(ctx->h, D, split ? Lw.tm_qkv128 : Lw.tm_qkv, split ? 128 : 256, n, ctx->qkv_dim, D,
                              EPI_STORE_F32, e, st),
-                   "qkv gemm");
-            QW_TRY(launch_qkv_post(ctx->qkv, n, positions, tok_seq, Hq, Hkv, Lw.q_norm, Lw.k_norm, ctx->inv_freq,
+                   "qkv gemm"); }
+            { QW_PROF(QW_PROF_OTHER); QW_TRY(launch_qkv_post(ctx->qkv, n, positions, tok_seq, Hq, Hkv, Lw.q_norm, Lw.k_norm, ctx->inv_freq,
                                    c.rms_eps, tc_attn ? nullptr : ctx->q, tc_attn ? ctx->q_bf16 : nullptr, kvv,
                                    ctx->err, st),
-                   "qk-norm/rope/kv-write launch");
+                   "qk-norm/rope/kv-write launch"); }
         }
         if (tc_attn)
-            QW_TRY(launch_attn_prefill_tc(ctx->q_bf16, n, positions, ctx->tiles, n_tiles, Hq, Hkv, kvv, ctx->attn,
+            { QW_PROF(QW_PROF_ATTN); QW_TRY(launch_attn_prefill_tc(ctx->q_bf16, n, positions, ctx->tiles, n_tiles, Hq, Hkv, kvv, ctx->attn,
                                           split, ctx->err, st),
-                   "prefill attention launch");
+                   "prefill attention launch"); }
         else if (mode == 0)
-            QW_TRY(launch_attn_prefill(ctx->q, positions, ctx->tiles, n_tiles, Hq, Hkv, kvv, ctx->attn, split,
+            { QW_PROF(QW_PROF_ATTN); QW_TRY(launch_attn_prefill(ctx->q, positions, ctx->tiles, n_tiles, Hq, Hkv, kvv, ctx->attn, split,
                                        ctx->err, st),
-                   "prefill attention launch");
+                   "prefill attention launch"); }
         else
-            QW_TRY(launch_attn_decode(ctx->q, positions, n, Hq, Hkv, kvv, ctx->part, ctx->max_splits, ctx->attn,
+            { QW_PROF(QW_PROF_ATTN); QW_TRY(launch_attn_decode(ctx->q, positions, n, Hq, Hkv, kvv, ctx->part, ctx->max_splits, ctx->attn,
                                       split, ctx->err, ctx->n_sm, st),
-                   "decode attention launch");
+                   "decode attention launch"); }
         e = GemmEpilogue{ctx->x, nullptr, D, ctx->err, split};
         // N = hidden is narrow: 128-wide tiles give split-K decode batches more units,
         // 256-wide tiles halve the activation re-reads of a prefill
         if (split)
-            QW_TRY(gemm_bf16(ctx->attn, ctx->attn_dim, Lw.tm_o, 128, n, D, ctx->attn_dim, EPI_ADD_ATOMIC, e, st),
-                   "o_proj gemm");
+            { QW_PROF(QW_PROF_GEMM); QW_TRY(gemm_bf16(ctx->attn, ctx->attn_dim, Lw.tm_o, 128, n, D, ctx->attn_dim, EPI_ADD_ATOMIC, e, st),
+                   "o_proj gemm"); }
         else
-            QW_TRY(gemm_bf16(ctx->attn, ctx->attn_dim, Lw.tm_o256, 256, n, D, ctx->attn_dim, EPI_RESID_ADD, e, st,
+            { QW_PROF(QW_PROF_GEMM); QW_TRY(gemm_bf16(ctx->attn, ctx->attn_dim, Lw.tm_o256, 256, n, D, ctx->attn_dim, EPI_RESID_ADD, e, st,
                              &Lw.tm_o),
-                   "o_proj gemm");
-        QW_TRY(launch_rmsnorm_bf16(ctx->x, nullptr, n, D, Lw.post_norm, c.rms_eps, ctx->h, split, st),
-               "rmsnorm launch");
+                   "o_proj gemm"); }
+        { QW_PROF(QW_PROF_OTHER); QW_TRY(launch_rmsnorm_bf16(ctx->x, nullptr, n, D, Lw.post_norm, c.rms_eps, ctx->h, split, st),
+               "rmsnorm launch"); }
         if (split) {
             // small M: 128-wide tiles with the SwiGLU epilogue writing the hi/lo activation pairs
             e = GemmEpilogue{nullptr, ctx->act, I, ctx->err, split};
-            QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_gu128, 128, n, 2 * I, D, EPI_SWIGLU, e, st), "gate/up gemm");
+            { QW_PROF(QW_PROF_GEMM); QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_gu128, 128, n, 2 * I, D, EPI_SWIGLU, e, st), "gate/up gemm"); }
         } else {
             e = GemmEpilogue{nullptr, ctx->act, I, ctx->err, split};
-            QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_gu, 256, n, 2 * I, D, EPI_SWIGLU, e, st, &Lw.tm_gu128), "gate/up gemm");
+            { QW_PROF(QW_PROF_GEMM); QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_gu, 256, n, 2 * I, D, EPI_SWIGLU, e, st, &Lw.tm_gu128), "gate/up gemm"); }
         }
         e = GemmEpilogue{ctx->x, nullptr, D, ctx->err, split};
         if (split)
-            QW_TRY(gemm_bf16(ctx->act, I, Lw.tm_d, 128, n, D, I, EPI_ADD_ATOMIC, e, st), "down gemm");
+            { QW_PROF(QW_PROF_GEMM); QW_TRY(gemm_bf16(ctx->act, I, Lw.tm_d, 128, n, D, I, EPI_ADD_ATOMIC, e, st), "down gemm"); }
         else
-            QW_TRY(gemm_bf16(ctx->act, I, Lw.tm_d256, 256, n, D, I, EPI_RESID_ADD, e, st, &Lw.tm_d), "down gemm");
+            { QW_PROF(QW_PROF_GEMM); QW_TRY(gemm_bf16(ctx->act, I, Lw.tm_d256, 256, n, D, I, EPI_RESID_ADD, e, st, &Lw.tm_d), "down gemm"); }
         if (ctx->hidden)
             QW_CUDA(cudaMemcpyAsync(ctx->hidden + (size_t)l * ctx->max_rows * D, ctx->x, (size_t)n * D * 4,
                                     cudaMemcpyDeviceToDevice, st));
@@ -466,9 +507,9 @@ static int run_layers(qw_ctx* ctx, int n, const int* ids, const int* positions, 
 static int lm_head(qw_ctx* ctx, const int* rows, int n, float* out, cudaStream_t st) {
     const qw_config& c = ctx->cfg;
     const int split = n <= SPLIT_MAX_M;
-    QW_TRY(launch_rmsnorm_bf16(ctx->x, rows, n, c.hidden, ctx->final_norm, c.rms_eps, ctx->h, split, st), "final norm");
+    { QW_PROF(QW_PROF_LMHEAD); QW_TRY(launch_rmsnorm_bf16(ctx->x, rows, n, c.hidden, ctx->final_norm, c.rms_eps, ctx->h, split, st), "final norm"); }
     GemmEpilogue e{out, nullptr, c.vocab, ctx->err, split};
-    QW_TRY(gemm_bf16(ctx->h, c.hidden, ctx->tm_E, 256, n, c.vocab, c.hidden, EPI_STORE_F32, e, st), "lm head gemm");
+    { QW_PROF(QW_PROF_LMHEAD); QW_TRY(gemm_bf16(ctx->h, c.hidden, ctx->tm_E, 256, n, c.vocab, c.hidden, EPI_STORE_F32, e, st), "lm head gemm"); }
     return QW_OK;
 }
 
@@ -526,6 +567,7 @@ int qw_decode_step(qw_ctx* ctx, const int32_t* tokens, const int32_t* positions,
     int rc;
     ctx->last_fused = fused;
     if (fused) {
+        QW_PROF(QW_PROF_FUSED);
         rc = fused_decode(ctx->fused, tokens, positions, batch, kv->base, kv->layer_elems, kv->page_elems,
                           kv->n_pages, bt, bt_stride, out, ctx->err, st);
         if (rc) return fail(rc, "fused decode launch failed");
@@ -548,6 +590,8 @@ int qw_sample(qw_ctx* ctx, const float* logits, int32_t batch, const qw_sample_p
         logits = ctx->logits;
     }
     const int* hint = (logits == ctx->logits && ctx->last_fused && batch == 1) ? fused_argmax(ctx->fused) : nullptr;
+    cudaStream_t st = (cudaStream_t)stream;
+    QW_PROF(QW_PROF_SAMPLE);
     QW_TRY(launch_sample(logits, batch, ctx->cfg.vocab, params, rng_counter, out_ids, hint, ctx->err,
                          (cudaStream_t)stream),
            "sample launch");
@@ -637,6 +681,27 @@ int qw_debug_trace(qw_ctx* ctx, int32_t enable, uint64_t* host_out, int64_t n, i
     if (!ctx) return fail(QW_EINVAL, "null context");
     if (!ctx->fused) return fail(QW_EINVAL, "no fused decode kernel in this context");
     QW_TRY(fused_trace(ctx->fused, enable, host_out, n, n_needed), "trace copy failed");
+    return QW_OK;
+}
+
+int qw_debug_profile(qw_ctx* ctx, int32_t enable, double* ms_out, int64_t* count_out) {
+    if (!ctx) return fail(QW_EINVAL, "null context");
+    Profiler& p = ctx->prof;
+    if (ms_out || count_out) {
+        QW_CUDA(cudaDeviceSynchronize());
+        for (int k = 0; k < QW_PROF_CLASSES; ++k) {
+            if (ms_out) ms_out[k] = 0.0;
+            if (count_out) count_out[k] = 0;
+        }
+        for (size_t i = 0; i < p.used; ++i) {
+            float ms = 0.f;
+            QW_CUDA(cudaEventElapsedTime(&ms, p.ev[2 * i], p.ev[2 * i + 1]));
+            if (ms_out) ms_out[p.cls[i]] += ms;
+            if (count_out) count_out[p.cls[i]] += 1;
+        }
+    }
+    if (enable) p.used = 0;
+    p.on = enable != 0;
     return QW_OK;
 }
 

@@ -31,6 +31,7 @@
 
 #include <string.h>
 
+#include <mutex>
 #include <vector>
 
 #include "qw_common.cuh"
@@ -524,30 +525,40 @@ static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N,
     }
     using C = GemmCfg<BN>;
     auto kern = gemm_bf16_tc_kernel<BN, EPI, SPLIT, MC>;
-    static bool attr_set = false;
-    static int n_sm = 0, max_clusters = 0;
-    if (!attr_set) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
-            return QW_ECUDA;
-        if (MC) {
-            cudaLaunchConfig_t cfg = {};
-            cudaLaunchAttribute at[1];
-            at[0].id = cudaLaunchAttributeClusterDimension;
-            at[0].val.clusterDim.x = 2;
-            at[0].val.clusterDim.y = 1;
-            at[0].val.clusterDim.z = 1;
-            cfg.gridDim = dim3(2 * (n_sm / 2));
-            cfg.blockDim = dim3(C::THREADS);
-            cfg.dynamicSmemBytes = C::SMEM;
-            cfg.attrs = at;
-            cfg.numAttrs = 1;
-            if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess || max_clusters < 1)
+    // per device (function attributes and occupancy belong to the device), set up once under a lock
+    constexpr int kMaxDevices = 64;
+    static std::mutex mu;
+    static bool attr_set[kMaxDevices] = {};
+    static int n_sm_dev[kMaxDevices] = {}, max_clusters_dev[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QW_ECUDA;
+    int n_sm = 0, max_clusters = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!attr_set[dev]) {
+            cudaDeviceGetAttribute(&n_sm_dev[dev], cudaDevAttrMultiProcessorCount, dev);
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
                 return QW_ECUDA;
+            if (MC) {
+                cudaLaunchConfig_t cfg = {};
+                cudaLaunchAttribute at[1];
+                at[0].id = cudaLaunchAttributeClusterDimension;
+                at[0].val.clusterDim.x = 2;
+                at[0].val.clusterDim.y = 1;
+                at[0].val.clusterDim.z = 1;
+                cfg.gridDim = dim3(2 * (n_sm_dev[dev] / 2));
+                cfg.blockDim = dim3(C::THREADS);
+                cfg.dynamicSmemBytes = C::SMEM;
+                cfg.attrs = at;
+                cfg.numAttrs = 1;
+                if (cudaOccupancyMaxActiveClusters(&max_clusters_dev[dev], kern, &cfg) != cudaSuccess ||
+                    max_clusters_dev[dev] < 1)
+                    return QW_ECUDA;
+            }
+            attr_set[dev] = true;
         }
-        attr_set = true;
+        n_sm = n_sm_dev[dev];
+        max_clusters = max_clusters_dev[dev];
     }
     const int tiles_m = SPLIT ? (M + 63) / 64 : (M + C::BM - 1) / C::BM;
     const int tiles_n = (N + BN - 1) / BN;

@@ -3,8 +3,6 @@
 // Same kernels as qw_attn_decode; the only difference is where the split
 // partials live: a fixed array in this library's device image instead of a
 // context workspace, so the call needs no context and performs no allocation.
-#include <mutex>
-
 #include "qw_common.cuh"
 #include "qw_internal.h"
 
@@ -13,22 +11,15 @@
 static __device__ __align__(256) float g_attn_scratch[QW_NOALLOC_SCRATCH_FLOATS];
 
 namespace {
-constexpr int kMaxDevices = 256;
-std::mutex g_mu;
-float* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of g_attn_scratch on the current device, looked up once per device.
-// In host code the array's name is only a stand-in: kernels must get this address.
+// Device address of g_attn_scratch in the current device's current context.  In host code
+// the array's name is only a stand-in: kernels must get this address.  It is looked up on
+// every call rather than cached, because it belongs to a context: after cudaDeviceReset, or
+// with another context current on the same device, a cached address would be stale.  The
+// lookup allocates nothing.
 int scratch_on_current_device(float** out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QW_ECUDA;
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || !p) return QW_ECUDA;
-        g_scratch_ptr[dev] = (float*)p;
-    }
-    *out = g_scratch_ptr[dev];
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || !p) return QW_ECUDA;
+    *out = (float*)p;
     return QW_OK;
 }
 }  // namespace
