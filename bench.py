@@ -21,8 +21,8 @@ The library is single-GPU: it runs on the current CUDA device only and this
 script measures one GPU.  Asked for more (--gpus N > 1, or a torchrun launch
 with WORLD_SIZE > 1), rank 0 prints one line saying so and nothing runs.
 
---impl reference times the CPU oracle on the host cores on the same workload,
-metric and config.
+--impl reference times the plain single-precision C oracle (OpenMP over the host
+cores) on a bounded sample of the same workload, with the same metric and config.
 """
 from __future__ import annotations
 
@@ -398,17 +398,18 @@ class Prefill:
 
 # ------------------------------------------------------------------ CPU oracle
 def oracle_rate(workload: str, max_seconds=15.0):
-    """The oracle, unmodified, on a bounded sample of the workload; (units/s, sample text, threads)."""
+    """The C oracle (plain single precision, OpenMP over the host cores), unmodified, on a bounded
+    sample of the workload; (units/s, sample text, threads)."""
     import numpy as np
-    from oracle import qwen3_ref as R
+    from oracle import qwen3_c as C
     w = synth.make_weights(S)
-    orc = R.Qwen3Oracle(w, S)
-    threads = os.cpu_count()
+    orc = C.COracle(w, S)
+    threads = C.threads()
     if workload == "prefill":
-        T = 256                         # a 256-token prefix of sequence 0
+        T = 128                         # a 128-token prefix of sequence 0
         ids = synth.token_ids(0, 2, T, S.vocab).numpy()
         t0 = time.perf_counter()
-        orc.forward(ids, np.arange(T), orc.new_cache(), last_only=True)
+        orc.forward(ids, np.arange(T), orc.new_cache(T), last_only=True)
         dt = time.perf_counter() - t0
         return T / dt, f"prefill of the first {T} tokens of one 2048-token sequence ({dt:.1f} s)", threads
     if workload in ("decode_bs64", "decode_bs16_32k"):
@@ -422,32 +423,34 @@ def oracle_rate(workload: str, max_seconds=15.0):
         per_tok = S.n_kv_heads * 128
         elapsed, n = 0.0, 0
         while n < 1 or (elapsed < max_seconds and n < len(lens)):
-            cache = [None] * S.n_layers
+            L = lens[n]
+            cache = orc.new_cache(L + 1)
             for layer in range(S.n_layers):        # cache set-up, not timed
-                k = synth.kv_values(0, layer, 0, n * (1 << 15) * per_tok, lens[n] * per_tok, 1.0)
-                v = synth.kv_values(0, layer, 1, n * (1 << 15) * per_tok, lens[n] * per_tok, 0.64)
-                cache[layer] = R.LayerCache(R.bf16_to_f64(k).reshape(lens[n], 8, 128).transpose(1, 0, 2),
-                                            R.bf16_to_f64(v).reshape(lens[n], 8, 128).transpose(1, 0, 2),
-                                            np.arange(lens[n]))
+                k = synth.kv_values(0, layer, 0, n * (1 << 15) * per_tok, L * per_tok, 1.0)
+                v = synth.kv_values(0, layer, 1, n * (1 << 15) * per_tok, L * per_tok, 0.64)
+                cache.fill_prefix(layer, synth.bf16_to_f32(k).numpy().reshape(L, 8, 128),
+                                  synth.bf16_to_f32(v).numpy().reshape(L, 8, 128))
+            cache.set_len(L)
             t0 = time.perf_counter()
-            logits = orc.forward([int(toks[n])], [lens[n]], cache, last_only=True)
-            R.sample(logits[0], *params, R.sampling_uniform(n, 0))
+            logits = orc.forward([int(toks[n])], [L], cache, last_only=True)
+            C.sample_detail(logits[0], *params, C.sampling_uniform(n, 0))
             elapsed += time.perf_counter() - t0
             n += 1
+            del cache
         return n / elapsed, (f"{n} of the {len(lens)} sequences, one decode step each ({elapsed:.1f} s timed; "
                              f"cache set-up untimed)"), threads
     ids = synth.token_ids(0, 1, PROMPT, S.vocab).numpy()
-    cache = orc.new_cache()
+    cache = orc.new_cache(PROMPT + 4096)
     logits = orc.forward(ids, np.arange(PROMPT), cache, last_only=True)
     tok = int(np.argmax(logits[0]))
     t0 = time.perf_counter()
     n = 0
-    while n < 2 or time.perf_counter() - t0 < max_seconds:
+    while n < 2 or (time.perf_counter() - t0 < max_seconds and n < 4096):
         logits = orc.forward([tok], [PROMPT + n], cache, last_only=True)
         tok = int(np.argmax(logits[0]))
         n += 1
     dt = time.perf_counter() - t0
-    return n / dt, f"{n} batch-1 decode steps after the 512-token prompt ({dt:.1f} s; prefill untimed)", threads
+    return n / dt, f"{n} batch-1 greedy decode steps after the 512-token prompt ({dt:.1f} s; prefill untimed)", threads
 
 
 def run_reference(args):
@@ -455,7 +458,7 @@ def run_reference(args):
     unit = "tok/s"
     line = {"metric": METRICS[args.workload], "value": v, "unit": unit, "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded random-init weights and token ids)",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded random-init weights and token ids)",
             "impl": "reference", "config": config_of(args.workload, args.steps),
             "cpu_baseline": {"value": v, "unit": unit, "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}

@@ -47,7 +47,6 @@ extern "C" {
 
 #define QW_PAGE_SIZE 16   /* tokens per KV page */
 #define QW_HEAD_DIM 128   /* the only head size the kernels implement */
-#define QW_MAX_TOP_K 1024 /* largest top_k qw_sample accepts */
 #define QW_NOALLOC_SCRATCH_FLOATS (1 << 20) /* fixed scratch of qw_attn_decode_noalloc: 4 MiB */
 #define QW_TRACE_SLOTS 24  /* timestamps per CTA and layer in qw_debug_trace */
 
@@ -107,7 +106,7 @@ typedef struct qw_weights {
 /* Per-row sampling parameters (Step 8 sample(), plus a top-k cap). */
 typedef struct qw_sample_params {
     float temperature;  /* 0: greedy argmax (lowest id wins a tie); > 0: sample */
-    int32_t top_k;      /* 1 .. QW_MAX_TOP_K: at most this many candidates (used when temperature > 0) */
+    int32_t top_k;      /* >= 0: at most this many candidates; 0 (or >= vocab): no cap (used when temperature > 0) */
     float top_p;        /* (0, 1]: keep the smallest prefix of the sorted distribution whose mass reaches top_p */
     uint32_t reserved;  /* set to 0 */
     uint64_t seed;      /* Philox4x32-10 key of this row (e.g. the sequence id) */
@@ -161,16 +160,22 @@ int qw_decode_step(qw_ctx* ctx, const int32_t* tokens, const int32_t* positions,
 
 /* Sample one id per row (Step 8 sample()).
  *   logits   DEVICE float[batch][vocab], or NULL for the context's logits from the last
- *            qw_decode_step / qw_prefill call that returned them in the context.
+ *            qw_decode_step / qw_prefill call that returned them in the context (those
+ *            come with per-tile maxima from the LM head, so greedy rows read no logits).
  *   params   DEVICE qw_sample_params[batch].
  *   rng_counter  Philox counter of this step: row b draws u from Philox4x32-10 with
  *            key = params[b].seed and counter = (rng_counter, 0, 0) as four 32-bit
  *            words (low word first); u = (word0 >> 8) * 2^-24.
  *   out_ids  DEVICE int32[batch].
- * Greedy rows take the argmax.  Sampling rows take softmax(logits / temperature) over
- * the whole vocabulary, sort it descending (ties: lower id first), keep
- * cutoff = min(top_k, 1 + #(cumsum < top_p)) entries, and return the first kept
- * entry whose cumulative kept mass exceeds u * (kept mass). */
+ * Greedy rows take the argmax (lowest id on ties).  Sampling rows take softmax(logits /
+ * temperature) over the whole vocabulary, in the order probability descending, id
+ * ascending; keep cutoff = 1 + #(cumsum < top_p) entries, capped at top_k when top_k > 0;
+ * and return the first kept entry whose cumulative kept mass exceeds u * (kept mass).  Any
+ * nucleus size is supported (top_k = 0 with top_p < 1 is the article's sample()).  The
+ * cuts are found without sorting (radix searches over the logits by count and by mass), so
+ * a draw whose cumulative sum lies within fp32 rounding of a cut may differ from an exact
+ * sorted evaluation.  Invalid parameters (top_k < 0, top_p outside (0, 1]) record QW_EINVAL
+ * for qw_check and are clamped. */
 int qw_sample(qw_ctx* ctx, const float* logits, int32_t batch, const qw_sample_params* params,
               uint64_t rng_counter, int32_t* out_ids, void* stream);
 
@@ -264,14 +269,15 @@ int qw_debug_gemm(const uint16_t* A, const uint16_t* B, void* C, int32_t M, int3
 /* Tracing hook of the fused batch-1 decode kernel.  enable = 1: the following fused
  * steps record %globaltimer stamps (ns) at every phase boundary; enable = 0: stop.
  * host_out (nullable, HOST uint64[n]): receives the stamps of the last traced step,
- * [CTA][layer 0..n_layers][QW_TRACE_SLOTS] (slot 0/1: before/after the wait for the layer
- * input, 2: q|k|v published, 3: attention input ready, 4: attention split published,
- * 5: attention merged, 6: o_proj published, 7: MLP input ready, 8: layer published,
- * 9: the producer has issued the layer's weights, 10/12: normalised input ready for
- * q|k|v / gate-up, 11/13: their dot products done, 14: down_proj rows done, 15: o_proj
- * rows start, 16/17: first weight stage of q|k|v / gate-up arrived, 18/19: attention
- * keys start / done, 20/21: first key stage arrived / its scores published, 22/23: SM
- * clock64 at 20/21 (cycles, not ns); layer n_layers: LM head wait begin/end and done).  *n_needed receives the buffer length.  Synchronous. */
+ * [CTA][layer 0..n_layers][QW_TRACE_SLOTS]: slot 0/1: before/after the wait for the layer
+ * input; attention CTAs: 2 q|k|v rows done, 3 q|k|v exchange complete, 4 keys done,
+ * 5 attention partials exchanged, 6 o_proj rows done, 7 o_proj reduced in the cluster,
+ * 8 group slot published; every CTA: 9/10 before/after the wait for the attention output,
+ * 11 gate/up rows done, 12 down_proj rows done, 13 reduced in the cluster, 14 cluster slot
+ * published, 15 the producer has issued the layer's weights, 17 feed-forward input normalised,
+ * 18 (attention CTAs) queries and the new key/value ready; layer n_layers: LM head wait
+ * begin/end (0/1) and rows done (2); unused slots hold 0.  *n_needed receives the buffer
+ * length.  Synchronous. */
 int qw_debug_trace(qw_ctx* ctx, int32_t enable, uint64_t* host_out, int64_t n, int64_t* n_needed);
 
 /* Device time per kernel class, for measurement.  enable = 1: from now on record a CUDA
@@ -281,6 +287,13 @@ int qw_debug_trace(qw_ctx* ctx, int32_t enable, uint64_t* host_out, int64_t n, i
  * synchronisation, the summed milliseconds and the number of launches of each class
  * (QW_PROF_*) recorded since the last enable.  Not for use inside stream capture. */
 int qw_debug_profile(qw_ctx* ctx, int32_t enable, double* ms_out, int64_t* count_out);
+
+/* Failure-detection test hook: the next fused batch-1 decode step waits at one grid-wide
+ * exchange for one arrival more than will ever come, with a 2 ms limit instead of the usual
+ * 2 s.  That step gives up everywhere without a device fault; qw_check then returns
+ * QW_ETIMEOUT, clears the kernel's counters, and the context keeps working.  Errors:
+ * QW_EINVAL without a fused kernel. */
+int qw_debug_inject_timeout(qw_ctx* ctx);
 
 /* Select the prefill attention kernel: 0 = tcgen05/TMEM flash kernel (default),
  * 1 = mma.sync flash kernel.  For comparisons in tests. */

@@ -139,3 +139,40 @@ def split_rows(a: torch.Tensor) -> torch.Tensor:
     out[dst] = hi
     out[dst + 64] = lo
     return out
+
+
+def sample_draw_is_valid(logits, temperature: float, top_k: int, top_p: float, u: float, got: int,
+                         eps: float = 2e-4) -> bool:
+    """Whether `got` is the inverse-CDF draw of u from Step 8's kept list up to rounding of the
+    cumulative sums: its rank in (probability desc, id asc) order lies in the top-p prefix (and
+    under top_k), and its cumulative interval, normalised by the kept mass, contains u within
+    eps.  Used where the exact comparison is exempt (large nuclei: boundaries closer than 1e-3)."""
+    z = np.asarray(logits, dtype=np.float64) / temperature
+    p = np.exp(z - z.max())
+    p /= p.sum()
+    order = np.lexsort((np.arange(p.size), -p))
+    c = np.cumsum(p[order])
+    cutoff = int(np.sum(c < top_p)) + 1
+    if top_k > 0:
+        cutoff = min(cutoff, top_k)
+    cutoff = min(cutoff, p.size)
+    kept_mass = c[cutoff - 1]
+    rank = int(np.nonzero(order == got)[0][0])
+    c_prev = c[rank - 1] if rank else 0.0
+    in_prefix = rank < cutoff or c_prev < top_p + eps
+    under_k = top_k <= 0 or rank < top_k
+    in_interval = c_prev / kept_mass <= u + eps and c[rank] / kept_mass >= u - eps
+    return in_prefix and under_k and in_interval
+
+
+def c_oracle_prefix_cache(corc, shape, seq: int, L: int, extra: int = 1):
+    """The C oracle's cache of one sequence holding the synthetic prefix (positions 0..L-1),
+    with room for `extra` more positions; values from the seeded generator (run on the GPU when
+    there is one: it is bit-identical on every device)."""
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    cache = corc.new_cache(L + extra)
+    for layer in range(shape.n_layers):
+        k, v = synth_kv(seq, layer, L, shape.n_kv_heads, device=dev)
+        cache.fill_prefix(layer, k.float().cpu().numpy(), v.float().cpu().numpy())
+    cache.set_len(L)
+    return cache

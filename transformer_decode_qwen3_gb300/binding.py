@@ -22,14 +22,13 @@ LIB_PATH = os.path.join(PKG, "libqwdecode.so")
 QW_OK, QW_EINVAL, QW_ERANGE, QW_ENOMEM, QW_EKVFULL, QW_ECUDA, QW_ETIMEOUT = 0, -1, -2, -3, -4, -5, -6
 QW_PAGE_SIZE = 16
 QW_HEAD_DIM = 128
-QW_MAX_TOP_K = 1024
 QW_TRACE_SLOTS = 24
 PROF_CLASSES = ("gemm", "attn", "other", "lm_head", "sample", "fused")
 
 EXPORTED = ["qw_config_default", "qw_init", "qw_destroy", "qw_kv_create", "qw_kv_destroy", "qw_kv_layout",
             "qw_prefill", "qw_decode_step", "qw_sample", "qw_check", "qw_last_error_message",
             "qw_debug_hidden", "qw_set_decode_path", "qw_debug_gemm", "qw_kernel_launches", "qw_attn_decode", "qw_attn_decode_noalloc", "qw_debug_trace",
-            "qw_set_prefill_attention", "qw_generate", "qw_debug_profile"]
+            "qw_set_prefill_attention", "qw_generate", "qw_debug_profile", "qw_debug_inject_timeout"]
 
 
 class QwConfig(ctypes.Structure):
@@ -97,6 +96,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qw_debug_trace.argtypes = [vp, i32, vp, i64, ctypes.POINTER(i64)]
     lib.qw_set_prefill_attention.argtypes = [vp, i32]
     lib.qw_debug_profile.argtypes = [vp, i32, vp, vp]
+    lib.qw_debug_inject_timeout.argtypes = [vp]
     lib.qw_kernel_launches.argtypes = []
     lib.qw_kernel_launches.restype = ctypes.c_uint64
     for name in EXPORTED:
@@ -245,6 +245,10 @@ class Model:
         _check(_lib.qw_debug_profile(self.handle, int(enable), ctypes.addressof(ms) if fetch else None,
                                      ctypes.addressof(cnt) if fetch else None), "qw_debug_profile")
         return {k: (ms[i], cnt[i]) for i, k in enumerate(PROF_CLASSES)} if fetch else None
+
+    def inject_timeout(self):
+        """Make the next fused decode step time out at one wait (failure-detection test hook)."""
+        _check(_lib.qw_debug_inject_timeout(self.handle), "qw_debug_inject_timeout")
 
     def check(self, stream=None):
         _check(_lib.qw_check(self.handle, _stream(stream)), "qw_check")

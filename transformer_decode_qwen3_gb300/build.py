@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libqwdecode.so")
-SOURCES = ["qw_api.cu", "qw_gemm.cu", "qw_kernels.cu", "qw_fused.cu", "qw_noalloc.cu", "qw_attn_tc.cu"]
+SOURCES = ["qw_api.cu", "qw_gemm.cu", "qw_kernels.cu", "qw_fused.cu", "qw_noalloc.cu", "qw_attn_tc.cu", "qw_sample.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
                      "-I", INCLUDE]

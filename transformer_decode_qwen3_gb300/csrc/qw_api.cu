@@ -73,6 +73,9 @@ struct qw_ctx {
     float *x = nullptr, *qkv = nullptr, *q = nullptr, *logits = nullptr, *part = nullptr, *hidden = nullptr;
     uint16_t *h = nullptr, *attn = nullptr, *act = nullptr, *q_bf16 = nullptr;
     float2* rope_tab = nullptr;   // [rows][64] RoPE (cos, sin) of the current prefill
+    float2* tile_part = nullptr;  // [max_batch][n_part] per-256-column (max, argmax) of the context's logits
+    int n_part = 0;
+    int part_rows = 0;            // rows of the context's logits that tile_part describes (0: none)
     int* gen_pos = nullptr;       // [GEN_CHUNK] positions of a qw_generate chunk
     int *tok_seq = nullptr, *iota = nullptr, *rows_last = nullptr, *err = nullptr;
     int4* tiles = nullptr;
@@ -316,6 +319,8 @@ int qw_init(const qw_config* cfg, const qw_weights* w, qw_ctx** out) {
     const size_t orope = take((size_t)T * 64 * 8);
     const size_t ogen = take((size_t)GEN_CHUNK * 4);
     const size_t ologits = take((size_t)c.max_batch * V * 4);
+    ctx->n_part = (V + 255) / 256;
+    const size_t otpart = take((size_t)c.max_batch * ctx->n_part * 8);
     const size_t opart = take((size_t)c.max_batch * Hq * ctx->max_splits * (d + 2) * 4);
     const size_t oh = take((size_t)TA * D * 2);
     const size_t oattn = take((size_t)TA * ctx->attn_dim * 2);
@@ -338,6 +343,7 @@ int qw_init(const qw_config* cfg, const qw_weights* w, qw_ctx** out) {
     ctx->rope_tab = (float2*)(W + orope);
     ctx->gen_pos = (int*)(W + ogen);
     ctx->logits = (float*)(W + ologits);
+    ctx->tile_part = (float2*)(W + otpart);
     ctx->part = (float*)(W + opart);
     ctx->h = (uint16_t*)(W + oh);
     ctx->attn = (uint16_t*)(W + oattn);
@@ -509,7 +515,12 @@ static int lm_head(qw_ctx* ctx, const int* rows, int n, float* out, cudaStream_t
     const int split = n <= SPLIT_MAX_M;
     { QW_PROF(QW_PROF_LMHEAD); QW_TRY(launch_rmsnorm_bf16(ctx->x, rows, n, c.hidden, ctx->final_norm, c.rms_eps, ctx->h, split, st), "final norm"); }
     GemmEpilogue e{out, nullptr, c.vocab, ctx->err, split};
+    if (out == ctx->logits && n <= c.max_batch) {   // the sampler's argmax and max start from these
+        e.tile_max = ctx->tile_part;
+        e.tile_ld = ctx->n_part;
+    }
     { QW_PROF(QW_PROF_LMHEAD); QW_TRY(gemm_bf16(ctx->h, c.hidden, ctx->tm_E, 256, n, c.vocab, c.hidden, EPI_STORE_F32, e, st), "lm head gemm"); }
+    ctx->part_rows = e.tile_max ? n : 0;
     return QW_OK;
 }
 
@@ -561,13 +572,15 @@ int qw_decode_step(qw_ctx* ctx, const int32_t* tokens, const int32_t* positions,
     cudaStream_t st = (cudaStream_t)stream;
     float* out = logits ? logits : ctx->logits;
     // automatic choice: the fused kernel for batch 1, unless per-layer residuals are kept for checking
-    const bool fused = fused_supported(ctx->fused, batch) &&
+    const bool fused = fused_supported(ctx->fused, batch, bt_stride) &&
                        (ctx->decode_path == 2 || (ctx->decode_path == 0 && !ctx->hidden));
-    if (ctx->decode_path == 2 && !fused) return fail(QW_EINVAL, "qw_decode_step: the fused path takes batch 1 only");
+    if (ctx->decode_path == 2 && !fused)
+        return fail(QW_EINVAL, "qw_decode_step: the fused path takes batch 1 and block tables of at most 4088 pages");
     int rc;
     ctx->last_fused = fused;
     if (fused) {
         QW_PROF(QW_PROF_FUSED);
+        ctx->part_rows = 0;
         rc = fused_decode(ctx->fused, tokens, positions, batch, kv->base, kv->layer_elems, kv->page_elems,
                           kv->n_pages, bt, bt_stride, out, ctx->err, st);
         if (rc) return fail(rc, "fused decode launch failed");
@@ -589,11 +602,13 @@ int qw_sample(qw_ctx* ctx, const float* logits, int32_t batch, const qw_sample_p
         if (ctx->logits_rows < batch) return fail(QW_EINVAL, "qw_sample: the context holds fewer logits rows than batch");
         logits = ctx->logits;
     }
-    const int* hint = (logits == ctx->logits && ctx->last_fused && batch == 1) ? fused_argmax(ctx->fused) : nullptr;
+    const bool own = logits == ctx->logits;   // the context's logits of the last call
+    const int* hint = (own && ctx->last_fused && batch == 1) ? fused_argmax(ctx->fused) : nullptr;
+    const float2* part = (own && ctx->part_rows >= batch) ? ctx->tile_part : nullptr;
     cudaStream_t st = (cudaStream_t)stream;
     QW_PROF(QW_PROF_SAMPLE);
-    QW_TRY(launch_sample(logits, batch, ctx->cfg.vocab, params, rng_counter, out_ids, hint, ctx->err,
-                         (cudaStream_t)stream),
+    QW_TRY(launch_sample(logits, batch, ctx->cfg.vocab, params, rng_counter, out_ids, part, ctx->n_part, hint,
+                         ctx->err, (cudaStream_t)stream),
            "sample launch");
     return QW_OK;
 }
@@ -703,6 +718,12 @@ int qw_debug_profile(qw_ctx* ctx, int32_t enable, double* ms_out, int64_t* count
     if (enable) p.used = 0;
     p.on = enable != 0;
     return QW_OK;
+}
+
+int qw_debug_inject_timeout(qw_ctx* ctx) {
+    if (!ctx) return fail(QW_EINVAL, "null context");
+    if (!ctx->fused) return fail(QW_EINVAL, "no fused decode kernel in this context");
+    return fused_inject_timeout(ctx->fused);
 }
 
 int qw_set_prefill_attention(qw_ctx* ctx, int32_t variant) {

@@ -1,29 +1,35 @@
 // Fused persistent decode for one sequence (batch 1): one cooperative launch per
 // step runs the article's whole forward pass (Steps 2-8) for the new token.
 //
-// Every CTA (one per SM) owns fixed slices of every weight matrix.  Warp 0 streams
-// those slices -- q|k|v rows, the transposed o_proj rows, gate/up row pairs, the
-// transposed down_proj rows of all layers, then the tied LM-head rows -- through a
-// shared-memory ring with cp.async.bulk, in the order the consumers use them and
-// independent of any data dependency, so HBM keeps streaming while the consumers
-// wait.  Warps 1..8 consume the ring:
+// The grid is made of clusters of 8 CTAs (one CTA per SM).  Clusters 0..7 each own
+// one KV head group g (two query heads sharing KV head g, Step 5) and do the whole
+// attention sublayer of that group without leaving the cluster:
 //
-//   P1  x -> RMSNorm -> q|k|v rows (dot products)          -> raw q|k|v in global
-//   P2  attention split (KV head g, part s of the cache)   -> partial (m, l, o)
-//   P3  merge the splits of the CTA's attention dims, o_proj as a sum of scaled rows
-//       of Wo^T (one row per attention dim)                -> atomic adds into oacc
-//   P4  x + oacc -> RMSNorm -> gate/up pairs -> SwiGLU -> down_proj as scaled rows of
-//       Wd^T                                                -> atomic adds into dacc
-//   LM  x + oacc + dacc -> final RMSNorm -> LM-head rows -> logits, argmax
+//   A1  x -> RMSNorm -> this CTA's 64 of the group's 512 q|k|v rows; the values are
+//       pushed into every cluster peer's shared memory (st.async, counted by an mbarrier)
+//   A2  QK-Norm, RoPE, the new K/V into the cache; attention over this CTA's eighth of
+//       the cached pages -> partial (max, sum, weighted values), pushed to the peers
+//       that own each output dimension
+//   A3  merge of the 8 partials for this CTA's 32 attention dims, o_proj as the sum of
+//       32 scaled rows of Wo^T, a reduction of the 8 CTAs' partial outputs through
+//       shared memory, and one store of this CTA's 128 outputs into the group's slot
 //
-// Phases meet through monotonically increasing counters in global memory (one
-// launch adds a known amount, so the targets are epoch * amount); every wait is
-// bounded by %globaltimer and ends in QW_ETIMEOUT instead of a hang.  The residual
-// stream stays in fp32: R (materialised once per layer), oacc and dacc are
-// double-buffered by layer parity and zeroed by their owner CTA once no reader can
-// be left.
-#include <cooperative_groups.h>
-
+// Then every cluster runs the feed-forward sublayer (Step 6), each CTA owning a slice
+// of the SwiGLU units:
+//
+//   M1  x + sum of the 8 group slots -> RMSNorm -> gate/up row pairs -> SwiGLU ->
+//       down_proj as scaled rows of Wd^T -> reduction inside the cluster -> one slot
+//       per cluster
+//   LM  x + sum of the cluster slots -> final RMSNorm -> tied LM-head rows, argmax
+//
+// So a layer crosses the GPU twice (group slots -> feed-forward, cluster slots -> next
+// layer), each time through per-cluster counters (release add / acquire poll, bounded
+// by %globaltimer); everything else moves between the 8 SMs of a cluster.  Every CTA
+// keeps its own copy of the fp32 residual stream and adds the slots in a fixed order,
+// so the step is deterministic.  Warp 0 of each CTA streams the CTA's weight rows and
+// KV pages of every layer, then the LM-head rows, through a shared-memory ring with
+// cp.async.bulk in consumption order, independent of the data, so HBM keeps streaming
+// while the consumers wait.
 #include <vector>
 
 #include "qw_common.cuh"
@@ -33,7 +39,9 @@
 namespace qw {
 namespace fused {
 
-constexpr int D = 1024, HQ = 16, HKV = 8, HD = 128, INTER = 3072, QKVR = 4096, AD = 2048;
+constexpr int D = 1024, HQ = 16, HKV = 8, HD = 128, INTER = 3072, AD = 2048;
+constexpr int CL = 8;                 // CTAs per cluster
+constexpr int MAX_CLUSTERS = 16;
 constexpr int NS = 6;                 // ring stages
 constexpr int STAGE = 32768;          // bytes per stage
 constexpr int ROW_B = D * 2;          // every streamed row is 1024 bf16
@@ -43,12 +51,20 @@ constexpr int PAGES_PER_STAGE = STAGE / (2 * PAGE_B);  // 4
 constexpr int NCW = 8;                // consumer warps
 constexpr int THREADS = 32 * (NCW + 1);
 constexpr int CNT_STRIDE = 32;        // counters 128 bytes apart
-constexpr int PART = HD + 2;
-constexpr int MAX_ROWS = 64;          // per-phase result slots (q|k|v rows per CTA <= 4096/G + 1)
+constexpr int QROWS = 512 / CL;       // q|k|v rows per attention CTA: 64
+constexpr int ODIMS = 2 * HD / CL;    // attention dims per attention CTA: 32
+constexpr int OWN = D / CL;           // outputs each CTA reduces for its cluster: 128
+constexpr int MAX_ROWS = 128;         // per-phase result slots
 constexpr int MAX_LAYERS = 64;
-constexpr uint64_t WAIT_NS = 2000000000ull;
+constexpr int PF = 8;                 // L2 prefetch distance beyond the ring, in stages
+constexpr int MAX_PAGES = 512;        // pages per attention CTA: caches up to 8 * 512 * 16 = 65536 positions
+constexpr int CNT_PER_LAYER = HKV + MAX_CLUSTERS;
+constexpr uint64_t WAIT_NS = 2000000000ull;        // 2 s: far beyond any legitimate wait
+constexpr uint64_t FAULT_WAIT_NS = 2000000ull;     // 2 ms: the injected timeout of the test hook
 constexpr int TRACE_SLOTS = QW_TRACE_SLOTS;
-constexpr int NSH = 8;   // accumulator shards: CTA c adds into shard c % NSH (fewer adds per address)
+constexpr uint32_t QKV_BYTES = 512 * 4;                 // per layer into each attention CTA
+constexpr uint32_t PART_BYTES = CL * ODIMS * 4 + CL * 16;  // O of my dims + (M, L) of both heads, 8 sources
+constexpr uint32_t RED_BYTES = CL * OWN * 4;            // 8 partial vectors of my 128 outputs
 
 struct LayerPtrs {
     const uint16_t *wqkv, *woT, *wgu, *wdT;
@@ -71,26 +87,26 @@ struct Params {
     int64_t layer_elems, page_elems;
     int n_pages;
     float* logits;
-    float* R;      // [2][D]
-    float* oacc;   // [2][NSH][D]
-    float* dacc;   // [2][NSH][D]
-    float* qkv;    // [QKVR]
-    float* part;   // [HQ][nsa][PART]
+    float* oslot;    // [2][HKV][D]  o_proj outputs of each KV group (layer parity)
+    float* dslot;    // [2][MAX_CLUSTERS][D]  down_proj outputs of each cluster
     float* lm_part;  // [G][2]
     int* argmax;     // [1]
     unsigned* sync;  // counters
     int* err;
-    int nsa;         // attention splits per KV head
+    int n_clusters;
     unsigned long long* trace;  // nullable: [G][n_layers + 1][TRACE_SLOTS] %globaltimer stamps
+    uint64_t wait_ns;           // limit of every bounded wait
+    unsigned fault_extra;       // test hook: layer 0's feed-forward waits for this many arrivals more than come
 };
 
 // counter slots
 QW_DEV unsigned* c_epoch(const Params& p) { return p.sync; }
-QW_DEV unsigned* c_qkvh(const Params& p, int l, int g) { return p.sync + CNT_STRIDE * (1 + l * 18 + g); }
-QW_DEV unsigned* c_split(const Params& p, int l, int g) { return p.sync + CNT_STRIDE * (1 + l * 18 + 8 + g); }
-QW_DEV unsigned* c_o(const Params& p, int l) { return p.sync + CNT_STRIDE * (1 + l * 18 + 16); }
-QW_DEV unsigned* c_x(const Params& p, int l) { return p.sync + CNT_STRIDE * (1 + l * 18 + 17); }
-QW_DEV unsigned* c_lm(const Params& p) { return p.sync + CNT_STRIDE * (1 + p.n_layers * 18); }
+QW_DEV unsigned* c_abort(const Params& p) { return p.sync + CNT_STRIDE; }
+QW_DEV unsigned* c_o(const Params& p, int l, int g) { return p.sync + CNT_STRIDE * (2 + l * CNT_PER_LAYER + g); }
+QW_DEV unsigned* c_x(const Params& p, int l, int c) {
+    return p.sync + CNT_STRIDE * (2 + l * CNT_PER_LAYER + HKV + c);
+}
+QW_DEV unsigned* c_lm(const Params& p) { return p.sync + CNT_STRIDE * (2 + p.n_layers * CNT_PER_LAYER); }
 
 QW_DEV unsigned ld_acquire(const unsigned* ptr) {
     unsigned v;
@@ -103,50 +119,146 @@ QW_DEV uint64_t gtimer() {
     return t;
 }
 QW_DEV void bar_consumers() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-// Phase-boundary timestamp (tracing builds of a step only).
-QW_DEV void stamp(const Params& p, int l, int k) {
-    if (p.trace) p.trace[((size_t)blockIdx.x * (p.n_layers + 1) + l) * TRACE_SLOTS + k] = gtimer();
+QW_DEV uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+QW_DEV uint32_t cluster_id() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+QW_DEV void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Address of this CTA's shared variable `local` in the shared memory of cluster peer `rank`.
+QW_DEV uint32_t peer_addr(const void* local, int rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+    return r;
+}
+// 16 (8) bytes into a peer's shared memory; the peer's mbarrier counts them on arrival.
+QW_DEV void push4(uint32_t raddr, float4 v, uint32_t rbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     raddr),
+                 "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(rbar)
+                 : "memory");
+}
+QW_DEV void push2(uint32_t raddr, float a, float b, uint32_t rbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(raddr),
+                 "f"(a), "f"(b), "r"(rbar)
+                 : "memory");
+}
+QW_DEV bool mbar_test_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+QW_DEV bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
 }
 
 struct Smem {
     uint64_t full[NS], empty[NS];
+    uint64_t bar_qkv, bar_part, bar_redo, bar_redd;  // cluster exchanges (one phase per layer)
     int spg[NS][PAGES_PER_STAGE];  // page ids of a KV stage (-1: none or out of range)
+    int pages[MAX_PAGES];          // page ids of this CTA's share of the cache (-1: out of range)
     volatile int abort_flag;
-    int pad;
-    alignas(16) float h[D];  // normalised activation of the current phase (read as float4)
-    float res[MAX_ROWS];   // dot products of the current phase
-    float coef[MAX_ROWS];  // scale of each row in the scaled-row phases
+    int s_ok_x, s_ok_o;              // results of the two global waits of a layer (one slot each)
+    alignas(16) float h[D];          // normalised activation of the current phase (read as float4)
+    alignas(16) float res[MAX_ROWS]; // dot products of the current phase
+    float coef[MAX_ROWS];            // scale of each row in the scaled-row phases
     float wsum[NCW];
+    alignas(16) float qkv_s[512];         // the group's q head 2g | q head 2g+1 | k | v, pushed by the peers
+    alignas(16) float part_o[CL][ODIMS];  // attention outputs of my 32 dims from each peer (unnormalised)
+    alignas(16) float part_ml[CL][4];     // (max, sum) of both heads from each peer
+    alignas(16) float red_o[CL][OWN];     // o_proj partials of my 128 outputs from each peer
+    alignas(16) float red_d[CL][OWN];     // down_proj partials of my 128 outputs from each peer
     // rotated queries, pre-scaled to log2 units: dim 8 u + 4 h + e of head hh at q[hh][h][u][e], so
     // that the float4 reads of 8 different chunks u hit 8 different bank groups
     alignas(16) float q[2][2][HD / 8][4];
     alignas(16) uint16_t kn_b[HD];   // the new key and value as bf16 (as the cache holds them)
     alignas(16) uint16_t vn_b[HD];
-    alignas(16) float pp[2][2][64];  // attention: exp2(s - m_w) per key slot (two stage buffers)
-    float am[2][NCW][2], al[2][NCW][2];  // per-warp max and sum of those (two stage buffers)
-    alignas(16) float ao[PAGES_PER_STAGE][2][HD];  // per-page partial outputs
-    float alq[PAGES_PER_STAGE][2];
+    alignas(16) float wo[NCW][2][HD];  // attention: each warp's weighted values of both heads
+    float wml[NCW][4];                 // each warp's (max, sum) of both heads
     float lm_val[NCW];
     int lm_idx[NCW];
     int last_cta;
 };
 constexpr int SMEM_BYTES = NS * STAGE + 1024 + (int)sizeof(Smem);
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
-// Bounded wait for a global counter (one thread); false on timeout or abort.
-QW_DEV bool wait_count(const unsigned* ptr, unsigned target, Smem& sm, int* err) {
-    if ((int)(ld_acquire(ptr) - target) >= 0) return true;
+// Phase-boundary timestamp (tracing builds of a step only).
+QW_DEV void stamp(const Params& p, int l, int k) {
+    if (p.trace) p.trace[((size_t)blockIdx.x * (p.n_layers + 1) + l) * TRACE_SLOTS + k] = gtimer();
+}
+
+QW_DEV void give_up(const Params& p, Smem& sm) {
+    set_error(p.err, QW_ETIMEOUT);
+    sm.abort_flag = 1;
+    atomicExch(c_abort(p), 1u);
+}
+
+// Bounded wait of one warp for `n` counters (lane i polls first + i * CNT_STRIDE) to reach
+// `target`; warp-uniform result, false on timeout or abort.
+QW_DEV bool wait_counters(const Params& p, const unsigned* first, int n, unsigned target, Smem& sm) {
+    const int lane = threadIdx.x & 31;
+    const unsigned* ptr = first + (lane < n ? lane : 0) * CNT_STRIDE;
+    auto done = [&]() { return __all_sync(0xffffffffu, lane >= n || (int)(ld_acquire(ptr) - target) >= 0); };
+    if (done()) return true;
     const uint64_t t0 = gtimer();
     for (unsigned i = 0;; ++i) {
-        if ((int)(ld_acquire(ptr) - target) >= 0) return true;
+        if (done()) return true;
         if ((i & 63) == 63) {
-            if (sm.abort_flag) return false;
-            if (gtimer() - t0 > WAIT_NS) {
-                set_error(err, QW_ETIMEOUT);
-                sm.abort_flag = 1;
+            int bad = 0;
+            if (lane == 0) bad = sm.abort_flag || ld_acquire(c_abort(p)) != 0 || gtimer() - t0 > p.wait_ns;
+            if (__shfl_sync(0xffffffffu, bad, 0)) {
+                if (lane == 0 && !sm.abort_flag) give_up(p, sm);
                 return false;
             }
         }
     }
+}
+
+// Bounded wait for phase `parity` of a cluster-exchange mbarrier: lane 0 of each calling warp
+// polls (one poller per warp, not 32), __syncwarp orders the other lanes after its acquire.
+QW_DEV bool wait_cluster(const Params& p, uint64_t* bar, uint32_t parity, Smem& sm) {
+    int good = 1;
+    if ((threadIdx.x & 31) == 0 && !mbar_test_wait_cluster(bar, parity)) {
+        const uint64_t t0 = gtimer();
+        for (unsigned i = 0;; ++i) {
+            if (mbar_test_wait_cluster(bar, parity) || mbar_try_wait_cluster(bar, parity)) break;
+            if ((i & 63) == 63) {
+                if (sm.abort_flag || ld_acquire(c_abort(p)) != 0) {
+                    good = 0;
+                    break;
+                }
+                if (gtimer() - t0 > p.wait_ns) {
+                    give_up(p, sm);
+                    good = 0;
+                    break;
+                }
+            }
+        }
+    }
+    good = __shfl_sync(0xffffffffu, good, 0);
+    __syncwarp();
+    return good != 0;
 }
 
 // Publish: called by one thread after a barrier of every thread whose writes it
@@ -164,104 +276,164 @@ QW_DEV void unpack8(uint4 w, float (&f)[8]) {
 QW_DEV int slice_lo(int n, int c, int G) { return (int)((long)n * c / G); }
 
 struct Work {
-    int q0, q1;    // q|k|v rows
-    int j0, j1;    // attention dims (rows of Wo^T)
-    int p0, p1;    // gate/up pairs (rows of Wd^T)
-    int v0, v1;    // LM-head rows
-    int d0, d1;    // residual rows owned (materialise R, zero the accumulators)
-    int g, s;      // attention item (g < 0: none)
-    int pg_lo, pg_hi;  // pages of the attention item
-    bool has_new;      // the item holds the new token's page
+    int cid, rank;     // cluster and rank in it
+    bool attn;         // the cluster owns KV group g = cid
+    int qrow0;         // first of this CTA's 64 q|k|v rows
+    int j0;            // first of this CTA's 32 attention dims (rows of Wo^T)
+    int pg_lo, pg_hi;  // pages of this CTA's share of the cache
+    bool has_new;      // that share holds the new token's page
+    int p0, p1;        // SwiGLU units (gate/up row pairs, rows of Wd^T)
+    int v0, v1;        // LM-head rows
 };
 
-QW_DEV Work make_work(const Params& p, int c, int G, int pos, bool bad_pos) {
+QW_DEV Work make_work(const Params& p, int pos, bool bad_pos) {
     Work w;
-    w.q0 = slice_lo(QKVR, c, G);
-    w.q1 = slice_lo(QKVR, c + 1, G);
-    w.j0 = slice_lo(AD, c, G);
-    w.j1 = slice_lo(AD, c + 1, G);
+    const int G = gridDim.x, c = blockIdx.x;
+    w.cid = (int)cluster_id();
+    w.rank = (int)cluster_rank();
+    w.attn = w.cid < HKV;
+    const int g = w.cid, r = w.rank;
+    // q head 2g: ranks 0,1; q head 2g+1: ranks 2,3; k head g: ranks 4,5; v head g: ranks 6,7
+    w.qrow0 = r < 4 ? 256 * g + 64 * r : (r < 6 ? 2048 + 128 * g + 64 * (r - 4) : 3072 + 128 * g + 64 * (r - 6));
+    w.j0 = 256 * g + ODIMS * r;
+    if (bad_pos) pos = 0;
+    const int np = pos / QW_PAGE_SIZE + 1;  // pages holding positions 0..pos
+    w.pg_lo = (int)((long)np * r / CL);
+    w.pg_hi = (int)((long)np * (r + 1) / CL);
+    w.has_new = (pos / QW_PAGE_SIZE) >= w.pg_lo && (pos / QW_PAGE_SIZE) < w.pg_hi;
     w.p0 = slice_lo(INTER, c, G);
     w.p1 = slice_lo(INTER, c + 1, G);
     w.v0 = slice_lo(p.V, c, G);
     w.v1 = slice_lo(p.V, c + 1, G);
-    w.d0 = 4 * slice_lo(D / 4, c, G);      // owned residual entries, in float4 groups
-    w.d1 = 4 * slice_lo(D / 4, c + 1, G);
-    w.g = -1;
-    w.s = 0;
-    w.pg_lo = w.pg_hi = 0;
-    w.has_new = false;
-    if (c < HKV * p.nsa) {
-        if (bad_pos) pos = 0;
-        w.g = c / p.nsa;
-        w.s = c % p.nsa;
-        const int np = pos / QW_PAGE_SIZE + 1;  // pages holding positions 0..pos
-        w.pg_lo = (int)((long)np * w.s / p.nsa);
-        w.pg_hi = (int)((long)np * (w.s + 1) / p.nsa);
-        w.has_new = (pos / QW_PAGE_SIZE) >= w.pg_lo && (pos / QW_PAGE_SIZE) < w.pg_hi;
-    }
     return w;
 }
 
 // ---------------------------------------------------------------- producer
+// The stages a CTA streams, in consumption order.  Layer l (attention CTAs): part 0 its q|k|v
+// rows, part 1 its KV pages, part 2 its Wo^T rows; every CTA: part 3 its gate/up row pairs,
+// part 4 its Wd^T rows.  After the last layer, part 5: its LM-head rows.
+struct Seq {
+    int l = 0, part = 0, i = 0;   // layer, part, stage within the part
+};
+struct StageDesc {
+    const uint16_t* rows;   // row stages: first row
+    int n;                  // rows, or pages
+    int pg0;                // page stages: index of the first page in this CTA's page list
+    int l;                  // page stages: layer
+    bool pages;
+};
+
 struct Producer {
     uint8_t* ring;
     Smem* sm;
-    int* err;
+    const Params* p;
+    const Work* w;
+    bool bad_pos;
     unsigned it = 0;
     bool stop = false;
+    Seq ld, pf;               // next stage to load into the ring / to prefetch into L2
+    unsigned pf_count = NS;   // index of the stage pf points at (the first NS stages load directly)
 
+    // The stage at q (advancing q); false past the end.
+    QW_DEV bool next(Seq& q, StageDesc& d) const {
+        for (;;) {
+            if (q.l > p->n_layers) return false;
+            const int part = q.l == p->n_layers ? 5 : q.part;
+            const uint16_t* base = nullptr;
+            int total = 0;
+            bool pages = false;
+            if (part == 5) {
+                base = p->E + (size_t)w->v0 * D;
+                total = w->v1 - w->v0;
+            } else if (part <= 2 && !w->attn) {
+                total = 0;
+            } else {
+                const LayerPtrs& L = p->layers[q.l];
+                if (part == 0) base = L.wqkv + (size_t)w->qrow0 * D, total = QROWS;
+                else if (part == 1) pages = true, total = bad_pos ? 0 : w->pg_hi - w->pg_lo;
+                else if (part == 2) base = L.woT + (size_t)w->j0 * D, total = ODIMS;
+                else if (part == 3) base = L.wgu + (size_t)2 * w->p0 * D, total = 2 * (w->p1 - w->p0);
+                else base = L.wdT + (size_t)w->p0 * D, total = w->p1 - w->p0;
+            }
+            const int per = pages ? PAGES_PER_STAGE : ROWS_PER_STAGE;
+            if (q.i * per < total) {
+                d.pages = pages;
+                d.l = q.l;
+                d.n = min(per, total - q.i * per);
+                d.pg0 = q.i * per;
+                d.rows = pages ? nullptr : base + (size_t)q.i * per * D;
+                ++q.i;
+                return true;
+            }
+            q.i = 0;
+            if (part == 5 || ++q.part == 5) {
+                q.part = 0;
+                ++q.l;
+            }
+        }
+    }
+    QW_DEV const uint16_t* page_ptr(int l, int idx, int which) const {
+        const int pg = sm->pages[idx];
+        return p->kv + (int64_t)l * p->layer_elems + (int64_t)pg * p->page_elems +
+               ((int64_t)which * HKV + w->cid) * QW_PAGE_SIZE * HD;
+    }
     QW_DEV bool acquire(int& s) {
         s = it % NS;
         const uint32_t ph = (it / NS) & 1;
+        if (mbar_test_wait(&sm->empty[s], ph ^ 1)) return true;
         for (uint32_t i = 0; i < QW_SPIN_LIMIT; ++i) {
             if (mbar_try_wait(&sm->empty[s], ph ^ 1)) return true;
-            if ((i & 63) == 63 && sm->abort_flag) return false;
+            if ((i & 63) == 63 && (sm->abort_flag || ld_acquire(c_abort(*p)) != 0)) return false;
             if (i > 64) __nanosleep(64);
         }
-        set_error(err, QW_ETIMEOUT);
-        sm->abort_flag = 1;
+        give_up(*p, *sm);
         return false;
     }
-    QW_DEV void rows(const uint16_t* base, int nrows) {
-        for (int r0 = 0; r0 < nrows && !stop; r0 += ROWS_PER_STAGE) {
-            const int n = min(ROWS_PER_STAGE, nrows - r0);
-            int s;
-            if (!acquire(s)) {
-                stop = true;
-                return;
+    // L2 prefetch of the stages up to index `upto`: HBM streams at the pace of consumption,
+    // PF stages ahead of the ring, and the ring loads then hit L2.
+    QW_DEV void prefetch_until(unsigned upto) {
+        StageDesc d;
+        while (pf_count <= upto && next(pf, d)) {
+            ++pf_count;
+            if (!d.pages) {
+                prefetch_l2(d.rows, d.n * ROW_B);
+            } else {
+                for (int i = 0; i < d.n; ++i) {
+                    if (sm->pages[d.pg0 + i] < 0) continue;
+                    prefetch_l2(page_ptr(d.l, d.pg0 + i, 0), PAGE_B);
+                    prefetch_l2(page_ptr(d.l, d.pg0 + i, 1), PAGE_B);
+                }
             }
-            mbar_arrive_expect_tx(&sm->full[s], n * ROW_B);
-            bulk_load(ring + s * STAGE, base + (size_t)r0 * D, n * ROW_B, &sm->full[s]);
-            ++it;
         }
     }
-    // K and V of KV head g for pages [lo, hi) of one sequence: page i of a stage holds K at
-    // i * 8 KB and V at i * 8 KB + 4 KB.
-    QW_DEV void pages(const uint16_t* kv_layer, int64_t page_elems, int n_pages, const int* bt, int g, int lo,
-                      int hi) {
-        for (int p0 = lo; p0 < hi && !stop; p0 += PAGES_PER_STAGE) {
-            const int n = min(PAGES_PER_STAGE, hi - p0);
+    // Stream every stage through the ring.
+    QW_DEV void run() {
+        StageDesc d;
+        while (!stop && next(ld, d)) {
+            prefetch_until(it + NS + PF - 1);
             int s;
             if (!acquire(s)) {
                 stop = true;
                 return;
             }
-            int pgs[PAGES_PER_STAGE];
-            int valid = 0;
-            for (int i = 0; i < PAGES_PER_STAGE; ++i) pgs[i] = i < n ? __ldg(bt + p0 + i) : -1;  // loads in flight together
-            for (int i = 0; i < PAGES_PER_STAGE; ++i) {
-                if (pgs[i] < 0 || pgs[i] >= n_pages) pgs[i] = -1;
-                valid += pgs[i] >= 0;
-                sm->spg[s][i] = pgs[i];  // published to the consumers by the arrive below
-            }
-            mbar_arrive_expect_tx(&sm->full[s], valid * 2 * PAGE_B);
-            for (int i = 0; i < n; ++i) {
-                const int pg = pgs[i];
-                if (pg < 0) continue;
-                const uint16_t* kp = kv_layer + (int64_t)pg * page_elems + (int64_t)g * QW_PAGE_SIZE * HD;
-                bulk_load(ring + s * STAGE + i * 2 * PAGE_B, kp, PAGE_B, &sm->full[s]);
-                bulk_load(ring + s * STAGE + i * 2 * PAGE_B + PAGE_B, kp + (int64_t)HKV * QW_PAGE_SIZE * HD, PAGE_B,
-                          &sm->full[s]);
+            if (!d.pages) {
+                mbar_arrive_expect_tx(&sm->full[s], d.n * ROW_B);
+                bulk_load(ring + s * STAGE, d.rows, d.n * ROW_B, &sm->full[s]);
+            } else {
+                // page i of a stage holds K at i * 8 KB and V at i * 8 KB + 4 KB
+                int valid = 0;
+                for (int i = 0; i < PAGES_PER_STAGE; ++i) {
+                    const int pg = i < d.n ? sm->pages[d.pg0 + i] : -1;
+                    valid += pg >= 0;
+                    sm->spg[s][i] = pg;  // published to the consumers by the arrive below
+                }
+                mbar_arrive_expect_tx(&sm->full[s], valid * 2 * PAGE_B);
+                for (int i = 0; i < d.n; ++i) {
+                    if (sm->pages[d.pg0 + i] < 0) continue;
+                    bulk_load(ring + s * STAGE + i * 2 * PAGE_B, page_ptr(d.l, d.pg0 + i, 0), PAGE_B, &sm->full[s]);
+                    bulk_load(ring + s * STAGE + i * 2 * PAGE_B + PAGE_B, page_ptr(d.l, d.pg0 + i, 1), PAGE_B,
+                              &sm->full[s]);
+                }
             }
             ++it;
         }
@@ -269,11 +441,29 @@ struct Producer {
     // Before the CTA exits: every copy issued must have landed.
     QW_DEV void drain() {
         const unsigned first = it > (unsigned)NS ? it - NS : 0;
-        for (unsigned i = first; i < it; ++i) mbar_wait(&sm->full[i % NS], (i / NS) & 1, err);
+        for (unsigned i = first; i < it; ++i) mbar_wait(&sm->full[i % NS], (i / NS) & 1, p->err);
     }
 };
 
 // ---------------------------------------------------------------- consumer helpers
+QW_DEV uint64_t pack2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+QW_DEV void unpack2(uint64_t v, float& lo, float& hi) { asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v)); }
+QW_DEV float hsum2(uint64_t v) {
+    float lo, hi;
+    unpack2(v, lo, hi);
+    return lo + hi;
+}
+// acc.{lo,hi} += a.{lo,hi} * b.{lo,hi} (packed fp32, the rounding of two fmaf)
+QW_DEV void ffma2(uint64_t& acc, uint64_t a, uint64_t b) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+// a bf16 pair (low element in the low half) as packed fp32
+QW_DEV uint64_t bf2_to_f2(uint32_t w) { return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)); }
+
 struct Consumer {
     uint8_t* ring;
     Smem* sm;
@@ -281,9 +471,14 @@ struct Consumer {
     int cw, lane;   // consumer warp 0..7, lane
     unsigned it = 0;
 
+    // One lane of the warp waits for the stage (256 threads polling one mbarrier serialise on
+    // it); __syncwarp then orders the other lanes' reads of the stage after that acquire.
     QW_DEV const uint8_t* stage_wait(bool& ok) {
         const int s = it % NS;
-        ok = ok && !sm->abort_flag && mbar_wait(&sm->full[s], (it / NS) & 1, err);
+        int good = ok;
+        if (lane == 0) good = good && !sm->abort_flag && mbar_wait(&sm->full[s], (it / NS) & 1, err);
+        ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+        __syncwarp();
         if (!ok) sm->abort_flag = 1;
         return ring + s * STAGE;
     }
@@ -293,22 +488,23 @@ struct Consumer {
         if (lane == 0) mbar_arrive(&sm->empty[it % NS]);
         ++it;
     }
-    // Dot products of `nrows` streamed rows with sm->h; results to sm->res[0..nrows).
-    QW_DEV bool dot_rows(int nrows, bool ok, const Params* tp = nullptr, int tl = 0, int tslot = 0) {
-        float hreg[4][8];
+    // Dot products of `nrows` streamed rows with sm->h; results to sm->res[0..nrows).  Lane l
+    // takes columns 8 l + 256 i .. + 7 (i < 4) of rows cw and cw + 8, with packed fp32 FMAs.
+    QW_DEV bool dot_rows(int nrows, bool ok) {
+        uint64_t h2[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const float4 a = *(const float4*)&sm->h[8 * lane + 256 * i];
             const float4 b = *(const float4*)&sm->h[8 * lane + 256 * i + 4];
-            hreg[i][0] = a.x; hreg[i][1] = a.y; hreg[i][2] = a.z; hreg[i][3] = a.w;
-            hreg[i][4] = b.x; hreg[i][5] = b.y; hreg[i][6] = b.z; hreg[i][7] = b.w;
+            h2[i][0] = pack2(a.x, a.y);
+            h2[i][1] = pack2(a.z, a.w);
+            h2[i][2] = pack2(b.x, b.y);
+            h2[i][3] = pack2(b.z, b.w);
         }
         for (int r0 = 0; r0 < nrows; r0 += ROWS_PER_STAGE) {
             const int n = min(ROWS_PER_STAGE, nrows - r0);
             const uint8_t* st = stage_wait(ok);
-            if (tp && r0 == 0 && cw == 0 && lane == 0) stamp(*tp, tl, tslot);
             if (ok) {
-                // rows cw and cw + 8 together: two independent chains per row, loads issued first
                 for (int r = cw; r < n; r += 2 * NCW) {
                     const bool two = r + NCW < n;
                     const uint4* ra = (const uint4*)(st + r * ROW_B);
@@ -319,30 +515,28 @@ struct Consumer {
                         wa[i] = ra[lane + 32 * i];
                         wb[i] = rb[lane + 32 * i];
                     }
-                    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+                    uint64_t a0 = 0, a1 = 0, b0 = 0, b1 = 0;   // two packed accumulators per row
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        float fa[8], fb[8];
-                        unpack8(wa[i], fa);
-                        unpack8(wb[i], fb);
+                        ffma2(a0, h2[i][0], bf2_to_f2(wa[i].x));
+                        ffma2(a1, h2[i][1], bf2_to_f2(wa[i].y));
+                        ffma2(a0, h2[i][2], bf2_to_f2(wa[i].z));
+                        ffma2(a1, h2[i][3], bf2_to_f2(wa[i].w));
+                        ffma2(b0, h2[i][0], bf2_to_f2(wb[i].x));
+                        ffma2(b1, h2[i][1], bf2_to_f2(wb[i].y));
+                        ffma2(b0, h2[i][2], bf2_to_f2(wb[i].z));
+                        ffma2(b1, h2[i][3], bf2_to_f2(wb[i].w));
+                    }
+                    const float a = hsum2(a0) + hsum2(a1), b = hsum2(b0) + hsum2(b1);
+                    // two-row butterfly: after the first exchange lanes 0..15 carry row a and
+                    // lanes 16..31 row b, so both rows reduce with 5 shuffles instead of 10
+                    const bool up = lane & 16;
+                    float v = up ? b : a;
+                    v += __shfl_xor_sync(0xffffffffu, up ? a : b, 16);
 #pragma unroll
-                        for (int e = 0; e < 8; e += 2) {
-                            a0 = fmaf(hreg[i][e], fa[e], a0);
-                            a1 = fmaf(hreg[i][e + 1], fa[e + 1], a1);
-                            b0 = fmaf(hreg[i][e], fb[e], b0);
-                            b1 = fmaf(hreg[i][e + 1], fb[e + 1], b1);
-                        }
-                    }
-                    float a = a0 + a1, b = b0 + b1;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        a += __shfl_xor_sync(0xffffffffu, a, o);
-                        b += __shfl_xor_sync(0xffffffffu, b, o);
-                    }
-                    if (lane == 0) {
-                        sm->res[r0 + r] = a;
-                        if (two) sm->res[r0 + r + NCW] = b;
-                    }
+                    for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                    if (lane == 0) sm->res[r0 + r] = v;
+                    if (lane == 16 && two) sm->res[r0 + r + NCW] = v;
                 }
             }
             stage_release();
@@ -357,15 +551,17 @@ struct Consumer {
             const uint8_t* st = stage_wait(ok);
             if (ok) {
                 const uint8_t* col = st + (128 * cw + 4 * lane) * 2;
+                uint64_t c01 = pack2(acc[0], acc[1]), c23 = pack2(acc[2], acc[3]);
 #pragma unroll 4
                 for (int r = 0; r < n; ++r) {
                     const uint2 wv = *(const uint2*)(col + r * ROW_B);
                     const float a = sm->coef[r0 + r];
-                    acc[0] = fmaf(a, bf16_lo(wv.x), acc[0]);
-                    acc[1] = fmaf(a, bf16_hi(wv.x), acc[1]);
-                    acc[2] = fmaf(a, bf16_lo(wv.y), acc[2]);
-                    acc[3] = fmaf(a, bf16_hi(wv.y), acc[3]);
+                    const uint64_t aa = pack2(a, a);
+                    ffma2(c01, aa, bf2_to_f2(wv.x));
+                    ffma2(c23, aa, bf2_to_f2(wv.y));
                 }
+                unpack2(c01, acc[0], acc[1]);
+                unpack2(c23, acc[2], acc[3]);
             }
             stage_release();
         }
@@ -373,29 +569,9 @@ struct Consumer {
     }
 };
 
-// Sum over the NSH shards of a [NSH][D] accumulator at entries k0 .. k0+3 (loads in flight together).
-QW_DEV float4 sum_shards(const float* base, int k0) {
-    float4 v[NSH];
-#pragma unroll
-    for (int s = 0; s < NSH; ++s) v[s] = __ldcg((const float4*)(base + s * D + k0));
-    float4 t = v[0];
-#pragma unroll
-    for (int s = 1; s < NSH; ++s) {
-        t.x += v[s].x;
-        t.y += v[s].y;
-        t.z += v[s].z;
-        t.w += v[s].w;
-    }
-    return t;
-}
-
-// Add this lane's 4 output columns into global dst (one 16-byte atomic).
-QW_DEV void add_columns(const float (&acc)[4], float* dst, int cw, int lane) {
-    atomicAdd((float4*)(dst + 128 * cw + 4 * lane), make_float4(acc[0], acc[1], acc[2], acc[3]));
-}
-
-// x (4 entries per consumer thread) -> sm.h = x / rms(x) * w.  Consumer barriers inside.
-QW_DEV void norm_into_h(Smem& sm, const float (&x)[4], int k0, const float* w, float eps, int tid) {
+// x (4 entries per consumer thread) -> sm.h = x / rms(x) * w, w = this thread's 4 norm weights
+// (loaded ahead, so no global load sits on the critical path).  Consumer barriers inside.
+QW_DEV void norm_into_h(Smem& sm, const float (&x)[4], int k0, const float4 w, float eps, int tid) {
     float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
     ss = warp_sum(ss);
     if ((tid & 31) == 0) sm.wsum[tid >> 5] = ss;
@@ -404,51 +580,106 @@ QW_DEV void norm_into_h(Smem& sm, const float (&x)[4], int k0, const float* w, f
 #pragma unroll
     for (int i = 0; i < NCW; ++i) tot += sm.wsum[i];
     const float s = 1.0f / sqrtf(tot / (float)D + eps);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) sm.h[k0 + e] = x[e] * s * w[k0 + e];
+    *(float4*)&sm.h[k0] = make_float4(x[0] * s * w.x, x[1] * s * w.y, x[2] * s * w.z, x[3] * s * w.w);
     bar_consumers();
 }
 
-__global__ void __launch_bounds__(THREADS, 1) fused_decode_kernel(Params p) {
+// Cluster reduction of one 1024-wide partial per CTA: this thread's 4 columns (128 cw + 4 lane)
+// go to peer cw, which owns outputs [128 cw, 128 cw + 128).
+QW_DEV void push_partial(Smem& sm, float (&red)[CL][OWN], uint64_t* bar, const float (&acc)[4], int cw, int lane,
+                         int rank) {
+    push4(peer_addr(&red[rank][4 * lane], cw), make_float4(acc[0], acc[1], acc[2], acc[3]), peer_addr(bar, cw));
+}
+
+// Sum of the 8 peers' partials of this CTA's outputs (fixed order) into dst[128 rank + ..]:
+// threads 0..31 of the consumers, one float4 each.
+QW_DEV void store_reduced(const float (&red)[CL][OWN], float* dst, int rank, int tid) {
+    if (tid < OWN / 4) {
+        float4 t = *(const float4*)&red[0][4 * tid];
+#pragma unroll
+        for (int s = 1; s < CL; ++s) {
+            const float4 v = *(const float4*)&red[s][4 * tid];
+            t.x += v.x;
+            t.y += v.y;
+            t.z += v.z;
+            t.w += v.w;
+        }
+        *(float4*)(dst + OWN * rank + 4 * tid) = t;
+    }
+}
+
+// x += sum over n slots of [n][D] at entries k0 .. k0+3 (fixed order; loads in flight together)
+QW_DEV void add_slots(float (&x)[4], const float* base, int n, int k0) {
+    float4 v[MAX_CLUSTERS];
+#pragma unroll
+    for (int s = 0; s < MAX_CLUSTERS; ++s)
+        if (s < n) v[s] = __ldcg((const float4*)(base + (size_t)s * D + k0));
+#pragma unroll
+    for (int s = 0; s < MAX_CLUSTERS; ++s)
+        if (s < n) {
+            x[0] += v[s].x;
+            x[1] += v[s].y;
+            x[2] += v[s].z;
+            x[3] += v[s].w;
+        }
+}
+
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_decode_kernel(const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     Smem& sm = *(Smem*)(ring + NS * STAGE);
     const int G = gridDim.x, c = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pos = p.positions[0];
+    const int tok = p.tokens[0];
+    // a position outside the block table, or a share of the cache longer than the page list
+    // (the host takes this kernel only for block tables of at most CL * MAX_PAGES pages)
+    const bool bad_pos = pos < 0 || pos >= p.bt_stride * QW_PAGE_SIZE || pos / QW_PAGE_SIZE >= CL * MAX_PAGES - CL;
+    const Work w = make_work(p, pos, bad_pos);
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], NCW);
         }
+        mbar_init(&sm.bar_qkv, 1);
+        mbar_init(&sm.bar_part, 1);
+        mbar_init(&sm.bar_redo, 1);
+        mbar_init(&sm.bar_redd, 1);
+        // phase 0 of each exchange: the bytes the peers will push in layer 0
+        if (w.attn) {
+            mbar_arrive_expect_tx(&sm.bar_qkv, QKV_BYTES);
+            mbar_arrive_expect_tx(&sm.bar_part, PART_BYTES);
+            mbar_arrive_expect_tx(&sm.bar_redo, RED_BYTES);
+        }
+        mbar_arrive_expect_tx(&sm.bar_redd, RED_BYTES);
         sm.abort_flag = 0;
         fence_mbar_init();
     }
-    __syncthreads();
-    const int pos = p.positions[0];
-    const int tok = p.tokens[0];
+    // every peer's barriers exist before anyone pushes into them
+    cluster_sync_all();
     const unsigned epoch = ld_acquire(c_epoch(p)) + 1;  // this launch's targets are epoch * amount
-    const bool bad_pos = pos < 0 || pos >= p.bt_stride * QW_PAGE_SIZE;
-    const Work w = make_work(p, c, G, pos, bad_pos);
     if (bad_pos && c == 0 && threadIdx.x == 0) set_error(p.err, QW_ERANGE);
 
     if (warp == 0) {
         // ------------------------------------------------ producer
-        if (lane == 0) {
-            Producer pr{ring, &sm, p.err};
-            for (int l = 0; l < p.n_layers && !pr.stop; ++l) {
-                const LayerPtrs& L = p.layers[l];
-                pr.rows(L.wqkv + (size_t)w.q0 * D, w.q1 - w.q0);
-                if (w.g >= 0 && !bad_pos)
-                    pr.pages(p.kv + (int64_t)l * p.layer_elems, p.page_elems, p.n_pages, p.bt, w.g, w.pg_lo,
-                             w.pg_hi);
-                pr.rows(L.woT + (size_t)w.j0 * D, w.j1 - w.j0);
-                pr.rows(L.wgu + (size_t)2 * w.p0 * D, 2 * (w.p1 - w.p0));
-                pr.rows(L.wdT + (size_t)w.p0 * D, w.p1 - w.p0);
-                stamp(p, l, 9);
+        // this CTA's page ids, read once for every layer (out-of-range ids become -1 and are reported)
+        if (w.attn && !bad_pos)
+            for (int i = lane; i < w.pg_hi - w.pg_lo; i += 32) {
+                int pg = __ldg(p.bt + w.pg_lo + i);
+                if (pg < 0 || pg >= p.n_pages) {
+                    set_error(p.err, QW_ERANGE);
+                    pg = -1;
+                }
+                sm.pages[i] = pg;
             }
-            pr.rows(p.E + (size_t)w.v0 * D, w.v1 - w.v0);
+        __syncwarp();
+        if (lane == 0) {
+            Producer pr{ring, &sm, &p, &w, bad_pos};
+            pr.run();
             pr.drain();
         }
+        __syncwarp();
+        cluster_sync_all();   // no peer pushes into this CTA's shared memory after it exits
         return;
     }
 
@@ -457,76 +688,75 @@ __global__ void __launch_bounds__(THREADS, 1) fused_decode_kernel(Params p) {
     const int cw = tid >> 5;
     Consumer cs{ring, &sm, p.err, cw, lane};
     bool ok = !bad_pos;
-    const int k0 = 4 * tid;  // this thread's 4 residual entries in the norm phases
-    const bool own = k0 >= w.d0 && k0 < w.d1;
+    const int k0 = 4 * tid;  // this thread's 4 residual entries
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
-    __shared__ bool s_ok;
+    const int NC = p.n_clusters;
+    const int g = w.cid, r = w.rank;
 
+    // this thread's entries of the residual stream: x before the layer (xa), after attention (xm)
+    float xa[4], xm[4];
+    {
+        const uint2 e = (tok >= 0 && tok < p.V) ? *(const uint2*)(p.E + (size_t)tok * D + k0) : make_uint2(0, 0);
+        xa[0] = bf16_lo(e.x); xa[1] = bf16_hi(e.x); xa[2] = bf16_lo(e.y); xa[3] = bf16_hi(e.y);
+        if (c == 0 && tid == 0 && !(tok >= 0 && tok < p.V)) set_error(p.err, QW_ERANGE);
+    }
+
+    // RoPE inverse frequencies of this lane's two rotation pairs (the same for every layer)
+    const float invf0 = p.inv_freq[lane], invf1 = p.inv_freq[lane + 32];
     for (int l = 0; l < p.n_layers; ++l) {
-        const LayerPtrs& L = p.layers[l];
-        const int pb = l & 1, qb = pb ^ 1;
-        // ---------------- P1: x -> norm -> q|k|v rows
-        if (tid == 0) {
-            stamp(p, l, 0);
-            s_ok = ok && (l == 0 || wait_count(c_x(p, l - 1), epoch * G, sm, p.err));
-            stamp(p, l, 1);
-        }
-        bar_consumers();
-        ok = s_ok;
-        float x[4];
-        if (l == 0) {
-            const uint2 e = (tok >= 0 && tok < p.V) ? *(const uint2*)(p.E + (size_t)tok * D + k0) : make_uint2(0, 0);
-            x[0] = bf16_lo(e.x); x[1] = bf16_hi(e.x); x[2] = bf16_lo(e.y); x[3] = bf16_hi(e.y);
-            if (c == 0 && tid == 0 && !(tok >= 0 && tok < p.V)) set_error(p.err, QW_ERANGE);
-        } else {
-            const float4 r = __ldcg((const float4*)(p.R + qb * D + k0));
-            const float4 o = sum_shards(p.oacc + qb * NSH * D, k0);
-            const float4 d = sum_shards(p.dacc + qb * NSH * D, k0);
-            x[0] = r.x + o.x + d.x; x[1] = r.y + o.y + d.y; x[2] = r.z + o.z + d.z; x[3] = r.w + o.w + d.w;
-        }
-        if (own) *(float4*)(p.R + pb * D + k0) = make_float4(x[0], x[1], x[2], x[3]);
-        norm_into_h(sm, x, k0, L.in_norm, p.eps, tid);
-        if (tid == 0) stamp(p, l, 10);
-        ok = cs.dot_rows(w.q1 - w.q0, ok, &p, l, 16);
-        if (tid == 0) stamp(p, l, 11);
-        bar_consumers();
-        for (int r = tid; r < w.q1 - w.q0; r += 256) p.qkv[w.q0 + r] = sm.res[r];
-        bar_consumers();
-        if (tid == 0) {
-            // rows of KV-head group g: q rows [256g, 256g+256), k rows 2048 + [128g, ..), v rows 3072 + [128g, ..)
-            for (int g = 0; g < HKV; ++g) {
-                int n = 0;
-                const int ranges[3][2] = {{256 * g, 256 * g + 256}, {2048 + 128 * g, 2048 + 128 * g + 128},
-                                          {3072 + 128 * g, 3072 + 128 * g + 128}};
-                for (int t = 0; t < 3; ++t) n += max(0, min(w.q1, ranges[t][1]) - max(w.q0, ranges[t][0]));
-                if (n) signal_add(c_qkvh(p, l, g), (unsigned)n);
-            }
-            stamp(p, l, 2);
-        }
-        // ---------------- P2: attention split
-        if (w.g >= 0) {
-            const int g = w.g;
-            if (tid == 0) {
-                s_ok = ok && wait_count(c_qkvh(p, l, g), epoch * 512, sm, p.err);
-                stamp(p, l, 3);
+        // this layer's small vectors, loaded before the waits so their latency hides behind them
+        const LayerPtrs L = p.layers[l];
+        const float4 w_in = __ldg((const float4*)(L.in_norm + k0));
+        const float4 w_post = __ldg((const float4*)(L.post_norm + k0));
+        float w_qk[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w_qk[i] = __ldg((cw < 2 ? L.q_norm : L.k_norm) + lane + 32 * i);
+        const int pb = l & 1;
+        const uint32_t par = (uint32_t)(l & 1);
+        const bool more = l + 1 < p.n_layers;
+        // ---------------- layer input: x = x_mid of the previous layer + its cluster slots
+        if (tid == 0) stamp(p, l, 0);
+        if (l > 0) {
+            if (cw == 0) {
+                const bool good = ok && wait_counters(p, c_x(p, l - 1, 0), NC, epoch * CL, sm);
+                if (lane == 0) sm.s_ok_x = good;
             }
             bar_consumers();
-            ok = s_ok;
+            ok = sm.s_ok_x;
+            xa[0] = xm[0]; xa[1] = xm[1]; xa[2] = xm[2]; xa[3] = xm[3];
+            add_slots(xa, p.dslot + (size_t)(pb ^ 1) * MAX_CLUSTERS * D, NC, k0);
+        }
+        if (tid == 0) stamp(p, l, 1);
+        if (w.attn) {
+            // ---------------- A1: norm -> this CTA's q|k|v rows -> every peer's qkv_s
+            norm_into_h(sm, xa, k0, w_in, p.eps, tid);
+            ok = cs.dot_rows(QROWS, ok);
+            if (tid == 0) stamp(p, l, 2);
+            bar_consumers();
+            if (ok && tid < 16 * CL) {
+                const int dst = tid >> 4, q4 = tid & 15;
+                push4(peer_addr(&sm.qkv_s[QROWS * r + 4 * q4], dst), *(const float4*)&sm.res[4 * q4],
+                      peer_addr(&sm.bar_qkv, dst));
+            }
+            ok = ok && wait_cluster(p, &sm.bar_qkv, par, sm);
+            if (tid == 0) {
+                if (ok && more) mbar_arrive_expect_tx(&sm.bar_qkv, QKV_BYTES);   // next layer's phase
+                stamp(p, l, 3);
+            }
+            // ---------------- A2: QK-Norm, RoPE, cache write, attention over this CTA's pages
             if (cw < 4 && ok) {
                 // warp 0,1: q heads 2g, 2g+1; warp 2: k head g; warp 3: v head g
-                const int off = cw < 2 ? (2 * g + cw) * HD : (cw == 2 ? 2048 + g * HD : 3072 + g * HD);
                 float y[4];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) y[i] = __ldcg(p.qkv + off + lane + 32 * i);
+                for (int i = 0; i < 4; ++i) y[i] = sm.qkv_s[HD * cw + lane + 32 * i];
                 if (cw < 3) {
                     const float ss = warp_sum(y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3]);
                     const float sc = 1.0f / sqrtf(ss / (float)HD + p.eps);
-                    const float* nw = cw < 2 ? L.q_norm : L.k_norm;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) y[i] = y[i] * sc * nw[lane + 32 * i];
+                    for (int i = 0; i < 4; ++i) y[i] = y[i] * sc * w_qk[i];
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
-                        const float ang = __fmul_rn((float)pos, p.inv_freq[lane + 32 * j]);
+                        const float ang = __fmul_rn((float)pos, j ? invf1 : invf0);
                         float sn, cs_;
                         sincosf(ang, &sn, &cs_);
                         const float a = y[j], b = y[j + 2];
@@ -564,255 +794,212 @@ __global__ void __launch_bounds__(THREADS, 1) fused_decode_kernel(Params p) {
             }
             bar_consumers();
             if (tid == 0) stamp(p, l, 18);
-            // Each stage holds up to 4 pages (64 key slots).  Scores: warp cw takes slots
-            // 8 cw .. 8 cw + 7, one per 4-lane group (kg = lane >> 2); lane dq = lane & 3 of a group
-            // takes the 16-byte chunks u = 4 c' + dq, c' = c ^ (kg & 1), of the key row (the xor
-            // puts the 8 lanes of each shared-memory phase on 8 different bank groups), and publishes exp2(s - m_w) with its warp max m_w and sum
-            // l_w.  P.V: thread (page pi = tid >> 6, dim pair dp = tid & 63) sums the 16 slots of
-            // page pi for both query heads under one running max M shared by all threads, so
-            // the four page partials add up without rescaling at the end.
+            // Each stage holds up to 4 pages (64 key slots); warp cw owns slots 8 cw .. 8 cw + 7 of
+            // every stage and keeps its own running max, sum and weighted values per query head
+            // (flash-decoding within the warp), so the key loop needs no CTA barrier; the 8 warps
+            // merge once after it.  Scores: one key per 4-lane group (kg = lane >> 2); lane
+            // dq = lane & 3 takes the 16-byte chunks u = 4 c' + dq, c' = c ^ (kg & 1), of the key
+            // row (the xor puts the 8 lanes of each shared-memory phase on 8 different bank
+            // groups).  P.V: lane takes dims 4 lane .. 4 lane + 3 of both heads.
             const int kg = lane >> 2, dq = lane & 3;
-            const int vpi = tid >> 6, dp = tid & 63;
-            float Mr[2] = {-INFINITY, -INFINITY}, lq[2] = {0.f, 0.f}, oq[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-            int buf = 0;
-            for (int pg0 = w.pg_lo; pg0 < w.pg_hi; pg0 += PAGES_PER_STAGE, buf ^= 1) {
+            float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
+            float orun[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            for (int pg0 = w.pg_lo; pg0 < w.pg_hi && !bad_pos; pg0 += PAGES_PER_STAGE) {
                 const int n = min(PAGES_PER_STAGE, w.pg_hi - pg0);
                 const uint8_t* st = cs.stage_wait(ok);
-                if (tid == 0 && pg0 == w.pg_lo) {
-                    stamp(p, l, 20);
-                    if (p.trace) p.trace[((size_t)blockIdx.x * (p.n_layers + 1) + l) * TRACE_SLOTS + 22] = clock64();
-                }
-                {
-                    const int pi = cw >> 1, slot = 8 * (cw & 1) + kg;
-                    const int kpos = (pg0 + pi) * QW_PAGE_SIZE + slot;
-                    const bool vis = ok && pi < n && kpos <= pos && sm.spg[cs.slot()][pi] >= 0;
-                    // the new token's key comes from the bf16 copy made above, not the (older) stage
-                    const uint8_t* krow = kpos == pos ? (const uint8_t*)sm.kn_b
-                                                      : st + (pi < n ? pi : 0) * 2 * PAGE_B + slot * HD * 2;
-                    float sc[2] = {0.f, 0.f};
+                const int pi = cw >> 1, slot0 = 8 * (cw & 1);
+                const bool page_ok = ok && pi < n && sm.spg[cs.slot()][pi] >= 0;
+                const int kpos = (pg0 + pi) * QW_PAGE_SIZE + slot0 + kg;
+                const bool vis = page_ok && kpos <= pos;
+                const uint8_t* page = st + (pi < n ? pi : 0) * 2 * PAGE_B;
+                // the new token's key and value come from the bf16 copies made above, not the stage
+                const uint8_t* krow = kpos == pos ? (const uint8_t*)sm.kn_b : page + (slot0 + kg) * HD * 2;
+                float sc[2] = {0.f, 0.f};
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        const int u = 4 * (c ^ (kg & 1)) + dq;
-                        float kf[8];
-                        unpack8(((const uint4*)krow)[u], kf);
-#pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const float4 qa = *(const float4*)sm.q[hh][0][u];
-                            const float4 qb = *(const float4*)sm.q[hh][1][u];
-                            sc[hh] += qa.x * kf[0] + qa.y * kf[1] + qa.z * kf[2] + qa.w * kf[3] + qb.x * kf[4] +
-                                      qb.y * kf[5] + qb.z * kf[6] + qb.w * kf[7];
-                        }
-                    }
+                for (int cc = 0; cc < 4; ++cc) {
+                    const int u = 4 * (cc ^ (kg & 1)) + dq;
+                    float kf[8];
+                    unpack8(((const uint4*)krow)[u], kf);
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
-                        sc[hh] += __shfl_xor_sync(0xffffffffu, sc[hh], 1);
-                        sc[hh] += __shfl_xor_sync(0xffffffffu, sc[hh], 2);
-                        float mw = vis ? sc[hh] : -INFINITY;
-#pragma unroll
-                        for (int o = 4; o < 32; o <<= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
-                        const float pe = vis ? exp2f(sc[hh] - mw) : 0.f;
-                        float lw = pe;
-#pragma unroll
-                        for (int o = 4; o < 32; o <<= 1) lw += __shfl_xor_sync(0xffffffffu, lw, o);
-                        if (dq == 0) sm.pp[buf][hh][8 * cw + kg] = pe;
-                        if (lane == 0) {
-                            sm.am[buf][cw][hh] = mw;
-                            sm.al[buf][cw][hh] = lw;
-                        }
+                        const float4 qa = *(const float4*)sm.q[hh][0][u];
+                        const float4 qb = *(const float4*)sm.q[hh][1][u];
+                        sc[hh] += qa.x * kf[0] + qa.y * kf[1] + qa.z * kf[2] + qa.w * kf[3] + qb.x * kf[4] +
+                                  qb.y * kf[5] + qb.z * kf[6] + qb.w * kf[7];
                     }
                 }
-                bar_consumers();
-                if (tid == 0 && pg0 == w.pg_lo) {
-                    if (p.trace) p.trace[((size_t)blockIdx.x * (p.n_layers + 1) + l) * TRACE_SLOTS + 23] = clock64();
-                    stamp(p, l, 21);
-                }
-                // P.V over page vpi; the buffers of this stage are not rewritten before the
-                // barrier of the next stage, which every thread reaches only after this part.
-                float Ms[2];
+                float pe[2];
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
-                    Ms[hh] = Mr[hh];
+                    sc[hh] += __shfl_xor_sync(0xffffffffu, sc[hh], 1);
+                    sc[hh] += __shfl_xor_sync(0xffffffffu, sc[hh], 2);
+                    float mw = vis ? sc[hh] : -INFINITY;
 #pragma unroll
-                    for (int i = 0; i < NCW; ++i) Ms[hh] = fmaxf(Ms[hh], sm.am[buf][i][hh]);
+                    for (int o = 4; o < 32; o <<= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
+                    const float mnew = fmaxf(mrun[hh], mw);
+                    const float alpha = mrun[hh] == -INFINITY ? 0.f : exp2f(mrun[hh] - mnew);
+                    pe[hh] = vis ? exp2f(sc[hh] - mnew) : 0.f;
+                    float ps = pe[hh];
+#pragma unroll
+                    for (int o = 4; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+                    lrun[hh] = lrun[hh] * alpha + ps;
+                    mrun[hh] = mnew;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) orun[hh][e] *= alpha;
                 }
-                float fa[2], fb[2];
+                if (page_ok) {
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    if (Ms[hh] == -INFINITY) {  // nothing visible yet for this head
-                        fa[hh] = fb[hh] = 0.f;
-                        continue;
+                    for (int k = 0; k < 8; ++k) {
+                        const float p0 = __shfl_sync(0xffffffffu, pe[0], 4 * k);
+                        const float p1 = __shfl_sync(0xffffffffu, pe[1], 4 * k);
+                        if (p0 == 0.f && p1 == 0.f) continue;   // invisible key (warp-uniform)
+                        const int kp = (pg0 + pi) * QW_PAGE_SIZE + slot0 + k;
+                        const uint2 v = kp == pos ? *(const uint2*)((const uint8_t*)sm.vn_b + 8 * lane)
+                                                  : *(const uint2*)(page + PAGE_B + (slot0 + k) * HD * 2 + 8 * lane);
+                        const float v0 = bf16_lo(v.x), v1 = bf16_hi(v.x), v2 = bf16_lo(v.y), v3 = bf16_hi(v.y);
+                        orun[0][0] = fmaf(p0, v0, orun[0][0]);
+                        orun[0][1] = fmaf(p0, v1, orun[0][1]);
+                        orun[0][2] = fmaf(p0, v2, orun[0][2]);
+                        orun[0][3] = fmaf(p0, v3, orun[0][3]);
+                        orun[1][0] = fmaf(p1, v0, orun[1][0]);
+                        orun[1][1] = fmaf(p1, v1, orun[1][1]);
+                        orun[1][2] = fmaf(p1, v2, orun[1][2]);
+                        orun[1][3] = fmaf(p1, v3, orun[1][3]);
                     }
-                    const float ma = sm.am[buf][2 * vpi][hh], mb = sm.am[buf][2 * vpi + 1][hh];
-                    const float alpha = Mr[hh] == -INFINITY ? 0.f : exp2f(Mr[hh] - Ms[hh]);
-                    fa[hh] = ma == -INFINITY ? 0.f : exp2f(ma - Ms[hh]);
-                    fb[hh] = mb == -INFINITY ? 0.f : exp2f(mb - Ms[hh]);
-                    lq[hh] = lq[hh] * alpha + fa[hh] * sm.al[buf][2 * vpi][hh] + fb[hh] * sm.al[buf][2 * vpi + 1][hh];
-                    oq[hh][0] *= alpha;
-                    oq[hh][1] *= alpha;
-                    Mr[hh] = Ms[hh];
-                }
-                if (fa[0] + fb[0] + fa[1] + fb[1] > 0.f) {  // page vpi has a visible key
-                    const uint8_t* vpage = st + vpi * 2 * PAGE_B + PAGE_B + 4 * dp;
-                    const int knew = pos - (pg0 + vpi) * QW_PAGE_SIZE;  // slot of the new token, if here
-                    float s0[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, s1[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-#pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        const float4* pa = (const float4*)&sm.pp[buf][0][16 * vpi + 8 * half];
-                        const float4* pb = (const float4*)&sm.pp[buf][1][16 * vpi + 8 * half];
-                        const float4 pa0 = pa[0], pa1 = pa[1], pb0 = pb[0], pb1 = pb[1];
-                        const float p0[8] = {pa0.x, pa0.y, pa0.z, pa0.w, pa1.x, pa1.y, pa1.z, pa1.w};
-                        const float p1[8] = {pb0.x, pb0.y, pb0.z, pb0.w, pb1.x, pb1.y, pb1.z, pb1.w};
-                        float (&acc)[2][2] = half ? s1 : s0;
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            const int slot = 8 * half + k;
-                            const uint32_t v = slot == knew ? *(const uint32_t*)((const uint8_t*)sm.vn_b + 4 * dp)
-                                                            : *(const uint32_t*)(vpage + slot * HD * 2);
-                            const float v0 = bf16_lo(v), v1 = bf16_hi(v);
-                            acc[0][0] = fmaf(p0[k], v0, acc[0][0]);
-                            acc[0][1] = fmaf(p0[k], v1, acc[0][1]);
-                            acc[1][0] = fmaf(p1[k], v0, acc[1][0]);
-                            acc[1][1] = fmaf(p1[k], v1, acc[1][1]);
-                        }
-                    }
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) oq[hh][e] += fa[hh] * s0[hh][e] + fb[hh] * s1[hh][e];
                 }
                 cs.stage_release();
             }
-            if (tid == 0) stamp(p, l, 19);
+            if (tid == 0) stamp(p, l, 4);
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                *(float2*)&sm.ao[vpi][hh][2 * dp] = make_float2(oq[hh][0], oq[hh][1]);
-                if (dp == 0) sm.alq[vpi][hh] = lq[hh];
+                *(float4*)&sm.wo[cw][hh][4 * lane] = make_float4(orun[hh][0], orun[hh][1], orun[hh][2], orun[hh][3]);
+                if (lane == 0) {
+                    sm.wml[cw][2 * hh] = mrun[hh];
+                    sm.wml[cw][2 * hh + 1] = lrun[hh];
+                }
             }
             bar_consumers();
             {
+                // thread (head hh, dim d): merge of the 8 warps (their maxima differ), then this CTA's
+                // partial; 4 consecutive dims go to their owner peer in one 16-byte push (owner of
+                // group dim 128 hh + d is peer (128 hh + d) / 32)
                 const int hh = tid >> 7, d = tid & 127;
+                float M = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < NCW; ++i)
+                    if (sm.wml[i][2 * hh + 1] > 0.f) M = fmaxf(M, sm.wml[i][2 * hh]);
                 float Ls = 0.f, O = 0.f;
 #pragma unroll
-                for (int i = 0; i < PAGES_PER_STAGE; ++i) {
-                    Ls += sm.alq[i][hh];
-                    O += sm.ao[i][hh][d];
+                for (int i = 0; i < NCW; ++i) {
+                    const float li = sm.wml[i][2 * hh + 1];
+                    const float f = li > 0.f ? exp2f(sm.wml[i][2 * hh] - M) : 0.f;
+                    Ls += f * li;
+                    O += f * sm.wo[i][hh][d];
                 }
-                float* dst = p.part + ((size_t)(2 * g + hh) * p.nsa + w.s) * PART;
-                dst[d] = O;
-                if (d == 0) {
-                    dst[HD] = Mr[hh];
-                    dst[HD + 1] = Ls;
+                const float o1 = __shfl_down_sync(0xffffffffu, O, 1);
+                const float o2 = __shfl_down_sync(0xffffffffu, O, 2);
+                const float o3 = __shfl_down_sync(0xffffffffu, O, 3);
+                if (ok && (d & 3) == 0) {
+                    const int dst = (HD * hh + d) / ODIMS;
+                    push4(peer_addr(&sm.part_o[r][d % ODIMS], dst), make_float4(O, o1, o2, o3),
+                          peer_addr(&sm.bar_part, dst));
                 }
+                if (ok && d < CL)   // (max, sum) of head hh to peer d
+                    push2(peer_addr(&sm.part_ml[r][2 * hh], d), M, Ls, peer_addr(&sm.bar_part, d));
             }
-            bar_consumers();
+            ok = ok && wait_cluster(p, &sm.bar_part, par, sm);
             if (tid == 0) {
-                signal_add(c_split(p, l, g), 1u);
-                stamp(p, l, 4);
-            }
-        }
-        // ---------------- P3: merge splits of this CTA's attention dims, o_proj rows of Wo^T
-        {
-            const int nj = w.j1 - w.j0;
-            if (tid == 0) {
-                bool good = ok;
-                const int g_lo = w.j0 / (2 * HD), g_hi = (w.j1 - 1) / (2 * HD);
-                for (int g = g_lo; g <= g_hi && good; ++g) good = wait_count(c_split(p, l, g), epoch * p.nsa, sm, p.err);
-                s_ok = good;
+                if (ok && more) mbar_arrive_expect_tx(&sm.bar_part, PART_BYTES);   // next layer's phase
                 stamp(p, l, 5);
             }
-            bar_consumers();
-            ok = s_ok;
-            if (ok) {
-                // at most two dims per warp: issue all loads before the reductions
-                float ms[2], ls[2], os[2];
+            // ---------------- A3: merge my 32 dims, o_proj rows of Wo^T, cluster reduction
+            if (cw == 0) {
+                const int hh = r / 4;   // my dims are 32 (r % 4) .. + 31 of head 2g + hh
+                float M = -INFINITY;
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int jj = cw + NCW * k;
-                    ms[k] = -INFINITY;
-                    ls[k] = os[k] = 0.f;
-                    if (jj < nj && lane < p.nsa) {
-                        const int j = w.j0 + jj;
-                        const float* base = p.part + ((size_t)(j / HD) * p.nsa + lane) * PART;
-                        ms[k] = __ldcg(base + HD);
-                        ls[k] = __ldcg(base + HD + 1);
-                        os[k] = __ldcg(base + j % HD);
-                    }
-                }
+                for (int s = 0; s < CL; ++s)
+                    if (sm.part_ml[s][2 * hh + 1] > 0.f) M = fmaxf(M, sm.part_ml[s][2 * hh]);
+                float Lt = 0.f, Ot = 0.f;
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int jj = cw + NCW * k;
-                    const float M = warp_max(ls[k] > 0.f ? ms[k] : -INFINITY);
-                    const float f = ls[k] > 0.f ? exp2f(ms[k] - M) : 0.f;
-                    const float Lt = warp_sum(ls[k] * f), Ot = warp_sum(os[k] * f);
-                    if (lane == 0 && jj < nj) sm.coef[jj] = Lt > 0.f ? Ot / Lt : 0.f;
+                for (int s = 0; s < CL; ++s) {
+                    const float Ls = sm.part_ml[s][2 * hh + 1];
+                    const float f = Ls > 0.f ? exp2f(sm.part_ml[s][2 * hh] - M) : 0.f;
+                    Lt += f * Ls;
+                    Ot += f * sm.part_o[s][lane];
                 }
+                sm.coef[lane] = Lt > 0.f ? Ot / Lt : 0.f;
             }
             bar_consumers();
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            if (tid == 0) stamp(p, l, 15);
-            ok = cs.scaled_rows(nj, acc, ok);
-            add_columns(acc, p.oacc + (pb * NSH + c % NSH) * D, cw, lane);
-            bar_consumers();
+            ok = cs.scaled_rows(ODIMS, acc, ok);
+            if (tid == 0) stamp(p, l, 6);
+            if (ok) push_partial(sm, sm.red_o, &sm.bar_redo, acc, cw, lane, r);
+            ok = ok && wait_cluster(p, &sm.bar_redo, par, sm);
             if (tid == 0) {
-                signal_add(c_o(p, l), 1u);
-                stamp(p, l, 6);
-            }
-        }
-        // ---------------- P4: norm -> gate/up -> SwiGLU -> down_proj rows of Wd^T
-        {
-            if (tid == 0) {
-                s_ok = ok && wait_count(c_o(p, l), epoch * G, sm, p.err);
+                if (ok && more) mbar_arrive_expect_tx(&sm.bar_redo, RED_BYTES);   // next layer's phase
                 stamp(p, l, 7);
             }
-            bar_consumers();
-            ok = s_ok;
-            const float4 r = __ldcg((const float4*)(p.R + pb * D + k0));
-            const float4 oa = sum_shards(p.oacc + pb * NSH * D, k0);
-            float xm[4] = {r.x + oa.x, r.y + oa.y, r.z + oa.z, r.w + oa.w};
-            if (own && l > 0) {  // every reader of the previous layer's accumulators is done
-#pragma unroll
-                for (int sh = 0; sh < NSH; ++sh) {
-                    *(float4*)(p.oacc + (qb * NSH + sh) * D + k0) = make_float4(0.f, 0.f, 0.f, 0.f);
-                    *(float4*)(p.dacc + (qb * NSH + sh) * D + k0) = make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            }
-            norm_into_h(sm, xm, k0, L.post_norm, p.eps, tid);
-            if (tid == 0) stamp(p, l, 12);
-            const int np2 = w.p1 - w.p0;
-            ok = cs.dot_rows(2 * np2, ok, &p, l, 17);
-            if (tid == 0) stamp(p, l, 13);
-            bar_consumers();
-            for (int j = tid; j < np2; j += 256) {
-                const float gt = sm.res[2 * j], up = sm.res[2 * j + 1];
-                sm.coef[j] = gt / (1.0f + expf(-gt)) * up;
-            }
-            bar_consumers();
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            ok = cs.scaled_rows(np2, acc, ok);
-            if (tid == 0) stamp(p, l, 14);
-            add_columns(acc, p.dacc + (pb * NSH + c % NSH) * D, cw, lane);
+            if (ok) store_reduced(sm.red_o, p.oslot + ((size_t)pb * HKV + g) * D, r, tid);
             bar_consumers();
             if (tid == 0) {
-                signal_add(c_x(p, l), 1u);
+                signal_add(c_o(p, l, g), 1u);
                 stamp(p, l, 8);
             }
+        }
+        // ---------------- M1: x + group slots -> norm -> gate/up -> SwiGLU -> down rows -> cluster slot
+        if (tid == 0) stamp(p, l, 9);
+        if (cw == 0) {
+            const bool good = ok && wait_counters(p, c_o(p, l, 0), HKV, epoch * CL + (l == 0 ? p.fault_extra : 0u), sm);
+            if (lane == 0) sm.s_ok_o = good;
+        }
+        bar_consumers();
+        ok = sm.s_ok_o;
+        xm[0] = xa[0]; xm[1] = xa[1]; xm[2] = xa[2]; xm[3] = xa[3];
+        add_slots(xm, p.oslot + (size_t)pb * HKV * D, HKV, k0);
+        if (tid == 0) stamp(p, l, 10);
+        norm_into_h(sm, xm, k0, w_post, p.eps, tid);
+        if (tid == 0) stamp(p, l, 17);
+        const int np2 = w.p1 - w.p0;
+        ok = cs.dot_rows(2 * np2, ok);
+        if (tid == 0) stamp(p, l, 11);
+        bar_consumers();
+        for (int j = tid; j < np2; j += 256) {
+            const float gt = sm.res[2 * j], up = sm.res[2 * j + 1];
+            sm.coef[j] = gt / (1.0f + expf(-gt)) * up;
+        }
+        bar_consumers();
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        ok = cs.scaled_rows(np2, acc, ok);
+        if (tid == 0) stamp(p, l, 12);
+        if (ok) push_partial(sm, sm.red_d, &sm.bar_redd, acc, cw, lane, r);
+        ok = ok && wait_cluster(p, &sm.bar_redd, par, sm);
+        if (tid == 0) {
+            if (ok && more) mbar_arrive_expect_tx(&sm.bar_redd, RED_BYTES);   // next layer's phase
+            stamp(p, l, 13);
+        }
+        if (ok) store_reduced(sm.red_d, p.dslot + ((size_t)pb * MAX_CLUSTERS + w.cid) * D, r, tid);
+        bar_consumers();
+        if (tid == 0) {
+            signal_add(c_x(p, l, w.cid), 1u);
+            stamp(p, l, 14);
+
         }
     }
     // ---------------- LM head: final norm, tied embedding rows, argmax
     {
         const int pl = (p.n_layers - 1) & 1;
-        if (tid == 0) {
-            stamp(p, p.n_layers, 0);
-            s_ok = ok && wait_count(c_x(p, p.n_layers - 1), epoch * G, sm, p.err);
-            stamp(p, p.n_layers, 1);
+        const float4 w_fin = __ldg((const float4*)(p.final_norm + k0));
+        if (tid == 0) stamp(p, p.n_layers, 0);
+        if (cw == 0) {
+            const bool good = ok && wait_counters(p, c_x(p, p.n_layers - 1, 0), NC, epoch * CL, sm);
+            if (lane == 0) sm.s_ok_x = good;
         }
         bar_consumers();
-        ok = s_ok;
-        const float4 r = __ldcg((const float4*)(p.R + pl * D + k0));
-        const float4 oa = sum_shards(p.oacc + pl * NSH * D, k0);
-        const float4 da = sum_shards(p.dacc + pl * NSH * D, k0);
-        float xf[4] = {r.x + oa.x + da.x, r.y + oa.y + da.y, r.z + oa.z + da.z, r.w + oa.w + da.w};
-        norm_into_h(sm, xf, k0, p.final_norm, p.eps, tid);
+        ok = sm.s_ok_x;
+        if (tid == 0) stamp(p, p.n_layers, 1);
+        float xf[4] = {xm[0], xm[1], xm[2], xm[3]};
+        add_slots(xf, p.dslot + (size_t)pl * MAX_CLUSTERS * D, NC, k0);
+        norm_into_h(sm, xf, k0, w_fin, p.eps, tid);
         float hreg[4][8];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -862,9 +1049,8 @@ __global__ void __launch_bounds__(THREADS, 1) fused_decode_kernel(Params p) {
             p.lm_part[2 * c + 1] = __int_as_float(bidx);
             unsigned prev;
             asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(c_lm(p)) : "memory");
-            sm.last_cta = prev == epoch * G - 1;
-            if (sm.last_cta) {
-                // last CTA: global argmax (lowest id on ties); below, reset the accumulators, next epoch
+            if (prev == epoch * G - 1) {
+                // last CTA: global argmax (lowest id on ties), then the next step's epoch
                 __threadfence();
                 float bv = -INFINITY;
                 int bi = 0x7FFFFFFF;
@@ -877,18 +1063,11 @@ __global__ void __launch_bounds__(THREADS, 1) fused_decode_kernel(Params p) {
                     }
                 }
                 *p.argmax = bi;
+                signal_add(c_epoch(p), 1u);
             }
-        }
-        bar_consumers();
-        if (sm.last_cta) {  // every CTA has read the last layer's accumulators
-            for (int k = tid; k < NSH * D; k += 256) {
-                p.oacc[pl * NSH * D + k] = 0.f;
-                p.dacc[pl * NSH * D + k] = 0.f;
-            }
-            bar_consumers();
-            if (tid == 0) signal_add(c_epoch(p), 1u);
         }
     }
+    cluster_sync_all();   // no peer pushes into this CTA's shared memory after it exits
 }
 
 // Wt[j][i] = W[i][j] for a [rows][cols] bf16 matrix.
@@ -910,46 +1089,49 @@ __global__ void transpose_bf16_kernel(const uint16_t* __restrict__ W, uint16_t* 
 
 // ---------------------------------------------------------------- host side
 struct FusedDecode {
-    int G = 0, nsa = 0, n_layers = 0, V = 0;
+    int G = 0, n_clusters = 0, n_layers = 0, V = 0;
     float eps = 0.f;
     uint8_t* buf = nullptr;
     fused::LayerPtrs* d_layers = nullptr;
     const uint16_t* E = nullptr;
     const float* final_norm = nullptr;
     const float* inv_freq = nullptr;
-    float *R = nullptr, *oacc = nullptr, *dacc = nullptr, *qkv = nullptr, *part = nullptr, *lm_part = nullptr;
+    float *oslot = nullptr, *dslot = nullptr, *lm_part = nullptr;
     int* argmax = nullptr;
     unsigned* sync = nullptr;
+    size_t state_bytes = 0;   // bytes from oslot through the counters (cleared by fused_reset)
     unsigned long long* trace = nullptr;
     bool trace_on = false;
+    bool fault_armed = false;   // the next launch waits for an arrival that never comes (test hook)
 };
 
 FusedDecode* fused_create(const FusedWeights& fw, int n_layers, int V, float eps, int hidden, int n_heads,
                           int n_kv_heads, int intermediate) {
     using namespace fused;
     if (hidden != D || n_heads != HQ || n_kv_heads != HKV || intermediate != INTER || n_layers > MAX_LAYERS) return nullptr;
-    int dev = 0, n_sm = 0, coop = 0;
+    int dev = 0, coop = 0;
     cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
     cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-    if (!coop || n_sm < HKV) return nullptr;
+    if (!coop) return nullptr;
     if (cudaFuncSetAttribute(fused_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
         cudaSuccess)
         return nullptr;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_decode_kernel, THREADS, SMEM_BYTES) !=
-            cudaSuccess ||
-        per_sm < 1)
-        return nullptr;
-    FusedDecode* f = new FusedDecode();
-    f->G = n_sm;
-    f->nsa = n_sm / HKV;
-    if (f->nsa > 32) f->nsa = 32;   // the split merge reads one split per lane
-    if ((QKVR + f->G - 1) / f->G > MAX_ROWS || (2 * (INTER + f->G - 1) / f->G) > MAX_ROWS ||
-        (AD + f->G - 1) / f->G > 2 * NCW) {  // the split merge takes at most two dims per warp
-        delete f;
-        return nullptr;
+    // as many clusters of 8 as can be resident at once (15 on a 152-SM GB300); 8 own the KV groups
+    int max_clusters = 0;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(CL);
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = SMEM_BYTES;
+        if (cudaOccupancyMaxActiveClusters(&max_clusters, fused_decode_kernel, &cfg) != cudaSuccess) return nullptr;
     }
+    const int nc = max_clusters < MAX_CLUSTERS ? max_clusters : MAX_CLUSTERS;
+    if (nc < HKV) return nullptr;
+    const int G = CL * nc;
+    if (2 * ((INTER + G - 1) / G) > MAX_ROWS) return nullptr;
+    FusedDecode* f = new FusedDecode();
+    f->G = G;
+    f->n_clusters = nc;
     f->n_layers = n_layers;
     f->V = V;
     f->eps = eps;
@@ -965,11 +1147,10 @@ FusedDecode* fused_create(const FusedWeights& fw, int n_layers, int V, float eps
     };
     const size_t o_w = take((woT + wdT) * 2 * n_layers);
     const size_t o_layers = take(sizeof(LayerPtrs) * n_layers);
-    const size_t o_state = take(sizeof(float) * (2 * D + 4 * NSH * D + QKVR));
-    const size_t o_part = take(sizeof(float) * HQ * f->nsa * PART);
-    const size_t o_lm = take(sizeof(float) * 2 * f->G + 64);
-    const size_t o_sync = take(sizeof(unsigned) * CNT_STRIDE * (2 + n_layers * 18));
-    const size_t o_trace = take(sizeof(unsigned long long) * f->G * (n_layers + 1) * TRACE_SLOTS);
+    const size_t o_state = take(sizeof(float) * 2 * (HKV + MAX_CLUSTERS) * D);
+    const size_t o_lm = take(sizeof(float) * 2 * G + 64);
+    const size_t o_sync = take(sizeof(unsigned) * CNT_STRIDE * (3 + n_layers * CNT_PER_LAYER));
+    const size_t o_trace = take(sizeof(unsigned long long) * G * (n_layers + 1) * TRACE_SLOTS);
     if (cudaMalloc(&f->buf, off) != cudaSuccess) {
         delete f;
         return nullptr;
@@ -985,15 +1166,12 @@ FusedDecode* fused_create(const FusedWeights& fw, int n_layers, int V, float eps
                           fw.k_norm[l]};
     }
     f->d_layers = (LayerPtrs*)(f->buf + o_layers);
-    float* st = (float*)(f->buf + o_state);
-    f->R = st;
-    f->oacc = st + 2 * D;
-    f->dacc = st + 2 * D + 2 * NSH * D;
-    f->qkv = st + 2 * D + 4 * NSH * D;
-    f->part = (float*)(f->buf + o_part);
+    f->oslot = (float*)(f->buf + o_state);
+    f->dslot = f->oslot + 2 * HKV * D;
     f->lm_part = (float*)(f->buf + o_lm);
-    f->argmax = (int*)(f->lm_part + 2 * f->G);
+    f->argmax = (int*)(f->lm_part + 2 * G);
     f->sync = (unsigned*)(f->buf + o_sync);
+    f->state_bytes = o_trace - o_state;
     f->trace = (unsigned long long*)(f->buf + o_trace);
     if (cudaMemcpy(f->d_layers, lp.data(), sizeof(LayerPtrs) * n_layers, cudaMemcpyHostToDevice) != cudaSuccess ||
         cudaMemset(f->buf + o_state, 0, off - o_state) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
@@ -1004,13 +1182,13 @@ FusedDecode* fused_create(const FusedWeights& fw, int n_layers, int V, float eps
     return f;
 }
 
-bool fused_supported(const FusedDecode* f, int batch) { return f != nullptr && batch == 1; }
+bool fused_supported(const FusedDecode* f, int batch, int bt_stride) {
+    return f != nullptr && batch == 1 && bt_stride <= fused::CL * fused::MAX_PAGES - fused::CL;
+}
 
 int fused_reset(FusedDecode* f, cudaStream_t st) {
-    // after a timeout the counters and accumulators are in an unknown state
-    const size_t bytes = (size_t)((uint8_t*)f->sync - (uint8_t*)f->R) +
-                         sizeof(unsigned) * fused::CNT_STRIDE * (2 + f->n_layers * 18);
-    return cudaMemsetAsync(f->R, 0, bytes, st) == cudaSuccess ? QW_OK : QW_ECUDA;
+    // after a timeout the counters and slots are in an unknown state
+    return cudaMemsetAsync(f->oslot, 0, f->state_bytes, st) == cudaSuccess ? QW_OK : QW_ECUDA;
 }
 
 int fused_decode(FusedDecode* f, const int* tokens, const int* positions, int batch, uint16_t* kv_base,
@@ -1035,25 +1213,39 @@ int fused_decode(FusedDecode* f, const int* tokens, const int* positions, int ba
     p.page_elems = page_elems;
     p.n_pages = n_pages;
     p.logits = logits;
-    p.R = f->R;
-    p.oacc = f->oacc;
-    p.dacc = f->dacc;
-    p.qkv = f->qkv;
-    p.part = f->part;
+    p.oslot = f->oslot;
+    p.dslot = f->dslot;
     p.lm_part = f->lm_part;
     p.argmax = f->argmax;
     p.sync = f->sync;
     p.err = err;
-    p.nsa = f->nsa;
+    p.n_clusters = f->n_clusters;
     p.trace = f->trace_on ? f->trace : nullptr;
-    void* args[] = {&p};
-    cudaError_t e = cudaLaunchCooperativeKernel((const void*)fused_decode_kernel, dim3(f->G), dim3(THREADS), args,
-                                                SMEM_BYTES, st);
+    p.wait_ns = f->fault_armed ? FAULT_WAIT_NS : WAIT_NS;
+    p.fault_extra = f->fault_armed ? 1u : 0u;
+    f->fault_armed = false;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeCooperative;   // every CTA resident at once: the counters are waited on
+    at[0].val.cooperative = 1;
+    cfg.gridDim = dim3(f->G);
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cfg.stream = st;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_decode_kernel, p);
     count_launches(1);
     return e == cudaSuccess ? QW_OK : QW_ECUDA;
 }
 
 const int* fused_argmax(const FusedDecode* f) { return f ? f->argmax : nullptr; }
+
+int fused_inject_timeout(FusedDecode* f) {
+    if (!f) return QW_EINVAL;
+    f->fault_armed = true;
+    return QW_OK;
+}
 
 int fused_trace(FusedDecode* f, int enable, uint64_t* host_out, int64_t n, int64_t* n_needed) {
     if (!f) return QW_EINVAL;

@@ -21,12 +21,16 @@ struct FusedWeights {
 // nullptr when the shape or the device does not fit the fused kernel.
 FusedDecode* fused_create(const FusedWeights& w, int n_layers, int V, float eps, int hidden, int n_heads,
                           int n_kv_heads, int intermediate);
-bool fused_supported(const FusedDecode* f, int batch);
+// The fused kernel takes batch 1 with block tables of at most 4088 pages (65408 positions).
+bool fused_supported(const FusedDecode* f, int batch, int bt_stride);
 int fused_decode(FusedDecode* f, const int* tokens, const int* positions, int batch, uint16_t* kv_base,
                  int64_t layer_elems, int64_t page_elems, int n_pages, const int* block_tables, int bt_stride,
                  float* logits, int* err, cudaStream_t st);
 // Clear the step counters and accumulators (after a device error left them mid-step).
 int fused_reset(FusedDecode* f, cudaStream_t st);
+// Test hook: the next fused step waits at one place for an arrival that never comes, with a
+// 2 ms limit, so that step ends in QW_ETIMEOUT (reported by qw_check) without a device fault.
+int fused_inject_timeout(FusedDecode* f);
 // Device int holding the argmax of the last fused step's logits.
 const int* fused_argmax(const FusedDecode* f);
 // Phase timestamps of the following fused steps (enable), copied out to host_out.

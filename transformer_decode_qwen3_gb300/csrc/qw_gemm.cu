@@ -435,6 +435,11 @@ __global__ void __launch_bounds__(256, 1)
                     __syncwarp();
                 }
             }
+            // LM head (fp32 store with ep.tile_max): this row's maximum over the tile and its
+            // lowest column, the partial the sampler's argmax and softmax start from
+            float tmax = -INFINITY;
+            int targ = n0;
+            const int mrow = SPLIT ? tm * 64 + ew * 32 + lane : tm * C::BM + et;
 #pragma unroll 1
             for (int c0 = 0; c0 < BN && EPI != EPI_QKV_ROPE && !(EPI == EPI_RESID_ADD && !SPLIT); c0 += 32) {
                 if (n0 + c0 >= N) break;  // uniform over the warpgroup
@@ -449,15 +454,23 @@ __global__ void __launch_bounds__(256, 1)
                     if (ew < 2) {
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] += xch[(ew * 32 + lane) * 33 + i];
-                        const int m = tm * 64 + ew * 32 + lane;
-                        if (m < M) epilogue_chunk<BN, EPI>(v, m, n0 + c0, ep);
+                        if (mrow < M) epilogue_chunk<BN, EPI>(v, mrow, n0 + c0, ep);
                     }
                     epi_bar();
                 } else {
-                    const int m = tm * C::BM + et;
-                    if (m < M) epilogue_chunk<BN, EPI>(v, m, n0 + c0, ep);
+                    if (mrow < M) epilogue_chunk<BN, EPI>(v, mrow, n0 + c0, ep);
+                }
+                if (EPI == EPI_STORE_F32 && ep.tile_max) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        if (n0 + c0 + i < N && v[i] > tmax) {
+                            tmax = v[i];
+                            targ = n0 + c0 + i;
+                        }
                 }
             }
+            if (EPI == EPI_STORE_F32 && ep.tile_max && (!SPLIT || ew < 2) && mrow < M)
+                ep.tile_max[(size_t)mrow * ep.tile_ld + tn] = make_float2(tmax, __int_as_float(targ));
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);

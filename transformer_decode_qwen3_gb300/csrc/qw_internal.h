@@ -48,6 +48,8 @@ struct GemmEpilogue {
     int* err;        // device error word
     int split;       // A holds hi/lo row pairs (see split_rows); SwiGLU output is written the same way
     QkvRope rope;    // EPI_QKV_ROPE only
+    float2* tile_max = nullptr;  // EPI_STORE_F32 (nullable): [m][tile_ld] (max, argmax as int bits) per BN-column tile
+    int tile_ld = 0;
 };
 
 // Rows an M-row activation occupies in the split (hi/lo) layout.
@@ -86,10 +88,12 @@ int launch_attn_prefill_tc(const uint16_t* q_bf16, int n_tok, const int* positio
                            int Hq, int Hkv, const KvView& kv, uint16_t* out, int split, int* err, cudaStream_t st);
 int launch_attn_decode(const float* q, const int* positions, int batch, int Hq, int Hkv, const KvView& kv,
                        float* part, int max_splits, uint16_t* out, int split, int* err, int n_sm, cudaStream_t st);
-// argmax_hint (nullable, batch 1): the argmax of the logits row, already computed by the
-// fused decode; greedy rows then skip the scan.
+// tile_part (nullable): [batch][n_part] per-tile (max, argmax) of the logits rows, left by the
+// LM-head projection; argmax_hint (nullable, batch 1): the argmax of the logits row, already
+// computed by the fused decode.  Greedy rows then skip the scan.
 int launch_sample(const float* logits, int batch, int vocab, const qw_sample_params* params, uint64_t rng_counter,
-                  int32_t* out_ids, const int* argmax_hint, int* err, cudaStream_t st);
+                  int32_t* out_ids, const float2* tile_part, int n_part, const int* argmax_hint, int* err,
+                  cudaStream_t st);
 int launch_bf16_to_f32(const uint16_t* src, float* dst, int n, cudaStream_t st);
 
 }  // namespace qw

@@ -624,182 +624,6 @@ int launch_attn_decode(const float* q, const int* positions, int batch, int Hq, 
     return check_launch();
 }
 
-// ---------------------------------------------------------------- Step 8: sample()
-// One 1024-thread CTA per row.  Greedy rows: argmax (lowest id on ties).  Sampling
-// rows: m = max, Z = sum exp((l - m) / T); a 4-pass radix select finds the top_k
-// largest logits, which are sorted (value descending, id ascending); their
-// probabilities are prefix-summed, the cutoff min(top_k, 1 + #(cumsum < top_p))
-// applied, and the first kept entry with cumsum > u * (kept mass) returned, u from
-// Philox4x32-10 (key = seed, counter = (rng_counter, 0, 0)).
-constexpr int SMP_THREADS = 1024;
-constexpr int SMP_CAND = 2048;
-
-QW_DEV uint32_t order_key(float v) {
-    const uint32_t u = __float_as_uint(v);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-template <typename T, typename Op>
-QW_DEV T block_reduce(T v, Op op, T* scratch) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
-    __syncthreads();
-    if (lane == 0) scratch[warp] = v;
-    __syncthreads();
-    v = scratch[lane < (int)(blockDim.x >> 5) ? lane : 0];
-    if (warp == 0) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
-        if (lane == 0) scratch[0] = v;
-    }
-    __syncthreads();
-    v = scratch[0];
-    __syncthreads();
-    return v;
-}
-
-__global__ void __launch_bounds__(SMP_THREADS) sample_kernel(const float* __restrict__ logits, int vocab,
-                                                             const qw_sample_params* __restrict__ params,
-                                                             uint64_t rng_counter, int32_t* __restrict__ out,
-                                                             const int* __restrict__ argmax_hint, int* err) {
-    const int row = blockIdx.x, tid = threadIdx.x;
-    const float* lg = logits + (size_t)row * vocab;
-    const qw_sample_params P = params[row];
-    __shared__ float s_f[32];
-    __shared__ unsigned long long s_u[32];
-    __shared__ int s_i[32];
-    __shared__ unsigned long long cand[SMP_CAND];
-    __shared__ uint32_t hist[256];
-    __shared__ uint32_t s_sel, s_rem, s_ncand;
-    __shared__ float cum[SMP_THREADS];
-
-    if (!(P.temperature > 0.f) && argmax_hint) {
-        if (tid == 0) out[row] = argmax_hint[row];
-        return;
-    }
-    if (!(P.temperature > 0.f)) {
-        // greedy: pack (order key, ~index) so one max reduction picks the lowest id among equal maxima
-        unsigned long long best = 0ull;
-        for (int j = tid; j < vocab; j += SMP_THREADS) {
-            const unsigned long long k =
-                ((unsigned long long)order_key(lg[j]) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)j);
-            best = k > best ? k : best;
-        }
-        best = block_reduce(best, [](unsigned long long a, unsigned long long b) { return a > b ? a : b; }, s_u);
-        if (tid == 0) out[row] = (int32_t)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
-        return;
-    }
-    int k = P.top_k;
-    float top_p = P.top_p;
-    if (k < 1 || k > QW_MAX_TOP_K || !(top_p > 0.f) || top_p > 1.f) {
-        if (tid == 0) set_error(err, QW_EINVAL);
-        k = min(max(k, 1), QW_MAX_TOP_K);
-        top_p = fminf(fmaxf(top_p, 1e-6f), 1.f);
-    }
-    k = min(k, vocab);
-    const float invT = 1.0f / P.temperature;
-    float mx = -INFINITY;
-    for (int j = tid; j < vocab; j += SMP_THREADS) mx = fmaxf(mx, lg[j]);
-    mx = block_reduce(mx, [](float a, float b) { return fmaxf(a, b); }, s_f);
-    float z = 0.f;
-    for (int j = tid; j < vocab; j += SMP_THREADS) z += expf((lg[j] - mx) * invT);
-    z = block_reduce(z, [](float a, float b) { return a + b; }, s_f);
-
-    // radix select: the k-th largest order key
-    uint32_t prefix = 0, pmask = 0;
-    if (tid == 0) s_rem = (uint32_t)k;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += SMP_THREADS) hist[i] = 0;
-        __syncthreads();
-        for (int j = tid; j < vocab; j += SMP_THREADS) {
-            const uint32_t u = order_key(lg[j]);
-            if ((u & pmask) == prefix) atomicAdd(&hist[(u >> shift) & 255u], 1u);
-        }
-        __syncthreads();
-        if (tid == 0) {
-            uint32_t c = 0, rem = s_rem;
-            int bsel = 0;
-            for (int bk = 255; bk >= 0; --bk) {
-                if (c + hist[bk] >= rem) {
-                    bsel = bk;
-                    break;
-                }
-                c += hist[bk];
-            }
-            s_sel = (uint32_t)bsel;
-            s_rem = rem - c;
-        }
-        __syncthreads();
-        prefix |= s_sel << shift;
-        pmask |= 255u << shift;
-    }
-    // collect every logit with key >= threshold
-    if (tid == 0) s_ncand = 0;
-    for (int i = tid; i < SMP_CAND; i += SMP_THREADS) cand[i] = 0ull;
-    __syncthreads();
-    for (int j = tid; j < vocab; j += SMP_THREADS) {
-        const uint32_t u = order_key(lg[j]);
-        if (u >= prefix) {
-            const uint32_t slot = atomicAdd(&s_ncand, 1u);
-            if (slot < SMP_CAND)
-                cand[slot] = ((unsigned long long)u << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)j);
-        }
-    }
-    __syncthreads();
-    if (tid == 0 && s_ncand > SMP_CAND) set_error(err, QW_EINVAL);
-    // bitonic sort, descending
-    for (int size = 2; size <= SMP_CAND; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int i = tid; i < SMP_CAND; i += SMP_THREADS) {
-                const int jx = i ^ stride;
-                if (jx > i) {
-                    const bool desc = (i & size) == 0;
-                    const unsigned long long a = cand[i], c = cand[jx];
-                    if (desc ? (a < c) : (a > c)) {
-                        cand[i] = c;
-                        cand[jx] = a;
-                    }
-                }
-            }
-            __syncthreads();
-        }
-    }
-    // probabilities of the k best in order, inclusive prefix sum
-    float p = 0.f;
-    if (tid < k) {
-        const uint32_t u = (uint32_t)(cand[tid] >> 32);
-        const uint32_t bits = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
-        p = expf((__uint_as_float(bits) - mx) * invT) / z;
-    }
-    cum[tid] = p;
-    __syncthreads();
-    for (int off = 1; off < SMP_THREADS; off <<= 1) {
-        const float add = tid >= off ? cum[tid - off] : 0.f;
-        __syncthreads();
-        cum[tid] += add;
-        __syncthreads();
-    }
-    // cutoff = min(k, 1 + #(cum < top_p))
-    int below = (tid < k && cum[tid] < top_p) ? 1 : 0;
-    below = block_reduce(below, [](int a, int b) { return a + b; }, s_i);
-    const int cutoff = min(k, below + 1);
-    uint32_t c4[4] = {(uint32_t)rng_counter, (uint32_t)(rng_counter >> 32), 0u, 0u};
-    philox4x32_10(c4, (uint32_t)P.seed, (uint32_t)(P.seed >> 32));
-    const float u = (float)(c4[0] >> 8) * (1.0f / 16777216.0f);
-    const float target = u * cum[cutoff - 1];
-    int first = (tid < cutoff && cum[tid] > target) ? tid : cutoff - 1;
-    first = block_reduce(first, [](int a, int b) { return a < b ? a : b; }, s_i);
-    if (tid == 0) out[row] = (int32_t)(0xFFFFFFFFu - (uint32_t)(cand[first] & 0xFFFFFFFFull));
-}
-
-int launch_sample(const float* logits, int batch, int vocab, const qw_sample_params* params, uint64_t rng_counter,
-                  int32_t* out_ids, const int* argmax_hint, int* err, cudaStream_t st) {
-    if (batch <= 0) return QW_OK;
-    sample_kernel<<<batch, SMP_THREADS, 0, st>>>(logits, vocab, params, rng_counter, out_ids, argmax_hint, err);
-    return check_launch();
-}
-
 // ---------------------------------------------------------------- weight staging
 __global__ void bf16_to_f32_kernel(const uint16_t* __restrict__ src, float* __restrict__ dst, int n) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
