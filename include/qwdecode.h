@@ -142,7 +142,10 @@ int qw_kv_layout(const qw_kv* kv, void** base, int64_t* layer_stride, int64_t* p
  *                    lives in page block_tables[s][p / QW_PAGE_SIZE], slot p % QW_PAGE_SIZE.
  *   last_logits      DEVICE float[n_seqs][vocab] or NULL: logits of each sequence's last token.
  * Writes K/V of every token into the pool.  Attention of a token at position p sees
- * the cached positions 0 .. p of its sequence (the causal mask of Step 5). */
+ * the cached positions 0 .. p of its sequence (the causal mask of Step 5).
+ * Sequences are independent, so one call may mix fresh prompts, prompt chunks appended
+ * to cached prefixes and decode tokens (a sequence of one token at the position after its
+ * cache): each gets the logits of its last token. */
 int qw_prefill(qw_ctx* ctx, const int32_t* ids, const int32_t* positions, const int32_t* cu_seqlens,
                int32_t n_seqs, qw_kv* kv, const int32_t* block_tables, int32_t bt_stride,
                float* last_logits, void* stream);
@@ -252,7 +255,7 @@ int qw_debug_hidden(qw_ctx* ctx, int32_t layer, float* out, int32_t n_rows, void
 
 /* Test hook for the tensor-core projection kernel alone: C = A . B^T with
  *   A DEVICE bf16[M][K], B DEVICE bf16[N][K] (the layout of every weight), K % 64 == 0,
- *   N % 32 == 0, bn = 128 or 256 (output tile width) and the epilogue
+ *   N % 32 == 0, bn = 128 or 256 (output tile width; 32 or 64 too with split = 1) and the epilogue
  *   epi = 0: C is float[M][N], C = A B^T;  1: C += A B^T (residual add);
  *   epi = 2: C is bf16[M][N/2], C[m][j] = silu(Y[m][2j]) * Y[m][2j+1] with Y = A B^T
  *   (the SwiGLU of Step 6 on gate/up rows interleaved);

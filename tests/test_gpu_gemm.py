@@ -56,7 +56,9 @@ def test_gemm_swiglu_pairs(bd):
 
 
 @pytest.mark.parametrize("M,N,K,bn,epi", [(1, 4096, 1024, 256, 0), (64, 1024, 2048, 128, 1), (65, 6144, 1024, 256, 2),
-                                          (200, 1024, 3072, 128, 1), (16, 151936, 1024, 256, 0)])
+                                          (200, 1024, 3072, 128, 1), (16, 151936, 1024, 256, 0),
+                                          (64, 4096, 1024, 32, 0), (3, 4096, 1024, 32, 0), (129, 4096, 1024, 32, 0),
+                                          (64, 6144, 1024, 64, 2), (70, 6144, 1024, 64, 2), (64, 1024, 1024, 64, 0)])
 def test_gemm_split_operand(bd, M, N, K, bn, epi):
     """Small-M mode: activations as bf16 hi/lo row pairs, summed in the epilogue (~16-bit mantissa)."""
     g = torch.Generator(device="cpu").manual_seed(M + N)
@@ -85,7 +87,8 @@ def test_gemm_split_operand(bd, M, N, K, bn, epi):
 
 
 @pytest.mark.parametrize("M,N,K,bn", [(1, 4096, 1024, 256), (64, 1024, 3072, 128), (64, 6144, 1024, 256),
-                                      (200, 1024, 2048, 128)])
+                                      (200, 1024, 2048, 128), (64, 1024, 2048, 32), (64, 1024, 3072, 32),
+                                      (5, 1024, 3072, 32), (130, 1024, 2048, 64)])
 def test_gemm_split_k_atomic(bd, M, N, K, bn):
     """Small-M split-K: every SM takes a K slice and adds its partial product atomically."""
     g = torch.Generator(device="cpu").manual_seed(M * 3 + N)

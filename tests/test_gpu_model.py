@@ -178,3 +178,48 @@ def test_prefill_attention_kernels_match_oracle(small, variant):
         ref = orc.forward(ids[cu[s]:cu[s + 1]].numpy(), np.arange(L), orc.new_cache(), last_only=True)
         err = Q.rel_l2_rows(last[s:s + 1].cpu().numpy(), ref)
         assert err.max() < Q.LOGIT_TOL, f"variant {variant} seq {s} (L={L}): {err.max():.2e}"
+
+
+def test_mixed_prefill_and_decode_in_one_call(small):
+    """One qw_prefill call carries a fresh prompt, a prompt chunk appended to a cached prefix,
+    and two decode tokens (one-token chunks at the position after their caches), each sequence
+    reading only its own pages; every sequence's last logits equal the oracle's over its whole
+    history, and the decode rows equal what qw_decode_step gives for the same tokens."""
+    bd, w, model, orc = small
+    # sequences: 0 fresh prompt of 37; 1 has 50 cached, adds a chunk of 20; 2 and 3 have 64 and
+    # 9 cached and decode one token each
+    hist = [0, 50, 64, 9]
+    new = [37, 20, 1, 1]
+    cap = 96
+    n_pages = 4 * (cap // Q.PAGE) + 3
+    kv = bd.KVPool(model, n_pages)
+    bt_np, _ = Q.block_tables(hist, cap, n_pages, seed=12)
+    bt = torch.from_numpy(bt_np).cuda()
+    ids_all = [synth.token_ids(0, 40 + s, hist[s] + new[s], S.vocab) for s in range(4)]
+    # the cached prefixes, written by one prefill of sequences 1..3
+    pre = [s for s in range(4) if hist[s]]
+    ids = torch.cat([ids_all[s][:hist[s]] for s in pre])
+    pos = torch.cat([torch.arange(hist[s], dtype=torch.int32) for s in pre])
+    cu = np.concatenate([[0], np.cumsum([hist[s] for s in pre])]).astype(np.int32)
+    model.prefill(ids.cuda(), pos.cuda(), cu, kv, bt[pre].contiguous(), torch.empty(len(pre), S.vocab, device="cuda"))
+    model.check()
+    # the mixed call
+    ids = torch.cat([ids_all[s][hist[s]:] for s in range(4)])
+    pos = torch.cat([torch.arange(hist[s], hist[s] + new[s], dtype=torch.int32) for s in range(4)])
+    cu = np.concatenate([[0], np.cumsum(new)]).astype(np.int32)
+    last = torch.empty(4, S.vocab, device="cuda")
+    model.prefill(ids.cuda(), pos.cuda(), cu, kv, bt, last)
+    model.check()
+    for s in range(4):
+        L = hist[s] + new[s]
+        ref = orc.forward(ids_all[s].numpy(), np.arange(L), orc.new_cache(), last_only=True)
+        err = Q.rel_l2_rows(last[s:s + 1].cpu().numpy(), ref).max()
+        assert err < Q.LOGIT_TOL, f"sequence {s}: logits rel L2 {err:.2e}"
+    # the decode rows as a decode step (same positions: the step rewrites the same cache slots)
+    rows = [2, 3]
+    dec = torch.empty(2, S.vocab, device="cuda")
+    model.decode_step(torch.tensor([int(ids_all[s][-1]) for s in rows], dtype=torch.int32).cuda(),
+                      torch.tensor([hist[s] for s in rows], dtype=torch.int32).cuda(), kv, bt[rows].contiguous(), dec)
+    model.check()
+    assert Q.rel_l2_rows(dec.cpu().numpy(), last[rows].cpu().numpy()).max() < Q.LOGIT_TOL
+    kv.close()

@@ -47,6 +47,7 @@ struct LayerW {
     CUtensorMap tm_qkv, tm_o, tm_gu, tm_d;
     CUtensorMap tm_o256, tm_d256;   // o_proj / down_proj with 256-row boxes (large-M products)
     CUtensorMap tm_qkv128, tm_gu128;  // q|k|v and gate/up with 128-row boxes (CTA-pair halves)
+    CUtensorMap tm_qkv32, tm_gu64, tm_o32, tm_d32;  // narrow boxes for decode batches
 };
 
 // Per-kernel-class device time (qw_debug_profile): CUDA events recorded on the launching
@@ -296,7 +297,11 @@ int qw_init(const qw_config* cfg, const qw_weights* w, qw_ctx** out) {
             make_tmap_bf16(&Lw.tm_o256, Lw.wo, ctx->attn_dim, D, (size_t)ctx->attn_dim * 2, 64, 256) ||
             make_tmap_bf16(&Lw.tm_d256, Lw.wd, I, D, (size_t)I * 2, 64, 256) ||
             make_tmap_bf16(&Lw.tm_qkv128, Lw.wqkv, D, ctx->qkv_dim, rowb, 64, 128) ||
-            make_tmap_bf16(&Lw.tm_gu128, Lw.wgu, D, 2 * I, rowb, 64, 128)) {
+            make_tmap_bf16(&Lw.tm_gu128, Lw.wgu, D, 2 * I, rowb, 64, 128) ||
+            make_tmap_bf16(&Lw.tm_qkv32, Lw.wqkv, D, ctx->qkv_dim, rowb, 64, 32) ||
+            make_tmap_bf16(&Lw.tm_gu64, Lw.wgu, D, 2 * I, rowb, 64, 64) ||
+            make_tmap_bf16(&Lw.tm_o32, Lw.wo, ctx->attn_dim, D, (size_t)ctx->attn_dim * 2, 64, 32) ||
+            make_tmap_bf16(&Lw.tm_d32, Lw.wd, I, D, (size_t)I * 2, 64, 32)) {
             free_ctx(ctx);
             return fail(QW_ECUDA, "cuTensorMapEncodeTiled failed for a weight");
         }
@@ -457,7 +462,7 @@ static int run_layers(qw_ctx* ctx, int n, const int* ids, const int* positions, 
         } else {
             // small M: 128-wide tiles (32 CTAs stream the weight for a 4096-wide q|k|v), measured
             // faster than split-K with atomic accumulation into a zeroed target
-            { QW_PROF(QW_PROF_GEMM); QW_TRY(gemm_bf16(ctx->h, D, split ? Lw.tm_qkv128 : Lw.tm_qkv, split ? 128 : 256, n, ctx->qkv_dim, D,
+            { QW_PROF(QW_PROF_GEMM); QW_TRY(gemm_bf16(ctx->h, D, split ? Lw.tm_qkv32 : Lw.tm_qkv, split ? 32 : 256, n, ctx->qkv_dim, D,
                              EPI_STORE_F32, e, st),
                    "qkv gemm"); }
             { QW_PROF(QW_PROF_OTHER); QW_TRY(launch_qkv_post(ctx->qkv, n, positions, tok_seq, Hq, Hkv, Lw.q_norm, Lw.k_norm, ctx->inv_freq,
@@ -481,7 +486,7 @@ static int run_layers(qw_ctx* ctx, int n, const int* ids, const int* positions, 
         // N = hidden is narrow: 128-wide tiles give split-K decode batches more units,
         // 256-wide tiles halve the activation re-reads of a prefill
         if (split)
-            { QW_PROF(QW_PROF_GEMM); QW_TRY(gemm_bf16(ctx->attn, ctx->attn_dim, Lw.tm_o, 128, n, D, ctx->attn_dim, EPI_ADD_ATOMIC, e, st),
+            { QW_PROF(QW_PROF_GEMM); QW_TRY(gemm_bf16(ctx->attn, ctx->attn_dim, Lw.tm_o32, 32, n, D, ctx->attn_dim, EPI_ADD_ATOMIC, e, st),
                    "o_proj gemm"); }
         else
             { QW_PROF(QW_PROF_GEMM); QW_TRY(gemm_bf16(ctx->attn, ctx->attn_dim, Lw.tm_o256, 256, n, D, ctx->attn_dim, EPI_RESID_ADD, e, st,
@@ -492,14 +497,14 @@ static int run_layers(qw_ctx* ctx, int n, const int* ids, const int* positions, 
         if (split) {
             // small M: 128-wide tiles with the SwiGLU epilogue writing the hi/lo activation pairs
             e = GemmEpilogue{nullptr, ctx->act, I, ctx->err, split};
-            { QW_PROF(QW_PROF_GEMM); QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_gu128, 128, n, 2 * I, D, EPI_SWIGLU, e, st), "gate/up gemm"); }
+            { QW_PROF(QW_PROF_GEMM); QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_gu64, 64, n, 2 * I, D, EPI_SWIGLU, e, st), "gate/up gemm"); }
         } else {
             e = GemmEpilogue{nullptr, ctx->act, I, ctx->err, split};
             { QW_PROF(QW_PROF_GEMM); QW_TRY(gemm_bf16(ctx->h, D, Lw.tm_gu, 256, n, 2 * I, D, EPI_SWIGLU, e, st, &Lw.tm_gu128), "gate/up gemm"); }
         }
         e = GemmEpilogue{ctx->x, nullptr, D, ctx->err, split};
         if (split)
-            { QW_PROF(QW_PROF_GEMM); QW_TRY(gemm_bf16(ctx->act, I, Lw.tm_d, 128, n, D, I, EPI_ADD_ATOMIC, e, st), "down gemm"); }
+            { QW_PROF(QW_PROF_GEMM); QW_TRY(gemm_bf16(ctx->act, I, Lw.tm_d32, 32, n, D, I, EPI_ADD_ATOMIC, e, st), "down gemm"); }
         else
             { QW_PROF(QW_PROF_GEMM); QW_TRY(gemm_bf16(ctx->act, I, Lw.tm_d256, 256, n, D, I, EPI_RESID_ADD, e, st, &Lw.tm_d), "down gemm"); }
         if (ctx->hidden)
@@ -679,7 +684,7 @@ int qw_debug_hidden(qw_ctx* ctx, int32_t layer, float* out, int32_t n_rows, void
 int qw_debug_gemm(const uint16_t* A, const uint16_t* B, void* C, int32_t M, int32_t N, int32_t K, int32_t epi,
                   int32_t bn, int32_t split, void* stream) {
     if (!A || !B || !C || M < 1 || N < 32 || K < 64 || K % 64 || N % 32 || epi < 0 || epi > 3 ||
-        (bn != 128 && bn != 256))
+        (bn != 128 && bn != 256 && !(split == 1 && (bn == 32 || bn == 64))))
         return fail(QW_EINVAL, "qw_debug_gemm: bad argument");
     if (split < 0 || split > 2) return fail(QW_EINVAL, "qw_debug_gemm: bad split");
     CUtensorMap tb, tb_half;

@@ -43,6 +43,15 @@ QW_DEV float warp_max(float v) {
     return v;
 }
 
+// ------------------------------------------------------------ programmatic dependent launch
+// A kernel launched with pdl_launch() may start while the previous kernel of the stream is
+// still running.  pdl_wait() returns once every prior kernel of the stream has completed and
+// its writes are visible; a kernel calls it before reading anything earlier kernels wrote and
+// before writing anything they may still read (in a kernel launched without the attribute it
+// returns at once).  pdl_trigger() lets the next kernel of the stream start launching.
+QW_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+QW_DEV void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------ shared-memory address
 QW_DEV uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 

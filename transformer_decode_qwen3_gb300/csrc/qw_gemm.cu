@@ -43,7 +43,7 @@ template <int BN>
 struct GemmCfg {
     static constexpr int BM = 128;
     static constexpr int BK = 64;                       // 64 bf16 = one 128-byte swizzle row
-    static constexpr int STAGES = BN >= 256 ? 4 : 6;
+    static constexpr int STAGES = BN >= 256 ? 4 : (BN >= 128 ? 6 : 8);
     static constexpr int A_BYTES = BM * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -310,6 +310,10 @@ __global__ void __launch_bounds__(256, 1)
     if (MC) cluster_sync();   // the peer's barriers are initialised before any multicast reaches them
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    if (!(warp == 0 && lane == 0)) {   // the producer waits after starting its weight loads
+        pdl_wait();
+        pdl_trigger();
+    }
 
     // unit t -> (m tile, n tile, K blocks [kb0, kb1)).  Consecutive CTAs share the A tile
     // (share_a: n tile fastest; the whole B fits in L2) or the B tile (m tile fastest).
@@ -324,6 +328,20 @@ __global__ void __launch_bounds__(256, 1)
 
     if (warp == 0) {
         if (lane == 0) {  // TMA producer
+            // The weight tiles of the first stages do not depend on earlier kernels: they start
+            // streaming before pdl_wait (launched with pdl_launch, the previous kernel may still run).
+            int n_pre = 0;
+            if (!MC && first < n_tiles) {
+                int tm, tn, kb0, kb1;
+                unit(first, tm, tn, kb0, kb1);
+                n_pre = min(C::STAGES, kb1 - kb0);
+                for (int i = 0; i < n_pre; ++i) {
+                    mbar_arrive_expect_tx(&full[i], C::STAGE_BYTES);
+                    tma_load_2d(sB + i * C::B_BYTES, &tmB, (kb0 + i) * C::BK, tn * BN, &full[i]);
+                }
+            }
+            pdl_wait();
+            pdl_trigger();
             uint32_t kb_all = 0;
             for (int t = first; t < n_tiles && !*abort_flag; t += stride) {
                 int tm, tn, kb0, kb1;
@@ -331,6 +349,10 @@ __global__ void __launch_bounds__(256, 1)
                 for (int kb = kb0; kb < kb1; ++kb, ++kb_all) {
                     const int s = kb_all % C::STAGES;
                     const uint32_t ph = (kb_all / C::STAGES) & 1;
+                    if (kb_all < (uint32_t)n_pre) {   // weights already on their way: the activations only
+                        tma_load_2d(sA + s * C::A_BYTES, &tmA, kb * C::BK, tm * C::BM, &full[s]);
+                        continue;
+                    }
                     if (!mbar_wait(&empty[s], ph ^ 1, ep.err) || *abort_flag) {
                         *abort_flag = 1;
                         break;
@@ -607,14 +629,29 @@ static int launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, int M, int N,
     }
     const int work = tiles_m * tiles_n * ksplit;
     const int grid = work < n_sm ? work : n_sm;
-    kern<<<grid, C::THREADS, C::SMEM, st>>>(ta, tb, tc, M, N, K, tiles_m, tiles_n, ksplit, share_a, ep);
+    const cudaError_t e = pdl_launch(kern, dim3(grid), dim3(C::THREADS), C::SMEM, st, ta, tb, tc, M, N, K, tiles_m,
+                                     tiles_n, ksplit, share_a, ep);
     count_launches(1);
-    return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ECUDA;
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? QW_OK : QW_ECUDA;
 }
 
 template <bool SPLIT>
 static int launch_split(const CUtensorMap& ta, const CUtensorMap& tb, int bn, int M, int N, int K, int epi,
                         const GemmEpilogue& ep, cudaStream_t st) {
+    if constexpr (SPLIT) {
+        // narrow tiles for decode batches: a 4096-wide q|k|v on 32-wide tiles covers 128 SMs
+        if (bn == 32 || bn == 64) {
+            if (epi == EPI_QKV_ROPE || epi == EPI_RESID_ADD) return QW_EINVAL;
+            if (bn == 32) {
+                if (epi == EPI_STORE_F32) return launch_bn<32, EPI_STORE_F32, true, false>(ta, tb, M, N, K, ep, st);
+                if (epi == EPI_ADD_ATOMIC) return launch_bn<32, EPI_ADD_ATOMIC, true, false>(ta, tb, M, N, K, ep, st);
+                return launch_bn<32, EPI_SWIGLU, true, false>(ta, tb, M, N, K, ep, st);
+            }
+            if (epi == EPI_STORE_F32) return launch_bn<64, EPI_STORE_F32, true, false>(ta, tb, M, N, K, ep, st);
+            if (epi == EPI_ADD_ATOMIC) return launch_bn<64, EPI_ADD_ATOMIC, true, false>(ta, tb, M, N, K, ep, st);
+            return launch_bn<64, EPI_SWIGLU, true, false>(ta, tb, M, N, K, ep, st);
+        }
+    }
     if (bn == 256) {
         if (epi == EPI_STORE_F32) return launch_bn<256, EPI_STORE_F32, SPLIT, false>(ta, tb, M, N, K, ep, st);
         if (epi == EPI_RESID_ADD) return launch_bn<256, EPI_RESID_ADD, SPLIT, false>(ta, tb, M, N, K, ep, st);
@@ -625,6 +662,7 @@ static int launch_split(const CUtensorMap& ta, const CUtensorMap& tb, int bn, in
         }
         return launch_bn<256, EPI_SWIGLU, SPLIT, false>(ta, tb, M, N, K, ep, st);
     }
+    if (bn != 128) return QW_EINVAL;
     if (epi == EPI_STORE_F32) return launch_bn<128, EPI_STORE_F32, SPLIT, false>(ta, tb, M, N, K, ep, st);
     if (epi == EPI_RESID_ADD) return launch_bn<128, EPI_RESID_ADD, SPLIT, false>(ta, tb, M, N, K, ep, st);
     if (epi == EPI_ADD_ATOMIC) return launch_bn<128, EPI_ADD_ATOMIC, SPLIT, false>(ta, tb, M, N, K, ep, st);
@@ -649,7 +687,7 @@ static int launch_mc(const CUtensorMap& ta, const CUtensorMap& tb_half, int M, i
 int gemm_bf16(const void* A, int lda_elems, const CUtensorMap& tmB, int bn, int M, int N, int K, int epi,
               const GemmEpilogue& ep, cudaStream_t st, const CUtensorMap* tmB_half) {
     if (M <= 0) return QW_OK;
-    if (K % 64 || N % 32 || (bn != 128 && bn != 256)) return QW_EINVAL;
+    if (K % 64 || N % 32 || (bn != 128 && bn != 256 && !(ep.split && (bn == 32 || bn == 64)))) return QW_EINVAL;
     // split layout: ceil(M/64) tiles of 128 rows (64 hi rows, then their 64 lo rows)
     const uint64_t rows = ep.split ? (uint64_t)((M + 63) / 64) * 128 : (uint64_t)M;
     CUtensorMap ta;

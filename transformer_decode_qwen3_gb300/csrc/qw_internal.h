@@ -11,6 +11,23 @@ namespace qw {
 // Counts every kernel launch the library makes (read by qw_kernel_launches).
 void count_launches(int n);
 
+// Launch `kern` on `st` with programmatic stream serialization: it may begin while the previous
+// kernel of the stream finishes, so it must call pdl_wait() before touching dependent data.
+template <typename... KArgs, typename... Args>
+cudaError_t pdl_launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Record `msg` for qw_last_error_message() on this thread and return `code`.
 int report_error(int code, const char* msg);
 

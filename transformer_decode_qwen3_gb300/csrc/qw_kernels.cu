@@ -35,6 +35,8 @@ QW_DEV void store_bf16x2(uint16_t* base, size_t ld, int row, int col, float a, f
 // and QW_ERANGE in the error word.
 __global__ void embed_kernel(const int* __restrict__ ids, const uint16_t* __restrict__ E, int vocab, int D,
                              float* __restrict__ x, int* err) {
+    pdl_wait();   // launched with pdl_launch: earlier kernels may still be running
+    pdl_trigger();
     const int t = blockIdx.x;
     const int id = ids[t];
     const bool bad = id < 0 || id >= vocab;
@@ -51,7 +53,7 @@ __global__ void embed_kernel(const int* __restrict__ ids, const uint16_t* __rest
 
 int launch_embed(const int* ids, int n, const uint16_t* E, int vocab, int D, float* x, int* err, cudaStream_t st) {
     if (n <= 0) return QW_OK;
-    embed_kernel<<<n, 128, 0, st>>>(ids, E, vocab, D, x, err);
+    if (pdl_launch(embed_kernel, dim3(n), dim3(128), 0, st, ids, E, vocab, D, x, err) != cudaSuccess) return QW_ECUDA;
     return check_launch();
 }
 
@@ -59,6 +61,8 @@ int launch_embed(const int* ids, int n, const uint16_t* E, int vocab, int D, flo
 // out[r] = bf16(x[src] / sqrt(mean(x[src]^2) + eps) * w), one warp per row.
 __global__ void rmsnorm_bf16_kernel(const float* __restrict__ x, const int* __restrict__ rows, int n, int D,
                                     const float* __restrict__ w, float eps, uint16_t* __restrict__ out, int split) {
+    pdl_wait();   // launched with pdl_launch: earlier kernels may still be running
+    pdl_trigger();
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (r >= n) return;
     const int src = rows ? rows[r] : r;
@@ -81,7 +85,9 @@ __global__ void rmsnorm_bf16_kernel(const float* __restrict__ x, const int* __re
 int launch_rmsnorm_bf16(const float* x, const int* rows, int n, int D, const float* w, float eps, uint16_t* out,
                         int split, cudaStream_t st) {
     if (n <= 0) return QW_OK;
-    rmsnorm_bf16_kernel<<<(n + 7) / 8, 256, 0, st>>>(x, rows, n, D, w, eps, out, split);
+    if (pdl_launch(rmsnorm_bf16_kernel, dim3((n + 7) / 8), dim3(256), 0, st, x, rows, n, D, w, eps, out, split) !=
+        cudaSuccess)
+        return QW_ECUDA;
     return check_launch();
 }
 
@@ -94,6 +100,8 @@ __global__ void qkv_post_kernel(const float* __restrict__ qkv, const int* __rest
                                 const int* __restrict__ tok_seq, int Hq, int Hkv, const float* __restrict__ q_norm,
                                 const float* __restrict__ k_norm, const float* __restrict__ inv_freq, float eps,
                                 float* __restrict__ q_out, uint16_t* __restrict__ q_bf16, KvView kv, int* err) {
+    pdl_wait();   // launched with pdl_launch: earlier kernels may still be running
+    pdl_trigger();
     const int t = blockIdx.x;
     const int hh = blockIdx.y * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     const int nh = Hq + 2 * Hkv;
@@ -163,6 +171,8 @@ int launch_positions(int* out, int start, int n, cudaStream_t st) {
 
 __global__ void rope_table_kernel(const int* __restrict__ positions, int n, const float* __restrict__ inv_freq,
                                   float2* __restrict__ tab) {
+    pdl_wait();   // launched with pdl_launch: earlier kernels may still be running
+    pdl_trigger();
     const int t = blockIdx.x, i = threadIdx.x;
     float sn, cs;
     sincosf(__fmul_rn((float)positions[t], inv_freq[i]), &sn, &cs);
@@ -171,7 +181,8 @@ __global__ void rope_table_kernel(const int* __restrict__ positions, int n, cons
 
 int launch_rope_table(const int* positions, int n, const float* inv_freq, float2* tab, cudaStream_t st) {
     if (n <= 0) return QW_OK;
-    rope_table_kernel<<<n, 64, 0, st>>>(positions, n, inv_freq, tab);
+    if (pdl_launch(rope_table_kernel, dim3(n), dim3(64), 0, st, positions, n, inv_freq, tab) != cudaSuccess)
+        return QW_ECUDA;
     return check_launch();
 }
 
@@ -180,8 +191,9 @@ int launch_qkv_post(const float* qkv, int n_tok, const int* positions, const int
                     uint16_t* q_bf16, const KvView& kv, int* err, cudaStream_t st) {
     if (n_tok <= 0) return QW_OK;
     dim3 grid(n_tok, (Hq + 2 * Hkv + 3) / 4);
-    qkv_post_kernel<<<grid, 128, 0, st>>>(qkv, positions, tok_seq, Hq, Hkv, q_norm, k_norm, inv_freq, eps, q_out,
-                                          q_bf16, kv, err);
+    if (pdl_launch(qkv_post_kernel, grid, dim3(128), 0, st, qkv, positions, tok_seq, Hq, Hkv, q_norm, k_norm, inv_freq,
+                   eps, q_out, q_bf16, kv, err) != cudaSuccess)
+        return QW_ECUDA;
     return check_launch();
 }
 
@@ -433,6 +445,8 @@ __global__ void __launch_bounds__(AD_WARPS * 32) attn_decode_kernel(const float*
                                                                     int Hkv, KvView kv, int chunk_pages,
                                                                     int n_splits, float* __restrict__ part,
                                                                     float scale_log2, int* err) {
+    pdl_wait();   // launched with pdl_launch: earlier kernels may still be running
+    pdl_trigger();
     const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int half = lane >> 4, dc = lane & 15;
@@ -584,6 +598,8 @@ __global__ void __launch_bounds__(AD_WARPS * 32) attn_decode_kernel(const float*
 
 __global__ void attn_combine_kernel(const float* __restrict__ part, int n_splits, int Hq,
                                     uint16_t* __restrict__ out, int split) {
+    pdl_wait();   // launched with pdl_launch: earlier kernels may still be running
+    pdl_trigger();
     const int h = blockIdx.x, b = blockIdx.y, d = threadIdx.x * 2;
     const float* base = part + ((size_t)b * Hq + h) * n_splits * AD_PART;
     float M = -INFINITY;
@@ -617,10 +633,13 @@ int launch_attn_decode(const float* q, const int* positions, int batch, int Hq, 
         n_splits = (kv.bt_stride + chunk - 1) / chunk;
     }
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)QW_HEAD_DIM);
-    attn_decode_kernel<<<dim3(n_splits, Hkv, batch), AD_WARPS * 32, 0, st>>>(q, positions, Hq, Hkv, kv, chunk,
-                                                                             n_splits, part, scale_log2, err);
+    if (pdl_launch(attn_decode_kernel, dim3(n_splits, Hkv, batch), dim3(AD_WARPS * 32), 0, st, q, positions, Hq, Hkv,
+                   kv, chunk, n_splits, part, scale_log2, err) != cudaSuccess)
+        return QW_ECUDA;
     if (check_launch()) return QW_ECUDA;
-    attn_combine_kernel<<<dim3(Hq, batch), QW_HEAD_DIM / 2, 0, st>>>(part, n_splits, Hq, out, split);
+    if (pdl_launch(attn_combine_kernel, dim3(Hq, batch), dim3(QW_HEAD_DIM / 2), 0, st, part, n_splits, Hq, out, split) !=
+        cudaSuccess)
+        return QW_ECUDA;
     return check_launch();
 }
 

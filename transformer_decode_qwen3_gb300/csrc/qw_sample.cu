@@ -179,6 +179,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS)
                   uint64_t rng_counter, int32_t* __restrict__ out, const float2* __restrict__ part, int n_part,
                   const int* __restrict__ argmax_hint, int* err) {
     __shared__ Shared sh;
+    pdl_wait();   // launched with pdl_launch: the LM head may still be running
+    pdl_trigger();
     const int row = blockIdx.x / CL, rank = (int)cluster_rank(), tid = threadIdx.x;
     const float* lg = logits + (size_t)row * vocab;
     const qw_sample_params P = params[row];
@@ -373,10 +375,10 @@ int launch_sample(const float* logits, int batch, int vocab, const qw_sample_par
                   int32_t* out_ids, const float2* tile_part, int n_part, const int* argmax_hint, int* err,
                   cudaStream_t st) {
     if (batch <= 0) return QW_OK;
-    smp::sample_kernel<<<batch * smp::CL, smp::THREADS, 0, st>>>(logits, vocab, params, rng_counter, out_ids, tile_part,
-                                                                 n_part, argmax_hint, err);
+    const cudaError_t e = pdl_launch(smp::sample_kernel, dim3(batch * smp::CL), dim3(smp::THREADS), 0, st, logits, vocab,
+                                     params, rng_counter, out_ids, tile_part, n_part, argmax_hint, err);
     count_launches(1);
-    return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ECUDA;
+    return e == cudaSuccess && cudaGetLastError() == cudaSuccess ? QW_OK : QW_ECUDA;
 }
 
 }  // namespace qw
