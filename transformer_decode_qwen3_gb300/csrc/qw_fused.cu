@@ -108,6 +108,7 @@ QW_DEV unsigned* c_x(const Params& p, int l, int c) {
 }
 QW_DEV unsigned* c_lm(const Params& p) { return p.sync + CNT_STRIDE * (2 + p.n_layers * CNT_PER_LAYER); }
 
+
 QW_DEV unsigned ld_acquire(const unsigned* ptr) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
@@ -216,7 +217,7 @@ QW_DEV void give_up(const Params& p, Smem& sm) {
 
 // Bounded wait of one warp for `n` counters (lane i polls first + i * CNT_STRIDE) to reach
 // `target`; warp-uniform result, false on timeout or abort.
-QW_DEV bool wait_counters(const Params& p, const unsigned* first, int n, unsigned target, Smem& sm) {
+__device__ __noinline__ bool wait_counters(const Params& p, const unsigned* first, int n, unsigned target, Smem& sm) {
     const int lane = threadIdx.x & 31;
     const unsigned* ptr = first + (lane < n ? lane : 0) * CNT_STRIDE;
     auto done = [&]() { return __all_sync(0xffffffffu, lane >= n || (int)(ld_acquire(ptr) - target) >= 0); };
@@ -237,7 +238,7 @@ QW_DEV bool wait_counters(const Params& p, const unsigned* first, int n, unsigne
 
 // Bounded wait for phase `parity` of a cluster-exchange mbarrier: lane 0 of each calling warp
 // polls (one poller per warp, not 32), __syncwarp orders the other lanes after its acquire.
-QW_DEV bool wait_cluster(const Params& p, uint64_t* bar, uint32_t parity, Smem& sm) {
+__device__ __noinline__ bool wait_cluster(const Params& p, uint64_t* bar, uint32_t parity, Smem& sm) {
     int good = 1;
     if ((threadIdx.x & 31) == 0 && !mbar_test_wait_cluster(bar, parity)) {
         const uint64_t t0 = gtimer();
@@ -266,6 +267,9 @@ QW_DEV bool wait_cluster(const Params& p, uint64_t* bar, uint32_t parity, Smem& 
 QW_DEV void signal_add(unsigned* ptr, unsigned v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
 }
+
+// sin and cos of a rotation angle (full-range sincosf; one out-of-line copy keeps the code small)
+__device__ __noinline__ void rope_sincos(float ang, float& sn, float& cs) { sincosf(ang, &sn, &cs); }
 
 QW_DEV void unpack8(uint4 w, float (&f)[8]) {
     f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x); f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
@@ -461,6 +465,13 @@ QW_DEV float hsum2(uint64_t v) {
 QW_DEV void ffma2(uint64_t& acc, uint64_t a, uint64_t b) {
     asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
 }
+// acc.{lo,hi} += b.{lo,hi}
+QW_DEV void add2(uint64_t& acc, uint64_t b) {
+    float a0, a1, b0, b1;
+    unpack2(acc, a0, a1);
+    unpack2(b, b0, b1);
+    acc = pack2(a0 + b0, a1 + b1);
+}
 // a bf16 pair (low element in the low half) as packed fp32
 QW_DEV uint64_t bf2_to_f2(uint32_t w) { return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)); }
 
@@ -470,6 +481,7 @@ struct Consumer {
     int* err;
     int cw, lane;   // consumer warp 0..7, lane
     unsigned it = 0;
+    unsigned pending = 0;   // stages done with but not yet handed back
 
     // One lane of the warp waits for the stage (256 threads polling one mbarrier serialise on
     // it); __syncwarp then orders the other lanes' reads of the stage after that acquire.
@@ -483,14 +495,47 @@ struct Consumer {
         return ring + s * STAGE;
     }
     QW_DEV int slot() const { return it % NS; }
-    QW_DEV void stage_release() {
+    // Wait for the next n (<= NS) stages at once: lane k tests stage it + k, so one round of
+    // mbarrier tests covers the whole phase; the stages are then read at ring + ((it + k) % NS) *
+    // STAGE and handed back one by one.  Returns the first stage.
+    QW_DEV const uint8_t* phase_wait(int n, bool& ok) {
+        const unsigned k = it + lane;
+        bool ready = lane >= n || mbar_test_wait(&sm->full[k % NS], (k / NS) & 1);
+        if (!__all_sync(0xffffffffu, ready)) {
+            int good = ok;
+            if (lane < n) good = good && mbar_wait(&sm->full[k % NS], (k / NS) & 1, err);
+            ok = __all_sync(0xffffffffu, good != 0);
+        }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm->empty[it % NS]);
-        ++it;
+        if (!ok || sm->abort_flag) {
+            ok = false;
+            sm->abort_flag = 1;
+        }
+        return ring + (it % NS) * STAGE;
     }
-    // Dot products of `nrows` streamed rows with sm->h; results to sm->res[0..nrows).  Lane l
-    // takes columns 8 l + 256 i .. + 7 (i < 4) of rows cw and cw + 8, with packed fp32 FMAs.
-    QW_DEV bool dot_rows(int nrows, bool ok) {
+    // Done with the current stage.  The slot is handed back to the producer at once, or, when
+    // `hold`, at the next flush(): the producer's refill writes 32 KB into shared memory, and
+    // while the consumers are still reading other stages those writes compete with their reads
+    // for the shared-memory port, so short phases hand their stages back when they end.
+    QW_DEV void stage_release(bool hold = false) {
+        ++it;
+        ++pending;
+        if (!hold) flush();
+    }
+    QW_DEV void flush() {
+        __syncwarp();
+        if (lane == 0)
+            for (unsigned k = pending; k > 0; --k) mbar_arrive(&sm->empty[(it - k) % NS]);
+        pending = 0;
+    }
+    // Dot products of `nrows` (at most 64, so at most 4 stages) streamed rows with sm->h.  Warp cw
+    // takes rows 2 cw and 2 cw + 1 of every stage; lane l keeps one packed fp32 partial per row over
+    // its columns 8 l + 256 i .. + 7 (i < 4) for the whole phase, and the warp reduces its 8 rows
+    // once at the end with a transposed butterfly (each exchange halves the values a lane carries:
+    // 9 shuffles for 8 rows), so nothing but the stage barrier separates the stages.  On return,
+    // lanes 4 k .. 4 k + 3 hold the sum of the warp's row k, which is row 16 (k >> 1) + 2 cw + (k & 1)
+    // of the phase (rows past nrows give 0).
+    QW_DEV float dot_rows(int nrows, bool& ok) {
         uint64_t h2[4][4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -501,87 +546,116 @@ struct Consumer {
             h2[i][2] = pack2(b.x, b.y);
             h2[i][3] = pack2(b.z, b.w);
         }
-        for (int r0 = 0; r0 < nrows; r0 += ROWS_PER_STAGE) {
-            const int n = min(ROWS_PER_STAGE, nrows - r0);
-            const uint8_t* st = stage_wait(ok);
-            if (ok) {
-                for (int r = cw; r < n; r += 2 * NCW) {
-                    const bool two = r + NCW < n;
-                    const uint4* ra = (const uint4*)(st + r * ROW_B);
-                    const uint4* rb = (const uint4*)(st + (two ? r + NCW : r) * ROW_B);
-                    uint4 wa[4], wb[4];
+        uint64_t acc[8];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        wa[i] = ra[lane + 32 * i];
-                        wb[i] = rb[lane + 32 * i];
+        for (int k = 0; k < 8; ++k) acc[k] = 0;
+        const int nst = (nrows + ROWS_PER_STAGE - 1) / ROWS_PER_STAGE;
+        const uint8_t* st0 = phase_wait(nst, ok);
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+            if (s < nst) {
+                const int n = min(ROWS_PER_STAGE, nrows - ROWS_PER_STAGE * s);
+                const uint8_t* st = ring + ((it + s) % NS) * STAGE;
+                if (ok) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int r = 2 * cw + j;
+                        if (r < n) {
+                            const uint4* ra = (const uint4*)(st + r * ROW_B);
+                            uint4 wa[4];
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) wa[i] = ra[lane + 32 * i];
+                            uint64_t a1 = 0;
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                ffma2(acc[2 * s + j], h2[i][0], bf2_to_f2(wa[i].x));
+                                ffma2(a1, h2[i][1], bf2_to_f2(wa[i].y));
+                                ffma2(acc[2 * s + j], h2[i][2], bf2_to_f2(wa[i].z));
+                                ffma2(a1, h2[i][3], bf2_to_f2(wa[i].w));
+                            }
+                            add2(acc[2 * s + j], a1);
+                        }
                     }
-                    uint64_t a0 = 0, a1 = 0, b0 = 0, b1 = 0;   // two packed accumulators per row
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        ffma2(a0, h2[i][0], bf2_to_f2(wa[i].x));
-                        ffma2(a1, h2[i][1], bf2_to_f2(wa[i].y));
-                        ffma2(a0, h2[i][2], bf2_to_f2(wa[i].z));
-                        ffma2(a1, h2[i][3], bf2_to_f2(wa[i].w));
-                        ffma2(b0, h2[i][0], bf2_to_f2(wb[i].x));
-                        ffma2(b1, h2[i][1], bf2_to_f2(wb[i].y));
-                        ffma2(b0, h2[i][2], bf2_to_f2(wb[i].z));
-                        ffma2(b1, h2[i][3], bf2_to_f2(wb[i].w));
-                    }
-                    const float a = hsum2(a0) + hsum2(a1), b = hsum2(b0) + hsum2(b1);
-                    // two-row butterfly: after the first exchange lanes 0..15 carry row a and
-                    // lanes 16..31 row b, so both rows reduce with 5 shuffles instead of 10
-                    const bool up = lane & 16;
-                    float v = up ? b : a;
-                    v += __shfl_xor_sync(0xffffffffu, up ? a : b, 16);
-#pragma unroll
-                    for (int o = 8; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                    if (lane == 0) sm->res[r0 + r] = v;
-                    if (lane == 16 && two) sm->res[r0 + r + NCW] = v;
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm->empty[(it + s) % NS]);
             }
-            stage_release();
         }
-        return ok;
+        (void)st0;
+        it += nst;
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = hsum2(acc[k]);
+        // exchange with lane ^ 16 (^ 8, ^ 4): the upper lane keeps the upper half of its values
+#pragma unroll
+        for (int o = 16, n = 8; o >= 4; o >>= 1, n >>= 1) {
+            const bool up = lane & o;
+#pragma unroll
+            for (int k = 0; k < n / 2; ++k) {
+                const float send = up ? v[k] : v[k + n / 2];
+                v[k] = (up ? v[k + n / 2] : v[k]) + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+        }
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+        v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
+        return v[0];
     }
     // acc (columns 128 cw + 4 lane .. +3) += sum over streamed rows r of sm->coef[r] * row_r.
     // Each warp covers its own 128 output columns of every row, so no cross-warp sum is needed.
     QW_DEV bool scaled_rows(int nrows, float (&acc)[4], bool ok) {
-        for (int r0 = 0; r0 < nrows; r0 += ROWS_PER_STAGE) {
-            const int n = min(ROWS_PER_STAGE, nrows - r0);
-            const uint8_t* st = stage_wait(ok);
-            if (ok) {
-                const uint8_t* col = st + (128 * cw + 4 * lane) * 2;
-                uint64_t c01 = pack2(acc[0], acc[1]), c23 = pack2(acc[2], acc[3]);
-#pragma unroll 4
-                for (int r = 0; r < n; ++r) {
-                    const uint2 wv = *(const uint2*)(col + r * ROW_B);
-                    const float a = sm->coef[r0 + r];
-                    const uint64_t aa = pack2(a, a);
-                    ffma2(c01, aa, bf2_to_f2(wv.x));
-                    ffma2(c23, aa, bf2_to_f2(wv.y));
+        const int nst = (nrows + ROWS_PER_STAGE - 1) / ROWS_PER_STAGE;   // at most 2 (host-checked)
+        phase_wait(nst, ok);
+        uint64_t c01 = pack2(acc[0], acc[1]), c23 = pack2(acc[2], acc[3]), d01 = 0, d23 = 0;
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            if (s < nst) {
+                const int n = min(ROWS_PER_STAGE, nrows - ROWS_PER_STAGE * s);
+                const uint8_t* col = ring + ((it + s) % NS) * STAGE + (128 * cw + 4 * lane) * 2;
+                const float* cf = sm->coef + ROWS_PER_STAGE * s;
+                if (ok) {
+                    // two accumulator pairs (even and odd rows) halve the dependent FMA chain
+#pragma unroll
+                    for (int r = 0; r < ROWS_PER_STAGE; r += 2) {
+                        if (r < n) {
+                            const uint2 wv = *(const uint2*)(col + r * ROW_B);
+                            const uint64_t aa = pack2(cf[r], cf[r]);
+                            ffma2(c01, aa, bf2_to_f2(wv.x));
+                            ffma2(c23, aa, bf2_to_f2(wv.y));
+                        }
+                        if (r + 1 < n) {
+                            const uint2 wv = *(const uint2*)(col + (r + 1) * ROW_B);
+                            const uint64_t aa = pack2(cf[r + 1], cf[r + 1]);
+                            ffma2(d01, aa, bf2_to_f2(wv.x));
+                            ffma2(d23, aa, bf2_to_f2(wv.y));
+                        }
+                    }
                 }
-                unpack2(c01, acc[0], acc[1]);
-                unpack2(c23, acc[2], acc[3]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm->empty[(it + s) % NS]);
             }
-            stage_release();
         }
+        it += nst;
+        add2(c01, d01);
+        add2(c23, d23);
+        unpack2(c01, acc[0], acc[1]);
+        unpack2(c23, acc[2], acc[3]);
         return ok;
     }
 };
 
-// x (4 entries per consumer thread) -> sm.h = x / rms(x) * w, w = this thread's 4 norm weights
-// (loaded ahead, so no global load sits on the critical path).  Consumer barriers inside.
-QW_DEV void norm_into_h(Smem& sm, const float (&x)[4], int k0, const float4 w, float eps, int tid) {
+// x (4 entries per consumer thread) -> sm.h = x * w, w = this thread's 4 norm weights (loaded
+// ahead, so no global load sits on the critical path); returns 1 / rms(x), by which the products
+// with sm.h are scaled.  One consumer barrier inside.
+QW_DEV float norm_into_h(Smem& sm, const float (&x)[4], int k0, const float4 w, float eps, int tid) {
     float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
     ss = warp_sum(ss);
     if ((tid & 31) == 0) sm.wsum[tid >> 5] = ss;
+    *(float4*)&sm.h[k0] = make_float4(x[0] * w.x, x[1] * w.y, x[2] * w.z, x[3] * w.w);
     bar_consumers();
     float tot = 0.f;
 #pragma unroll
     for (int i = 0; i < NCW; ++i) tot += sm.wsum[i];
-    const float s = 1.0f / sqrtf(tot / (float)D + eps);
-    *(float4*)&sm.h[k0] = make_float4(x[0] * s * w.x, x[1] * s * w.y, x[2] * s * w.z, x[3] * s * w.w);
-    bar_consumers();
+    return 1.0f / sqrtf(tot / (float)D + eps);
 }
 
 // Cluster reduction of one 1024-wide partial per CTA: this thread's 4 columns (128 cw + 4 lane)
@@ -729,8 +803,11 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
         if (tid == 0) stamp(p, l, 1);
         if (w.attn) {
             // ---------------- A1: norm -> this CTA's q|k|v rows -> every peer's qkv_s
-            norm_into_h(sm, xa, k0, w_in, p.eps, tid);
-            ok = cs.dot_rows(QROWS, ok);
+            const float s_in = norm_into_h(sm, xa, k0, w_in, p.eps, tid);
+            {
+                const float v = cs.dot_rows(QROWS, ok);
+                if ((lane & 3) == 0) sm.res[16 * (lane >> 3) + 2 * cw + ((lane >> 2) & 1)] = v * s_in;
+            }
             if (tid == 0) stamp(p, l, 2);
             bar_consumers();
             if (ok && tid < 16 * CL) {
@@ -758,7 +835,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
                     for (int j = 0; j < 2; ++j) {
                         const float ang = __fmul_rn((float)pos, j ? invf1 : invf0);
                         float sn, cs_;
-                        sincosf(ang, &sn, &cs_);
+                        rope_sincos(ang, sn, cs_);
                         const float a = y[j], b = y[j + 2];
                         y[j] = a * cs_ - b * sn;
                         y[j + 2] = a * sn + b * cs_;
@@ -939,11 +1016,15 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
                 if (ok && more) mbar_arrive_expect_tx(&sm.bar_redo, RED_BYTES);   // next layer's phase
                 stamp(p, l, 7);
             }
-            if (ok) store_reduced(sm.red_o, p.oslot + ((size_t)pb * HKV + g) * D, r, tid);
-            bar_consumers();
-            if (tid == 0) {
-                signal_add(c_o(p, l, g), 1u);
-                stamp(p, l, 8);
+            // warp 0 stores this CTA's 128 outputs and publishes them (the warp barrier orders its
+            // lanes' stores before lane 0's release); the other warps go straight on
+            if (cw == 0) {
+                if (ok) store_reduced(sm.red_o, p.oslot + ((size_t)pb * HKV + g) * D, r, tid);
+                __syncwarp();
+                if (lane == 0) {
+                    signal_add(c_o(p, l, g), 1u);
+                    stamp(p, l, 8);
+                }
             }
         }
         // ---------------- M1: x + group slots -> norm -> gate/up -> SwiGLU -> down rows -> cluster slot
@@ -957,16 +1038,17 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
         xm[0] = xa[0]; xm[1] = xa[1]; xm[2] = xa[2]; xm[3] = xa[3];
         add_slots(xm, p.oslot + (size_t)pb * HKV * D, HKV, k0);
         if (tid == 0) stamp(p, l, 10);
-        norm_into_h(sm, xm, k0, w_post, p.eps, tid);
+        const float s_post = norm_into_h(sm, xm, k0, w_post, p.eps, tid);
         if (tid == 0) stamp(p, l, 17);
         const int np2 = w.p1 - w.p0;
-        ok = cs.dot_rows(2 * np2, ok);
-        if (tid == 0) stamp(p, l, 11);
-        bar_consumers();
-        for (int j = tid; j < np2; j += 256) {
-            const float gt = sm.res[2 * j], up = sm.res[2 * j + 1];
-            sm.coef[j] = gt / (1.0f + expf(-gt)) * up;
+        {
+            // rows 2 u, 2 u + 1 (gate, up of SwiGLU unit u = 8 (lane >> 3) + cw) sit in lanes 4 apart
+            const float v = cs.dot_rows(2 * np2, ok) * s_post;
+            const float up = __shfl_xor_sync(0xffffffffu, v, 4);
+            const int u = 8 * (lane >> 3) + cw;
+            if ((lane & 7) == 0 && u < np2) sm.coef[u] = v / (1.0f + expf(-v)) * up;
         }
+        if (tid == 0) stamp(p, l, 11);
         bar_consumers();
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
         ok = cs.scaled_rows(np2, acc, ok);
@@ -977,12 +1059,13 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
             if (ok && more) mbar_arrive_expect_tx(&sm.bar_redd, RED_BYTES);   // next layer's phase
             stamp(p, l, 13);
         }
-        if (ok) store_reduced(sm.red_d, p.dslot + ((size_t)pb * MAX_CLUSTERS + w.cid) * D, r, tid);
-        bar_consumers();
-        if (tid == 0) {
-            signal_add(c_x(p, l, w.cid), 1u);
-            stamp(p, l, 14);
-
+        if (cw == 0) {
+            if (ok) store_reduced(sm.red_d, p.dslot + ((size_t)pb * MAX_CLUSTERS + w.cid) * D, r, tid);
+            __syncwarp();
+            if (lane == 0) {
+                signal_add(c_x(p, l, w.cid), 1u);
+                stamp(p, l, 14);
+            }
         }
     }
     // ---------------- LM head: final norm, tied embedding rows, argmax
@@ -999,12 +1082,12 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
         if (tid == 0) stamp(p, p.n_layers, 1);
         float xf[4] = {xm[0], xm[1], xm[2], xm[3]};
         add_slots(xf, p.dslot + (size_t)pl * MAX_CLUSTERS * D, NC, k0);
-        norm_into_h(sm, xf, k0, w_fin, p.eps, tid);
+        const float s_fin = norm_into_h(sm, xf, k0, w_fin, p.eps, tid);
         float hreg[4][8];
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) hreg[i][e] = sm.h[8 * lane + 256 * i + e];
+            for (int e = 0; e < 8; ++e) hreg[i][e] = sm.h[8 * lane + 256 * i + e] * s_fin;
         float best = -INFINITY;
         int bidx = 0x7FFFFFFF;
         const int nv = w.v1 - w.v0;
@@ -1128,7 +1211,8 @@ FusedDecode* fused_create(const FusedWeights& fw, int n_layers, int V, float eps
     const int nc = max_clusters < MAX_CLUSTERS ? max_clusters : MAX_CLUSTERS;
     if (nc < HKV) return nullptr;
     const int G = CL * nc;
-    if (2 * ((INTER + G - 1) / G) > MAX_ROWS) return nullptr;
+    // dot_rows takes at most 4 stages, scaled_rows at most 2
+    if (2 * ((INTER + G - 1) / G) > 4 * ROWS_PER_STAGE || ODIMS > 2 * ROWS_PER_STAGE) return nullptr;
     FusedDecode* f = new FusedDecode();
     f->G = G;
     f->n_clusters = nc;
