@@ -127,15 +127,51 @@ class LayerCache:
         self.pos = np.concatenate([self.pos, np.asarray(pos, dtype=np.int64)])
 
 
+# ---------------------------------------------------------------- weight-only int8 (not in the article)
+# The article's "What the script leaves out" section names quantisation without defining one.
+# Reading used here: symmetric int8 per output channel (per row of an [out][in] matrix, and per
+# vocabulary row of the tied embedding / LM head), computed in float32 with IEEE division:
+#   scale_r = float32(max_c |w_rc|) / 127,   q_rc = round_half_even(float32(w_rc) / scale_r),
+# codes clamped to [-127, 127]; a row of zeros has scale 0 and codes 0.  The model then uses the
+# dequantised weights q_rc * scale_r.
+QUANTISED_SUFFIXES = ("q_proj.weight", "k_proj.weight", "v_proj.weight", "o_proj.weight",
+                      "gate_proj.weight", "up_proj.weight", "down_proj.weight")
+
+
+def quantize_rows_int8(w) -> tuple[np.ndarray, np.ndarray]:
+    """Per-row symmetric int8 codes and float32 scales of a [rows][cols] matrix (bf16 or float)."""
+    w32 = bf16_to_f64(w).astype(np.float32) if isinstance(w, torch.Tensor) else np.asarray(w, np.float32)
+    amax = np.max(np.abs(w32), axis=1).astype(np.float32)
+    scale = (amax / np.float32(127)).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1)).astype(np.float32)
+    q = np.rint((w32 / safe[:, None]).astype(np.float32))
+    q = np.where(scale[:, None] > 0, np.clip(q, -127, 127), 0).astype(np.int8)
+    return q, scale
+
+
+def dequantize_rows_int8(q: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    """The weights the quantised model computes with: q_rc * scale_r, in float64."""
+    return q.astype(np.float64) * scale.astype(np.float64)[:, None]
+
+
 class Qwen3Oracle:
-    """The model of steps 2-8 over one sequence at a time, weights as float64 numpy arrays."""
+    """The model of steps 2-8 over one sequence at a time, weights as float64 numpy arrays.
+
+    weight_bits = 8: the projection matrices and the tied embedding are replaced by their
+    dequantised per-row int8 values (quantize_rows_int8); norm weights are kept."""
 
     def __init__(self, weights: dict, shape, eps: float = EPS, theta: float = THETA,
-                 kv_round_bf16: bool = False):
+                 kv_round_bf16: bool = False, weight_bits: int = 16):
         self.shape = shape
         self.eps, self.theta = eps, theta
         self.kv_round_bf16 = kv_round_bf16
         self.W = {name: bf16_to_f64(t) for name, t in weights.items()}
+        if weight_bits == 8:
+            for name in self.W:
+                if name == "model.embed_tokens.weight" or name.endswith(QUANTISED_SUFFIXES):
+                    self.W[name] = dequantize_rows_int8(*quantize_rows_int8(self.W[name]))
+        elif weight_bits != 16:
+            raise ValueError("weight_bits must be 16 or 8")
 
     # Step 5: attention with grouped query heads
     def attention(self, x, layer, cache, positions):

@@ -480,3 +480,44 @@ def test_synth_is_deterministic_and_scaled():
     assert c.equal(a[50000:51000])
     ids = synth.token_ids(0, 0, 10000, 151936)
     assert int(ids.min()) >= 0 and int(ids.max()) < 151936
+
+
+# ---------------------------------------------------------------- weight-only int8 (reading of the
+# article's "What the script leaves out" section: per-output-channel symmetric int8)
+def test_int8_quantiser_worked_example_with_half_even_ties():
+    # max |w| = 127/128 makes the scale exactly 2^-7, so w / scale is exact and the ties are real
+    row = np.array([[127 / 128, 0.5, 64.5 / 128, 65.5 / 128, -1.5 / 128, -0.5 / 128, 0.0, -127 / 128]])
+    q, s = R.quantize_rows_int8(row)
+    assert s.dtype == np.float32 and s[0] == np.float32(2.0 ** -7)
+    assert q.tolist() == [[127, 64, 64, 66, -2, 0, 0, -127]]
+
+
+def test_int8_quantiser_bounds_and_zero_rows():
+    rng = np.random.default_rng(5)
+    w = rng.normal(0, 0.02, size=(64, 96)).astype(np.float32)
+    w[3] = 0.0
+    q, s = R.quantize_rows_int8(w)
+    assert q.dtype == np.int8 and np.abs(q.astype(np.int32)).max() <= 127
+    assert s[3] == 0 and not q[3].any()
+    nz = s > 0
+    # the largest element of each row maps to +-127
+    assert (np.abs(q[nz].astype(np.int32)).max(axis=1) == 127).all()
+    # rounding to the nearest code: |w - q s| <= s / 2 (plus float32 rounding of the quotient)
+    err = np.abs(w.astype(np.float64) - R.dequantize_rows_int8(q, s))
+    assert (err <= s.astype(np.float64)[:, None] * (0.5 + 1e-5) + 1e-12).all()
+    # a per-row rescale of the input rescales the scale and keeps the codes
+    q2, s2 = R.quantize_rows_int8(w * np.float32(4.0))
+    assert (q2 == q).all() and np.allclose(s2, 4 * s, rtol=1e-6)
+
+
+def test_int8_oracle_replaces_projections_and_embedding_only(tiny_shape):
+    w = synth.make_weights(tiny_shape, seed=3)
+    o16 = R.Qwen3Oracle(w, tiny_shape)
+    o8 = R.Qwen3Oracle(w, tiny_shape, weight_bits=8)
+    for name, v in o16.W.items():
+        if name == "model.embed_tokens.weight" or name.endswith(R.QUANTISED_SUFFIXES):
+            q, s = R.quantize_rows_int8(w[name])
+            assert np.array_equal(o8.W[name], R.dequantize_rows_int8(q, s)), name
+            assert not np.array_equal(o8.W[name], v), name
+        else:
+            assert np.array_equal(o8.W[name], v), name
