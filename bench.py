@@ -11,6 +11,8 @@ Workloads (--workload; the default is the headline):
   prefill          prefill of 8 x 2048 random tokens (causal), last-token logits.
   decode_bs16_32k  16 sequences at cache length 32768 (synthetic caches, ~60 GB of
                    bf16 KV), greedy decode steps at positions 32768 .. 32768 + K - 1.
+  decode_bs1_int8  decode_bs1 with weight-only int8 weights (one power-of-two scale per
+                   output channel): the fused batch-1 kernel streams the int8 codes.
 The other workloads are also measured briefly and reported under "secondary".
 
 Random-init weights (seeded, N(0, 0.02)-shaped) and random token ids: no dataset,
@@ -49,6 +51,10 @@ LAYER_PARAMS = (S.n_heads * S.head_dim * S.hidden + 2 * S.n_kv_heads * S.head_di
                 S.hidden * S.n_heads * S.head_dim + 3 * S.intermediate * S.hidden)
 NORM_BYTES = 2 * (2 * S.hidden + 2 * S.head_dim)
 WEIGHT_BYTES = S.n_layers * (2 * LAYER_PARAMS + NORM_BYTES) + 2 * S.hidden + 2 * S.vocab * S.hidden
+# int8 codes + one fp32 scale per output channel (q|k|v rows, o_proj rows, gate/up rows, down rows)
+SCALES_PER_LAYER = (S.n_heads + 2 * S.n_kv_heads) * S.head_dim + S.hidden + 2 * S.intermediate + S.hidden
+WEIGHT_BYTES_INT8 = (S.n_layers * (LAYER_PARAMS + 4 * SCALES_PER_LAYER + NORM_BYTES) + 2 * S.hidden +
+                     S.vocab * S.hidden + 4 * S.vocab)
 KV_BYTES_PER_POS = S.n_layers * 2 * S.n_kv_heads * S.head_dim * 2          # 114,688 B per cached position
 KV_LAYER_BYTES_PER_POS = KV_BYTES_PER_POS // S.n_layers                     # 4,096 B
 PROMPT, PREFILL_B, PREFILL_T, BS64, LONG_B, LONG_L = 512, 8, 2048, 64, 16, 32768
@@ -57,15 +63,19 @@ METRICS = {
     "decode_bs64": "decode tok/s @bs64 (Qwen3-0.6B shape, ragged caches 128..4096, sampled)",
     "prefill": "prefill tok/s (Qwen3-0.6B shape, 8 x 2048 causal)",
     "decode_bs16_32k": "decode tok/s @bs16 (Qwen3-0.6B shape, caches at 32768, greedy)",
+    "decode_bs1_int8": "decode tok/s @bs1 (Qwen3-0.6B shape, weight-only int8, 512-token prompt, greedy)",
 }
 
 
 def config_of(name: str, K: int) -> dict:
     """The workload description both arms print (no model keys: the shape is in the metric)."""
     l2 = "inputs larger than L2 (1.19 GB of weights streamed per step), no flush"
-    if name == "decode_bs1":
-        return {"workload": f"decode bs1, prompt {PROMPT}, timed cache positions {PROMPT}..{PROMPT + K - 1}, greedy",
-                "global_batch": 1, "prompt": PROMPT, "cache_start": PROMPT, "cache_end": PROMPT + K, "l2": l2}
+    if name in ("decode_bs1", "decode_bs1_int8"):
+        q8 = name == "decode_bs1_int8"
+        return {"workload": f"decode bs1, prompt {PROMPT}, timed cache positions {PROMPT}..{PROMPT + K - 1}, greedy"
+                            + (", weight-only int8 per output channel" if q8 else ""),
+                "global_batch": 1, "prompt": PROMPT, "cache_start": PROMPT, "cache_end": PROMPT + K,
+                "weights": "int8 codes + fp32 scale per output channel" if q8 else "bf16", "l2": l2}
     if name == "decode_bs64":
         return {"workload": "decode bs64, ragged paged caches 128..4096, T 0.7 / top-k 50 / top-p 0.9",
                 "global_batch": BS64, "page": PAGE, "l2": l2}
@@ -272,6 +282,13 @@ class DecodeBs1:
         self.kv.close()
 
 
+class DecodeBs1Int8(DecodeBs1):
+    """DecodeBs1 on the weight-only int8 model: the fused kernel streams 0.60 GB of codes a step."""
+
+    def bytes_per_step(self, K):
+        return WEIGHT_BYTES_INT8 + sum((PROMPT + i + 1) * KV_BYTES_PER_POS for i in range(K)) / K
+
+
 class BatchDecode:
     """Batched decode over synthetic paged caches, one step per sequence per timed step."""
     roofline_class = "attn"
@@ -403,6 +420,13 @@ def oracle_rate(workload: str, max_seconds=15.0):
     import numpy as np
     from oracle import qwen3_c as C
     w = synth.make_weights(S)
+    if workload == "decode_bs1_int8":
+        # the oracle's own quantiser; the dequantised weights are exactly bf16 values
+        from oracle import qwen3_ref as R
+        for k in list(w):
+            if k == "model.embed_tokens.weight" or k.endswith(R.QUANTISED_SUFFIXES):
+                deq = R.dequantize_rows_int8(*R.quantize_rows_int8(w[k]))
+                w[k] = torch.from_numpy(deq.astype(np.float32)).to(torch.bfloat16)
     orc = C.COracle(w, S)
     threads = C.threads()
     if workload == "prefill":
@@ -469,6 +493,8 @@ def run_reference(args):
 def make_workload(name, bd, model, K, W):
     if name == "decode_bs1":
         return DecodeBs1(bd, model, max(K, W))
+    if name == "decode_bs1_int8":
+        return DecodeBs1Int8(bd, model, max(K, W))
     if name == "decode_bs64":
         return DecodeBs64(bd, model, max(K, W))
     if name == "decode_bs16_32k":
@@ -500,8 +526,9 @@ def measure(name, bd, model, K, W, hbm, tf_burst):
     else:
         nbytes = wl.roofline_bytes(K)
         ach = nbytes / (cls_ms / 1e3) / 1e9
-        what = ("decode step (the fused batch-1 kernel)" if name == "decode_bs1"
-                else "split-KV decode attention + merge (all 28 layers of a step)")
+        what = {"decode_bs1": "decode step (the fused batch-1 kernel)",
+                "decode_bs1_int8": "decode step (the fused batch-1 kernel streaming int8 weights)"}.get(
+                    name, "split-KV decode attention + merge (all 28 layers of a step)")
         out["roofline"] = {"bound": "hbm", "kernel": what, "achieved": ach, "peak": hbm, "unit": "GB/s",
                            "frac": ach / hbm, "traffic": ncu_traffic(name), "algorithmic_bytes": nbytes,
                            "kernel_ms": cls_ms,
@@ -543,8 +570,21 @@ def main():
     model = bd.Model(w, S, max_batch=64, max_tokens=PREFILL_B * PREFILL_T)
     del w
     torch.cuda.empty_cache()
+    models = {"bf16": model}
+
+    def model_for(name):
+        """The int8 workload runs on its own context (weights quantised at qw_init)."""
+        if name != "decode_bs1_int8":
+            return models["bf16"]
+        if "int8" not in models:
+            w8 = synth.make_weights(S, device="cuda")
+            models["int8"] = bd.Model(w8, S, max_batch=8, max_tokens=1024, weight_bits=8)
+            del w8
+            torch.cuda.empty_cache()
+        return models["int8"]
+
     with ClockSampler(torch.cuda.current_device()) as clk:
-        m = measure(args.workload, bd, model, args.steps, args.warmup, hbm, tf_burst)
+        m = measure(args.workload, bd, model_for(args.workload), args.steps, args.warmup, hbm, tf_burst)
     m["roofline"]["peak_kind"] = f"{peak_kind} ({'copy bandwidth' if m['roofline']['unit'] == 'GB/s' else 'bf16 burst'})"
     line = {"metric": METRICS[args.workload], "value": m["value"], "unit": "tok/s", "n_gpus": 1,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": m["ms_per_step"], "higher_is_better": True,
@@ -559,8 +599,8 @@ def main():
         for name in METRICS:
             if name == args.workload:
                 continue
-            K2 = 64 if name == "decode_bs1" else (16 if name == "decode_bs16_32k" else 5)
-            r = measure(name, bd, model, K2, 3, hbm, tf_burst)
+            K2 = 64 if name in ("decode_bs1", "decode_bs1_int8") else (16 if name == "decode_bs16_32k" else 5)
+            r = measure(name, bd, model_for(name), K2, 3, hbm, tf_burst)
             sec[name] = {"tok_s": r["value"], "ms_per_step": r["ms_per_step"], "roofline": r["roofline"],
                          "e2e_tok_s": r["e2e"]["value"], "kernels": r["kernels"], "config": config_of(name, K2)}
             torch.cuda.empty_cache()
@@ -569,7 +609,8 @@ def main():
         v, sample, threads = oracle_rate(args.workload)
         line["cpu_baseline"] = {"value": v, "unit": "tok/s", "cores": threads, "kind": "oracle", "sample": sample}
     print(json.dumps(line), flush=True)
-    model.close()
+    for m_ in models.values():
+        m_.close()
 
 
 if __name__ == "__main__":

@@ -79,6 +79,14 @@ typedef struct qw_config {
     int32_t debug_hidden;  /* nonzero: keep the residual after every layer for qw_debug_hidden */
     float rms_eps;
     double rope_theta;
+    /* 16: bf16 weights as given.  8: weight-only int8, one scale per output channel (per row
+     * of each projection and of the tied embedding): scale = the smallest power of two >=
+     * max|w| / 127 (that quotient in IEEE fp32), code = w / scale rounded half to even, within
+     * +-127.  The model then computes with the dequantised weights code * scale on every path
+     * (exactly representable in bf16); the fused batch-1 decode streams the int8 codes (half
+     * the bytes).  Not in the article, whose "What the script leaves out" section names
+     * quantisation without defining one. */
+    int32_t weight_bits;
 } qw_config;
 
 /* Weights as the checkpoint names them (Step 5-8 code): bf16 bit patterns,

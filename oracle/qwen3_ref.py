@@ -130,19 +130,30 @@ class LayerCache:
 # ---------------------------------------------------------------- weight-only int8 (not in the article)
 # The article's "What the script leaves out" section names quantisation without defining one.
 # Reading used here: symmetric int8 per output channel (per row of an [out][in] matrix, and per
-# vocabulary row of the tied embedding / LM head), computed in float32 with IEEE division:
-#   scale_r = float32(max_c |w_rc|) / 127,   q_rc = round_half_even(float32(w_rc) / scale_r),
-# codes clamped to [-127, 127]; a row of zeros has scale 0 and codes 0.  The model then uses the
-# dequantised weights q_rc * scale_r.
+# vocabulary row of the tied embedding / LM head) with a power-of-two scale:
+#   t_r = float32(max_c |w_rc|) / 127 (IEEE float32 division),
+#   scale_r = the smallest power of two >= t_r,
+#   q_rc = round_half_even(w_rc / scale_r) (exact: a division by a power of two), in [-127, 127];
+# a row of zeros has scale 0 and codes 0.  The model computes with q_rc * scale_r, which (seven
+# magnitude bits times a power of two) is exactly representable in bf16, so a path that streams
+# the codes and a path that streams bf16 compute with the same weights.
 QUANTISED_SUFFIXES = ("q_proj.weight", "k_proj.weight", "v_proj.weight", "o_proj.weight",
                       "gate_proj.weight", "up_proj.weight", "down_proj.weight")
 
 
+def pow2_ceil(t: np.ndarray) -> np.ndarray:
+    """Smallest power of two >= t for positive float32 t (0 stays 0), as float32."""
+    t = np.asarray(t, np.float32)
+    m, e = np.frexp(t)                       # t = m * 2^e, m in [0.5, 1)
+    s = np.ldexp(np.float32(1), np.where(m == 0.5, e - 1, e)).astype(np.float32)
+    return np.where(t > 0, s, np.float32(0)).astype(np.float32)
+
+
 def quantize_rows_int8(w) -> tuple[np.ndarray, np.ndarray]:
-    """Per-row symmetric int8 codes and float32 scales of a [rows][cols] matrix (bf16 or float)."""
+    """Per-row symmetric int8 codes and power-of-two float32 scales of a [rows][cols] matrix."""
     w32 = bf16_to_f64(w).astype(np.float32) if isinstance(w, torch.Tensor) else np.asarray(w, np.float32)
     amax = np.max(np.abs(w32), axis=1).astype(np.float32)
-    scale = (amax / np.float32(127)).astype(np.float32)
+    scale = pow2_ceil((amax / np.float32(127)).astype(np.float32))
     safe = np.where(scale > 0, scale, np.float32(1)).astype(np.float32)
     q = np.rint((w32 / safe[:, None]).astype(np.float32))
     q = np.where(scale[:, None] > 0, np.clip(q, -127, 127), 0).astype(np.int8)

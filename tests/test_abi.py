@@ -47,11 +47,12 @@ def test_config_default_is_qwen3_0_6b(lib):
     assert (cfg.n_layers, cfg.hidden, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.intermediate, cfg.vocab) == \
         (28, 1024, 16, 8, 128, 3072, 151936)
     assert abs(cfg.rms_eps - 1e-6) < 1e-12 and cfg.rope_theta == 1e6
+    assert cfg.weight_bits == 16
 
 
 @pytest.mark.parametrize("field,value", [("head_dim", 64), ("hidden", 1000), ("n_kv_heads", 3),
                                          ("intermediate", 100), ("vocab", 151937), ("max_batch", 0),
-                                         ("max_tokens", 0), ("n_layers", 0)])
+                                         ("max_tokens", 0), ("n_layers", 0), ("weight_bits", 4)])
 def test_init_rejects_bad_config_without_touching_the_gpu(lib, field, value):
     from transformer_decode_qwen3_gb300 import binding
     cfg = binding.QwConfig()

@@ -61,7 +61,7 @@ def _greedy(model, bd, logits):
     return ids.cpu().numpy()
 
 
-def _prompt_then_greedy(full, T, steps, call, path=0):
+def _prompt_then_greedy(full, T, steps, call, path=0, min_checked=0.5):
     bd, model, orc = full
     n_pages = math.ceil((T + steps) / Q.PAGE) + 1
     kv = bd.KVPool(model, n_pages)
@@ -89,7 +89,8 @@ def _prompt_then_greedy(full, T, steps, call, path=0):
     model.check()
     assert max(errs) < Q.LOGIT_TOL, f"worst logits rel L2 {max(errs):.2e} at step {int(np.argmax(errs))}"
     checked = Q.assert_tokens_match(gpu_ids, ref_rows, ref_ids)
-    assert checked >= len(gpu_ids) // 2
+    assert checked >= int(len(gpu_ids) * min_checked), f"only {checked} of {len(gpu_ids)} steps had a clear top-1"
+    assert checked >= 1
     return max(errs)
 
 

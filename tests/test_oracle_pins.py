@@ -490,6 +490,14 @@ def test_int8_quantiser_worked_example_with_half_even_ties():
     q, s = R.quantize_rows_int8(row)
     assert s.dtype == np.float32 and s[0] == np.float32(2.0 ** -7)
     assert q.tolist() == [[127, 64, 64, 66, -2, 0, 0, -127]]
+    # max |w| = 1.0: t = 1/127 rounds up to the power of two 2^-6, codes on that step
+    q, s = R.quantize_rows_int8(np.array([[1.0, -0.5, 0.25, 3 / 128]]))
+    assert s[0] == np.float32(2.0 ** -6) and q.tolist() == [[64, -32, 16, 2]]
+
+
+def test_int8_power_of_two_scale_rule():
+    t = np.array([2.0 ** -7, 1.0001 * 2.0 ** -7, 0.9999 * 2.0 ** -7, 3.0, 0.0], np.float32)
+    assert R.pow2_ceil(t).tolist() == [2.0 ** -7, 2.0 ** -6, 2.0 ** -7, 4.0, 0.0]
 
 
 def test_int8_quantiser_bounds_and_zero_rows():
@@ -500,14 +508,21 @@ def test_int8_quantiser_bounds_and_zero_rows():
     assert q.dtype == np.int8 and np.abs(q.astype(np.int32)).max() <= 127
     assert s[3] == 0 and not q[3].any()
     nz = s > 0
-    # the largest element of each row maps to +-127
-    assert (np.abs(q[nz].astype(np.int32)).max(axis=1) == 127).all()
-    # rounding to the nearest code: |w - q s| <= s / 2 (plus float32 rounding of the quotient)
-    err = np.abs(w.astype(np.float64) - R.dequantize_rows_int8(q, s))
-    assert (err <= s.astype(np.float64)[:, None] * (0.5 + 1e-5) + 1e-12).all()
-    # a per-row rescale of the input rescales the scale and keeps the codes
+    # scales are powers of two with max/127 <= scale < 2 max/127, so the row's largest code is in [64, 127]
+    m, _ = np.frexp(s[nz])
+    assert (m == 0.5).all()
+    amax = np.abs(w[nz]).max(axis=1)
+    assert ((amax / 127 <= s[nz] * (1 + 1e-6)) & (s[nz] < 2 * amax / 127)).all()
+    top = np.abs(q[nz].astype(np.int32)).max(axis=1)
+    assert ((top >= 64) & (top <= 127)).all()
+    # rounding to the nearest code: |w - q s| <= s / 2, exactly (the division is by a power of two)
+    deq = R.dequantize_rows_int8(q, s)
+    assert (np.abs(w.astype(np.float64) - deq) <= s.astype(np.float64)[:, None] / 2).all()
+    # the dequantised weights are exactly representable in bf16
+    assert np.array_equal(R.round_to_bf16(deq), deq)
+    # a power-of-two rescale of the input rescales the scale and keeps the codes
     q2, s2 = R.quantize_rows_int8(w * np.float32(4.0))
-    assert (q2 == q).all() and np.allclose(s2, 4 * s, rtol=1e-6)
+    assert (q2 == q).all() and np.array_equal(s2, 4 * s)
 
 
 def test_int8_oracle_replaces_projections_and_embedding_only(tiny_shape):

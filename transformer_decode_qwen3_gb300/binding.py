@@ -35,7 +35,8 @@ class QwConfig(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("hidden", ctypes.c_int32), ("n_heads", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("intermediate", ctypes.c_int32),
                 ("vocab", ctypes.c_int32), ("max_batch", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
-                ("debug_hidden", ctypes.c_int32), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_double)]
+                ("debug_hidden", ctypes.c_int32), ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_double),
+                ("weight_bits", ctypes.c_int32)]
 
 
 _PP = ctypes.POINTER(ctypes.c_void_p)
@@ -122,7 +123,7 @@ def _stream(stream) -> int | None:
 
 
 def default_config(shape: ModelShape | None = None, max_batch: int = 64, max_tokens: int = 16384,
-                   debug_hidden: bool = False) -> QwConfig:
+                   debug_hidden: bool = False, weight_bits: int = 16) -> QwConfig:
     lib = load()
     cfg = QwConfig()
     lib.qw_config_default(ctypes.byref(cfg))
@@ -131,6 +132,7 @@ def default_config(shape: ModelShape | None = None, max_batch: int = 64, max_tok
         cfg.n_kv_heads, cfg.head_dim, cfg.intermediate, cfg.vocab = (shape.n_kv_heads, shape.head_dim,
                                                                      shape.intermediate, shape.vocab)
     cfg.max_batch, cfg.max_tokens, cfg.debug_hidden = max_batch, max_tokens, int(debug_hidden)
+    cfg.weight_bits = weight_bits
     return cfg
 
 
@@ -138,10 +140,10 @@ class Model:
     """A qw_ctx: weights uploaded from a name -> bf16 tensor dict (host or device)."""
 
     def __init__(self, weights: dict, shape: ModelShape, max_batch: int = 64, max_tokens: int = 16384,
-                 debug_hidden: bool = False):
+                 debug_hidden: bool = False, weight_bits: int = 16):
         lib = load()
         self.shape = shape
-        self.cfg = default_config(shape, max_batch, max_tokens, debug_hidden)
+        self.cfg = default_config(shape, max_batch, max_tokens, debug_hidden, weight_bits)
         L = shape.n_layers
         t0 = weights["model.embed_tokens.weight"]
         on_device = t0.is_cuda

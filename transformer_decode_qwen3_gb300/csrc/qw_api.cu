@@ -64,6 +64,7 @@ struct qw_ctx {
     int dev = 0, n_sm = 0;
     int qkv_dim = 0, attn_dim = 0;
     uint8_t* wbuf = nullptr;
+    uint8_t* qbuf = nullptr;   // weight_bits 8: int8 codes and per-output-channel scales
     uint16_t* E = nullptr;
     float* final_norm = nullptr;
     float* inv_freq = nullptr;
@@ -143,6 +144,7 @@ void qw_config_default(qw_config* c) {
     c->debug_hidden = 0;
     c->rms_eps = 1e-6f;
     c->rope_theta = 1e6;
+    c->weight_bits = 16;
 }
 
 const char* qw_last_error_message(void) { return g_last_error.c_str(); }
@@ -160,6 +162,7 @@ static int validate_config(const qw_config* c) {
     if (c->max_batch < 1 || c->max_batch > 256) return fail(QW_EINVAL, "max_batch must be in [1, 256]");
     if (c->max_tokens < 1 || c->max_tokens > (1 << 20)) return fail(QW_EINVAL, "max_tokens must be in [1, 2^20]");
     if (!(c->rms_eps > 0.f) || !(c->rope_theta > 1.0)) return fail(QW_EINVAL, "rms_eps > 0 and rope_theta > 1 required");
+    if (c->weight_bits != 16 && c->weight_bits != 8) return fail(QW_EINVAL, "weight_bits must be 16 or 8");
     return QW_OK;
 }
 
@@ -184,6 +187,7 @@ static void free_ctx(qw_ctx* c) {
     for (cudaEvent_t e : c->prof.ev) cudaEventDestroy(e);
     if (c->fused) fused_destroy(c->fused);
     if (c->wbuf) cudaFree(c->wbuf);
+    if (c->qbuf) cudaFree(c->qbuf);
     if (c->wsbuf) cudaFree(c->wsbuf);
     delete c;
 }
@@ -311,6 +315,63 @@ int qw_init(const qw_config* cfg, const qw_weights* w, qw_ctx** out) {
         return fail(QW_ECUDA, "cuTensorMapEncodeTiled failed for the embedding");
     }
 
+    // ---- weight-only int8: codes and scales per output channel; the bf16 matrices become the
+    // dequantised weights, so every path (prefill, decode batches, the fused batch-1 kernel that
+    // streams the codes) computes with the same model
+    FusedWeights fw;
+    if (c.weight_bits == 8) {
+        size_t qoff = 0;
+        auto qtake = [&](size_t bytes) {
+            size_t o = qoff;
+            qoff = align_up(qoff + bytes, A);
+            return o;
+        };
+        struct QOffs { size_t qkv, o, gu, dn, sqkv, so, sgu, sd; };
+        const size_t oEq = qtake((size_t)V * D), osE = qtake((size_t)V * 4);
+        std::vector<QOffs> qo(c.n_layers);
+        for (int l = 0; l < c.n_layers; ++l) {
+            qo[l].qkv = qtake((size_t)ctx->qkv_dim * D);
+            qo[l].o = qtake((size_t)D * ctx->attn_dim);
+            qo[l].gu = qtake((size_t)2 * I * D);
+            qo[l].dn = qtake((size_t)D * I);
+            qo[l].sqkv = qtake((size_t)ctx->qkv_dim * 4);
+            qo[l].so = qtake((size_t)D * 4);
+            qo[l].sgu = qtake((size_t)2 * I * 4);
+            qo[l].sd = qtake((size_t)D * 4);
+        }
+        if (cudaMalloc(&ctx->qbuf, qoff) != cudaSuccess) {
+            free_ctx(ctx);
+            return fail(QW_ENOMEM, "int8 weight allocation failed");
+        }
+        uint8_t* Q = ctx->qbuf;
+        auto quant = [&](uint16_t* Wm, int rows, int cols, size_t oq, size_t os) {
+            return launch_quantize_rows(Wm, rows, cols, cols, (int8_t*)(Q + oq), (float*)(Q + os), 0);
+        };
+        int qrc = quant(ctx->E, V, D, oEq, osE);
+        fw.q8 = true;
+        fw.Eq = (const int8_t*)(Q + oEq);
+        fw.sE = (const float*)(Q + osE);
+        for (int l = 0; l < c.n_layers && qrc == QW_OK; ++l) {
+            LayerW& Lw = ctx->L[l];
+            if ((qrc = quant(Lw.wqkv, ctx->qkv_dim, D, qo[l].qkv, qo[l].sqkv)) ||
+                (qrc = quant(Lw.wo, D, ctx->attn_dim, qo[l].o, qo[l].so)) ||
+                (qrc = quant(Lw.wgu, 2 * I, D, qo[l].gu, qo[l].sgu)) || (qrc = quant(Lw.wd, D, I, qo[l].dn, qo[l].sd)))
+                break;
+            fw.wqkv_q.push_back((const int8_t*)(Q + qo[l].qkv));
+            fw.wo_q.push_back((const int8_t*)(Q + qo[l].o));
+            fw.wgu_q.push_back((const int8_t*)(Q + qo[l].gu));
+            fw.wd_q.push_back((const int8_t*)(Q + qo[l].dn));
+            fw.s_qkv.push_back((const float*)(Q + qo[l].sqkv));
+            fw.s_o.push_back((const float*)(Q + qo[l].so));
+            fw.s_gu.push_back((const float*)(Q + qo[l].sgu));
+            fw.s_d.push_back((const float*)(Q + qo[l].sd));
+        }
+        if (qrc != QW_OK) {
+            free_ctx(ctx);
+            return fail(qrc, "weight quantisation launch failed");
+        }
+    }
+
     // ---- workspaces
     const int T = std::max(c.max_tokens, c.max_batch);
     ctx->max_rows = T;
@@ -366,7 +427,6 @@ int qw_init(const qw_config* cfg, const qw_weights* w, qw_ctx** out) {
         QW_INIT_CUDA(cudaMemset(ctx->err, 0, 64));
     }
     {
-        FusedWeights fw;
         fw.E = ctx->E;
         fw.final_norm = ctx->final_norm;
         fw.inv_freq = ctx->inv_freq;

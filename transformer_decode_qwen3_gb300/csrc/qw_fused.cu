@@ -44,8 +44,10 @@ constexpr int CL = 8;                 // CTAs per cluster
 constexpr int MAX_CLUSTERS = 16;
 constexpr int NS = 6;                 // ring stages
 constexpr int STAGE = 32768;          // bytes per stage
-constexpr int ROW_B = D * 2;          // every streamed row is 1024 bf16
-constexpr int ROWS_PER_STAGE = STAGE / ROW_B;   // 16
+// Streamed weight rows are 1024 wide: bf16 (2 KB, 16 per stage) or, with weight-only int8
+// (Q8), int8 codes (1 KB, 32 per stage) with one fp32 scale per output channel.
+template <bool Q8> constexpr int row_bytes() { return Q8 ? D : 2 * D; }
+template <bool Q8> constexpr int rows_per_stage() { return STAGE / row_bytes<Q8>(); }
 constexpr int PAGE_B = QW_PAGE_SIZE * HD * 2;   // K (or V) of one head in one page: 4 KB
 constexpr int PAGES_PER_STAGE = STAGE / (2 * PAGE_B);  // 4
 constexpr int NCW = 8;                // consumer warps
@@ -67,14 +69,16 @@ constexpr uint32_t PART_BYTES = CL * ODIMS * 4 + CL * 16;  // O of my dims + (M,
 constexpr uint32_t RED_BYTES = CL * OWN * 4;            // 8 partial vectors of my 128 outputs
 
 struct LayerPtrs {
-    const uint16_t *wqkv, *woT, *wgu, *wdT;
+    const uint8_t *wqkv, *woT, *wgu, *wdT;        // rows of bf16 or of int8 codes
     const float *in_norm, *post_norm, *q_norm, *k_norm;
+    const float *s_qkv, *s_o, *s_gu, *s_d;        // int8: scale of each output channel (else null)
 };
 
 struct Params {
     const LayerPtrs* layers;
     int n_layers;
-    const uint16_t* E;
+    const uint8_t* E;        // embedding / tied LM head rows (bf16 or int8 codes)
+    const float* s_E;        // int8: scale of each vocabulary row
     const float* final_norm;
     const float* inv_freq;
     int V;
@@ -185,6 +189,7 @@ struct Smem {
     alignas(16) float res[MAX_ROWS]; // dot products of the current phase
     float coef[MAX_ROWS];            // scale of each row in the scaled-row phases
     float wsum[NCW];
+    float wmax[NCW];
     alignas(16) float qkv_s[512];         // the group's q head 2g | q head 2g+1 | k | v, pushed by the peers
     alignas(16) float part_o[CL][ODIMS];  // attention outputs of my 32 dims from each peer (unnormalised)
     alignas(16) float part_ml[CL][4];     // (max, sum) of both heads from each peer
@@ -320,14 +325,16 @@ struct Seq {
     int l = 0, part = 0, i = 0;   // layer, part, stage within the part
 };
 struct StageDesc {
-    const uint16_t* rows;   // row stages: first row
+    const uint8_t* rows;    // row stages: first row
     int n;                  // rows, or pages
     int pg0;                // page stages: index of the first page in this CTA's page list
     int l;                  // page stages: layer
     bool pages;
 };
 
+template <bool Q8>
 struct Producer {
+    static constexpr int RB = row_bytes<Q8>(), RPS = rows_per_stage<Q8>();
     uint8_t* ring;
     Smem* sm;
     const Params* p;
@@ -343,29 +350,29 @@ struct Producer {
         for (;;) {
             if (q.l > p->n_layers) return false;
             const int part = q.l == p->n_layers ? 5 : q.part;
-            const uint16_t* base = nullptr;
+            const uint8_t* base = nullptr;
             int total = 0;
             bool pages = false;
             if (part == 5) {
-                base = p->E + (size_t)w->v0 * D;
+                base = p->E + (size_t)w->v0 * RB;
                 total = w->v1 - w->v0;
             } else if (part <= 2 && !w->attn) {
                 total = 0;
             } else {
                 const LayerPtrs& L = p->layers[q.l];
-                if (part == 0) base = L.wqkv + (size_t)w->qrow0 * D, total = QROWS;
+                if (part == 0) base = L.wqkv + (size_t)w->qrow0 * RB, total = QROWS;
                 else if (part == 1) pages = true, total = bad_pos ? 0 : w->pg_hi - w->pg_lo;
-                else if (part == 2) base = L.woT + (size_t)w->j0 * D, total = ODIMS;
-                else if (part == 3) base = L.wgu + (size_t)2 * w->p0 * D, total = 2 * (w->p1 - w->p0);
-                else base = L.wdT + (size_t)w->p0 * D, total = w->p1 - w->p0;
+                else if (part == 2) base = L.woT + (size_t)w->j0 * RB, total = ODIMS;
+                else if (part == 3) base = L.wgu + (size_t)2 * w->p0 * RB, total = 2 * (w->p1 - w->p0);
+                else base = L.wdT + (size_t)w->p0 * RB, total = w->p1 - w->p0;
             }
-            const int per = pages ? PAGES_PER_STAGE : ROWS_PER_STAGE;
+            const int per = pages ? PAGES_PER_STAGE : RPS;
             if (q.i * per < total) {
                 d.pages = pages;
                 d.l = q.l;
                 d.n = min(per, total - q.i * per);
                 d.pg0 = q.i * per;
-                d.rows = pages ? nullptr : base + (size_t)q.i * per * D;
+                d.rows = pages ? nullptr : base + (size_t)q.i * per * RB;
                 ++q.i;
                 return true;
             }
@@ -400,7 +407,7 @@ struct Producer {
         while (pf_count <= upto && next(pf, d)) {
             ++pf_count;
             if (!d.pages) {
-                prefetch_l2(d.rows, d.n * ROW_B);
+                prefetch_l2(d.rows, d.n * RB);
             } else {
                 for (int i = 0; i < d.n; ++i) {
                     if (sm->pages[d.pg0 + i] < 0) continue;
@@ -421,8 +428,8 @@ struct Producer {
                 return;
             }
             if (!d.pages) {
-                mbar_arrive_expect_tx(&sm->full[s], d.n * ROW_B);
-                bulk_load(ring + s * STAGE, d.rows, d.n * ROW_B, &sm->full[s]);
+                mbar_arrive_expect_tx(&sm->full[s], d.n * RB);
+                bulk_load(ring + s * STAGE, d.rows, d.n * RB, &sm->full[s]);
             } else {
                 // page i of a stage holds K at i * 8 KB and V at i * 8 KB + 4 KB
                 int valid = 0;
@@ -475,7 +482,45 @@ QW_DEV void add2(uint64_t& acc, uint64_t b) {
 // a bf16 pair (low element in the low half) as packed fp32
 QW_DEV uint64_t bf2_to_f2(uint32_t w) { return pack2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)); }
 
+// int32 d = c + a.lo16 * b.byte0 + a.hi16 * b.byte1 (dp2a.lo) or bytes 2, 3 (dp2a.hi), signed
+QW_DEV int dp2a_lo(int a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.lo.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+QW_DEV int dp2a_hi(int a, uint32_t b, int c) {
+    int d;
+    asm("dp2a.hi.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+// Two values rounded to int16 (round half to even, clamped) packed low, high.
+QW_DEV int pack_i16(float a, float b) {
+    const int ia = max(-32767, min(32767, __float2int_rn(a)));
+    const int ib = max(-32767, min(32767, __float2int_rn(b)));
+    return (ia & 0xFFFF) | (ib << 16);
+}
+// Transposed butterfly over the warp: v[k] (k < n, n a power of two <= 8) of every lane in, on
+// return lanes with (lane >> (5 - log2 n)) == k hold the warp sum of value k.
+template <int N>
+QW_DEV float warp_reduce_n(float (&v)[N]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 16, n = N; n > 1; o >>= 1, n >>= 1) {
+        const bool up = lane & o;
+#pragma unroll
+        for (int k = 0; k < n / 2; ++k) {
+            const float send = up ? v[k] : v[k + n / 2];
+            v[k] = (up ? v[k + n / 2] : v[k]) + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+#pragma unroll
+    for (int o = 16 / N; o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+    return v[0];
+}
+
+template <bool Q8>
 struct Consumer {
+    static constexpr int RB = row_bytes<Q8>(), RPS = rows_per_stage<Q8>();
     uint8_t* ring;
     Smem* sm;
     int* err;
@@ -549,19 +594,19 @@ struct Consumer {
         uint64_t acc[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) acc[k] = 0;
-        const int nst = (nrows + ROWS_PER_STAGE - 1) / ROWS_PER_STAGE;
+        const int nst = (nrows + RPS - 1) / RPS;
         const uint8_t* st0 = phase_wait(nst, ok);
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
             if (s < nst) {
-                const int n = min(ROWS_PER_STAGE, nrows - ROWS_PER_STAGE * s);
+                const int n = min(RPS, nrows - RPS * s);
                 const uint8_t* st = ring + ((it + s) % NS) * STAGE;
                 if (ok) {
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
                         const int r = 2 * cw + j;
                         if (r < n) {
-                            const uint4* ra = (const uint4*)(st + r * ROW_B);
+                            const uint4* ra = (const uint4*)(st + r * RB);
                             uint4 wa[4];
 #pragma unroll
                             for (int i = 0; i < 4; ++i) wa[i] = ra[lane + 32 * i];
@@ -586,44 +631,131 @@ struct Consumer {
         float v[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) v[k] = hsum2(acc[k]);
-        // exchange with lane ^ 16 (^ 8, ^ 4): the upper lane keeps the upper half of its values
+        return warp_reduce_n<8>(v);
+    }
+    // Phase row of the value dot_rows leaves in this lane (lanes 4 k .. 4 k + 3 hold warp row k):
+    // bf16 row 16 (k >> 1) + 2 cw + (k & 1), int8 row 32 (k >> 2) + 4 cw + (k & 3).  Gate and up
+    // of a SwiGLU unit (rows 2u, 2u + 1) sit in lanes 4 apart either way.
+    QW_DEV int lane_row() const {
+        const int k = lane >> 2;
+        return Q8 ? 32 * (k >> 2) + 4 * cw + (k & 3) : 16 * (k >> 1) + 2 * cw + (k & 1);
+    }
+    // int8 rows (32 per stage, at most 2 stages): warp cw takes rows 4 cw .. 4 cw + 3 of every
+    // stage; lane l multiplies columns 16 l + 512 i .. + 15 (i < 2) with the activations rounded
+    // to int16 (h * hinv) by dp2a, exact in int32 (at most 32 * 127 * 32767 per lane and row).
+    // The result is in units of 1 / hinv (times the row's scale, applied by the caller).
+    QW_DEV float dot_rows_q8(int nrows, bool& ok, float hinv) {
+        int hq[16];
 #pragma unroll
-        for (int o = 16, n = 8; o >= 4; o >>= 1, n >>= 1) {
-            const bool up = lane & o;
+        for (int i = 0; i < 2; ++i)
 #pragma unroll
-            for (int k = 0; k < n / 2; ++k) {
-                const float send = up ? v[k] : v[k + n / 2];
-                v[k] = (up ? v[k + n / 2] : v[k]) + __shfl_xor_sync(0xffffffffu, send, o);
+            for (int m4 = 0; m4 < 4; ++m4) {
+                const float4 a = *(const float4*)&sm->h[16 * lane + 512 * i + 4 * m4];
+                hq[8 * i + 2 * m4] = pack_i16(a.x * hinv, a.y * hinv);
+                hq[8 * i + 2 * m4 + 1] = pack_i16(a.z * hinv, a.w * hinv);
+            }
+        int acc[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] = 0;
+        const int nst = (nrows + RPS - 1) / RPS;
+        phase_wait(nst, ok);
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            if (s < nst) {
+                const int n = min(RPS, nrows - RPS * s);
+                const uint8_t* st = ring + ((it + s) % NS) * STAGE;
+                if (ok) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int r = 4 * cw + j;
+                        if (r < n) {
+                            int a = acc[4 * s + j];
+#pragma unroll
+                            for (int i = 0; i < 2; ++i) {
+                                const uint4 w = *(const uint4*)(st + r * RB + 16 * lane + 512 * i);
+                                a = dp2a_lo(hq[8 * i + 0], w.x, a);
+                                a = dp2a_hi(hq[8 * i + 1], w.x, a);
+                                a = dp2a_lo(hq[8 * i + 2], w.y, a);
+                                a = dp2a_hi(hq[8 * i + 3], w.y, a);
+                                a = dp2a_lo(hq[8 * i + 4], w.z, a);
+                                a = dp2a_hi(hq[8 * i + 5], w.z, a);
+                                a = dp2a_lo(hq[8 * i + 6], w.w, a);
+                                a = dp2a_hi(hq[8 * i + 7], w.w, a);
+                            }
+                            acc[4 * s + j] = a;
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm->empty[(it + s) % NS]);
             }
         }
-        v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
-        v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
-        return v[0];
+        it += nst;
+        float v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = (float)acc[k];
+        return warp_reduce_n<8>(v);
+    }
+    // acc (columns 128 cw + 4 lane .. + 3) += sum over the int8 rows r (at most 32, one stage)
+    // of sm->coef[r] * code[r][col]: the coefficients rounded to int16 on a step of max|coef| /
+    // 32767, rows taken in pairs (a byte permute interleaves two rows' codes for dp2a), exact
+    // int32 sums scaled back by the step.  The output channel's scale is applied later.
+    QW_DEV bool scaled_rows_q8(int nrows, float (&acc)[4], bool ok) {
+        float cm = 0.f;
+        for (int r = 0; r < nrows; ++r) cm = fmaxf(cm, fabsf(sm->coef[r]));
+        const float cinv = cm > 0.f ? 32767.0f / cm : 0.f, cstep = cm / 32767.0f;
+        phase_wait(1, ok);
+        int a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+        const uint8_t* col = ring + (it % NS) * STAGE + 128 * cw + 4 * lane;
+        if (ok) {
+#pragma unroll
+            for (int r = 0; r < RPS; r += 2) {
+                if (r < nrows) {
+                    const bool two = r + 1 < nrows;
+                    const uint32_t A = *(const uint32_t*)(col + r * RB);
+                    const uint32_t B = two ? *(const uint32_t*)(col + (r + 1) * RB) : 0u;
+                    const int cp = pack_i16(sm->coef[r] * cinv, two ? sm->coef[r + 1] * cinv : 0.f);
+                    const uint32_t P0 = __byte_perm(A, B, 0x5140), P1 = __byte_perm(A, B, 0x7362);
+                    a0 = dp2a_lo(cp, P0, a0);
+                    a1 = dp2a_hi(cp, P0, a1);
+                    a2 = dp2a_lo(cp, P1, a2);
+                    a3 = dp2a_hi(cp, P1, a3);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->empty[it % NS]);
+        ++it;
+        acc[0] += (float)a0 * cstep;
+        acc[1] += (float)a1 * cstep;
+        acc[2] += (float)a2 * cstep;
+        acc[3] += (float)a3 * cstep;
+        return ok;
     }
     // acc (columns 128 cw + 4 lane .. +3) += sum over streamed rows r of sm->coef[r] * row_r.
     // Each warp covers its own 128 output columns of every row, so no cross-warp sum is needed.
     QW_DEV bool scaled_rows(int nrows, float (&acc)[4], bool ok) {
-        const int nst = (nrows + ROWS_PER_STAGE - 1) / ROWS_PER_STAGE;   // at most 2 (host-checked)
+        const int nst = (nrows + RPS - 1) / RPS;   // at most 2 (host-checked)
         phase_wait(nst, ok);
         uint64_t c01 = pack2(acc[0], acc[1]), c23 = pack2(acc[2], acc[3]), d01 = 0, d23 = 0;
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
             if (s < nst) {
-                const int n = min(ROWS_PER_STAGE, nrows - ROWS_PER_STAGE * s);
+                const int n = min(RPS, nrows - RPS * s);
                 const uint8_t* col = ring + ((it + s) % NS) * STAGE + (128 * cw + 4 * lane) * 2;
-                const float* cf = sm->coef + ROWS_PER_STAGE * s;
+                const float* cf = sm->coef + RPS * s;
                 if (ok) {
                     // two accumulator pairs (even and odd rows) halve the dependent FMA chain
 #pragma unroll
-                    for (int r = 0; r < ROWS_PER_STAGE; r += 2) {
+                    for (int r = 0; r < RPS; r += 2) {
                         if (r < n) {
-                            const uint2 wv = *(const uint2*)(col + r * ROW_B);
+                            const uint2 wv = *(const uint2*)(col + r * RB);
                             const uint64_t aa = pack2(cf[r], cf[r]);
                             ffma2(c01, aa, bf2_to_f2(wv.x));
                             ffma2(c23, aa, bf2_to_f2(wv.y));
                         }
                         if (r + 1 < n) {
-                            const uint2 wv = *(const uint2*)(col + (r + 1) * ROW_B);
+                            const uint2 wv = *(const uint2*)(col + (r + 1) * RB);
                             const uint64_t aa = pack2(cf[r + 1], cf[r + 1]);
                             ffma2(d01, aa, bf2_to_f2(wv.x));
                             ffma2(d23, aa, bf2_to_f2(wv.y));
@@ -646,15 +778,25 @@ struct Consumer {
 // x (4 entries per consumer thread) -> sm.h = x * w, w = this thread's 4 norm weights (loaded
 // ahead, so no global load sits on the critical path); returns 1 / rms(x), by which the products
 // with sm.h are scaled.  One consumer barrier inside.
-QW_DEV float norm_into_h(Smem& sm, const float (&x)[4], int k0, const float4 w, float eps, int tid) {
+QW_DEV float norm_into_h(Smem& sm, const float (&x)[4], int k0, const float4 w, float eps, int tid, float& hmax) {
     float ss = x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3];
+    const float4 h = make_float4(x[0] * w.x, x[1] * w.y, x[2] * w.z, x[3] * w.w);
+    float hm = fmaxf(fmaxf(fabsf(h.x), fabsf(h.y)), fmaxf(fabsf(h.z), fabsf(h.w)));
     ss = warp_sum(ss);
-    if ((tid & 31) == 0) sm.wsum[tid >> 5] = ss;
-    *(float4*)&sm.h[k0] = make_float4(x[0] * w.x, x[1] * w.y, x[2] * w.z, x[3] * w.w);
+    hm = warp_max(hm);
+    if ((tid & 31) == 0) {
+        sm.wsum[tid >> 5] = ss;
+        sm.wmax[tid >> 5] = hm;
+    }
+    *(float4*)&sm.h[k0] = h;
     bar_consumers();
     float tot = 0.f;
+    hmax = 0.f;
 #pragma unroll
-    for (int i = 0; i < NCW; ++i) tot += sm.wsum[i];
+    for (int i = 0; i < NCW; ++i) {
+        tot += sm.wsum[i];
+        hmax = fmaxf(hmax, sm.wmax[i]);
+    }
     return 1.0f / sqrtf(tot / (float)D + eps);
 }
 
@@ -667,7 +809,7 @@ QW_DEV void push_partial(Smem& sm, float (&red)[CL][OWN], uint64_t* bar, const f
 
 // Sum of the 8 peers' partials of this CTA's outputs (fixed order) into dst[128 rank + ..]:
 // threads 0..31 of the consumers, one float4 each.
-QW_DEV void store_reduced(const float (&red)[CL][OWN], float* dst, int rank, int tid) {
+QW_DEV void store_reduced(const float (&red)[CL][OWN], float* dst, int rank, int tid, float4 oscale) {
     if (tid < OWN / 4) {
         float4 t = *(const float4*)&red[0][4 * tid];
 #pragma unroll
@@ -678,6 +820,10 @@ QW_DEV void store_reduced(const float (&red)[CL][OWN], float* dst, int rank, int
             t.z += v.z;
             t.w += v.w;
         }
+        t.x *= oscale.x;
+        t.y *= oscale.y;
+        t.z *= oscale.z;
+        t.w *= oscale.w;
         *(float4*)(dst + OWN * rank + 4 * tid) = t;
     }
 }
@@ -698,6 +844,7 @@ QW_DEV void add_slots(float (&x)[4], const float* base, int n, int k0) {
         }
 }
 
+template <bool Q8>
 __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_decode_kernel(const __grid_constant__ Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* ring = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -748,7 +895,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
             }
         __syncwarp();
         if (lane == 0) {
-            Producer pr{ring, &sm, &p, &w, bad_pos};
+            Producer<Q8> pr{ring, &sm, &p, &w, bad_pos};
             pr.run();
             pr.drain();
         }
@@ -760,7 +907,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
     // ------------------------------------------------ consumers (warps 1..8)
     const int tid = threadIdx.x - 32;  // 0..255
     const int cw = tid >> 5;
-    Consumer cs{ring, &sm, p.err, cw, lane};
+    Consumer<Q8> cs{ring, &sm, p.err, cw, lane};
     bool ok = !bad_pos;
     const int k0 = 4 * tid;  // this thread's 4 residual entries
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)HD);
@@ -770,8 +917,16 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
     // this thread's entries of the residual stream: x before the layer (xa), after attention (xm)
     float xa[4], xm[4];
     {
-        const uint2 e = (tok >= 0 && tok < p.V) ? *(const uint2*)(p.E + (size_t)tok * D + k0) : make_uint2(0, 0);
-        xa[0] = bf16_lo(e.x); xa[1] = bf16_hi(e.x); xa[2] = bf16_lo(e.y); xa[3] = bf16_hi(e.y);
+        const bool tok_ok = tok >= 0 && tok < p.V;
+        if constexpr (Q8) {
+            const uint32_t e = tok_ok ? *(const uint32_t*)(p.E + (size_t)tok * D + k0) : 0u;
+            const float sc = tok_ok ? p.s_E[tok] : 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xa[i] = (float)(int8_t)(e >> (8 * i)) * sc;
+        } else {
+            const uint2 e = tok_ok ? *(const uint2*)(p.E + ((size_t)tok * D + k0) * 2) : make_uint2(0, 0);
+            xa[0] = bf16_lo(e.x); xa[1] = bf16_hi(e.x); xa[2] = bf16_lo(e.y); xa[3] = bf16_hi(e.y);
+        }
         if (c == 0 && tid == 0 && !(tok >= 0 && tok < p.V)) set_error(p.err, QW_ERANGE);
     }
 
@@ -785,6 +940,18 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
         float w_qk[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) w_qk[i] = __ldg((cw < 2 ? L.q_norm : L.k_norm) + lane + 32 * i);
+        // int8: the scales of this lane's q|k|v and gate/up rows and of the outputs this thread stores
+        float s_row_qkv = 1.f, s_row_gu = 1.f;
+        float4 s_out_o = make_float4(1.f, 1.f, 1.f, 1.f), s_out_d = s_out_o;
+        if constexpr (Q8) {
+            const int row = cs.lane_row();
+            if (w.attn) s_row_qkv = __ldg(L.s_qkv + w.qrow0 + row);
+            if (row < 2 * (w.p1 - w.p0)) s_row_gu = __ldg(L.s_gu + 2 * w.p0 + row);
+            if (tid < OWN / 4) {
+                if (w.attn) s_out_o = __ldg((const float4*)(L.s_o + OWN * w.rank + 4 * tid));
+                s_out_d = __ldg((const float4*)(L.s_d + OWN * w.rank + 4 * tid));
+            }
+        }
         const int pb = l & 1;
         const uint32_t par = (uint32_t)(l & 1);
         const bool more = l + 1 < p.n_layers;
@@ -803,10 +970,15 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
         if (tid == 0) stamp(p, l, 1);
         if (w.attn) {
             // ---------------- A1: norm -> this CTA's q|k|v rows -> every peer's qkv_s
-            const float s_in = norm_into_h(sm, xa, k0, w_in, p.eps, tid);
+            float hmax;
+            const float s_in = norm_into_h(sm, xa, k0, w_in, p.eps, tid, hmax);
             {
-                const float v = cs.dot_rows(QROWS, ok);
-                if ((lane & 3) == 0) sm.res[16 * (lane >> 3) + 2 * cw + ((lane >> 2) & 1)] = v * s_in;
+                float v;
+                if constexpr (Q8)
+                    v = cs.dot_rows_q8(QROWS, ok, hmax > 0.f ? 32767.0f / hmax : 0.f) * (hmax / 32767.0f) * s_row_qkv;
+                else
+                    v = cs.dot_rows(QROWS, ok);
+                if ((lane & 3) == 0) sm.res[cs.lane_row()] = v * s_in;
             }
             if (tid == 0) stamp(p, l, 2);
             bar_consumers();
@@ -1008,7 +1180,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
             }
             bar_consumers();
             float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            ok = cs.scaled_rows(ODIMS, acc, ok);
+            if constexpr (Q8) ok = cs.scaled_rows_q8(ODIMS, acc, ok);
+            else ok = cs.scaled_rows(ODIMS, acc, ok);
             if (tid == 0) stamp(p, l, 6);
             if (ok) push_partial(sm, sm.red_o, &sm.bar_redo, acc, cw, lane, r);
             ok = ok && wait_cluster(p, &sm.bar_redo, par, sm);
@@ -1019,7 +1192,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
             // warp 0 stores this CTA's 128 outputs and publishes them (the warp barrier orders its
             // lanes' stores before lane 0's release); the other warps go straight on
             if (cw == 0) {
-                if (ok) store_reduced(sm.red_o, p.oslot + ((size_t)pb * HKV + g) * D, r, tid);
+                if (ok) store_reduced(sm.red_o, p.oslot + ((size_t)pb * HKV + g) * D, r, tid, s_out_o);
                 __syncwarp();
                 if (lane == 0) {
                     signal_add(c_o(p, l, g), 1u);
@@ -1038,20 +1211,27 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
         xm[0] = xa[0]; xm[1] = xa[1]; xm[2] = xa[2]; xm[3] = xa[3];
         add_slots(xm, p.oslot + (size_t)pb * HKV * D, HKV, k0);
         if (tid == 0) stamp(p, l, 10);
-        const float s_post = norm_into_h(sm, xm, k0, w_post, p.eps, tid);
+        float hmax2;
+        const float s_post = norm_into_h(sm, xm, k0, w_post, p.eps, tid, hmax2);
         if (tid == 0) stamp(p, l, 17);
         const int np2 = w.p1 - w.p0;
         {
             // rows 2 u, 2 u + 1 (gate, up of SwiGLU unit u = 8 (lane >> 3) + cw) sit in lanes 4 apart
-            const float v = cs.dot_rows(2 * np2, ok) * s_post;
+            float v;
+            if constexpr (Q8)
+                v = cs.dot_rows_q8(2 * np2, ok, hmax2 > 0.f ? 32767.0f / hmax2 : 0.f) * (hmax2 / 32767.0f) * s_row_gu *
+                    s_post;
+            else
+                v = cs.dot_rows(2 * np2, ok) * s_post;
             const float up = __shfl_xor_sync(0xffffffffu, v, 4);
-            const int u = 8 * (lane >> 3) + cw;
+            const int u = cs.lane_row() >> 1;
             if ((lane & 7) == 0 && u < np2) sm.coef[u] = v / (1.0f + expf(-v)) * up;
         }
         if (tid == 0) stamp(p, l, 11);
         bar_consumers();
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        ok = cs.scaled_rows(np2, acc, ok);
+        if constexpr (Q8) ok = cs.scaled_rows_q8(np2, acc, ok);
+        else ok = cs.scaled_rows(np2, acc, ok);
         if (tid == 0) stamp(p, l, 12);
         if (ok) push_partial(sm, sm.red_d, &sm.bar_redd, acc, cw, lane, r);
         ok = ok && wait_cluster(p, &sm.bar_redd, par, sm);
@@ -1060,7 +1240,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
             stamp(p, l, 13);
         }
         if (cw == 0) {
-            if (ok) store_reduced(sm.red_d, p.dslot + ((size_t)pb * MAX_CLUSTERS + w.cid) * D, r, tid);
+            if (ok) store_reduced(sm.red_d, p.dslot + ((size_t)pb * MAX_CLUSTERS + w.cid) * D, r, tid, s_out_d);
             __syncwarp();
             if (lane == 0) {
                 signal_add(c_x(p, l, w.cid), 1u);
@@ -1082,39 +1262,106 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
         if (tid == 0) stamp(p, p.n_layers, 1);
         float xf[4] = {xm[0], xm[1], xm[2], xm[3]};
         add_slots(xf, p.dslot + (size_t)pl * MAX_CLUSTERS * D, NC, k0);
-        const float s_fin = norm_into_h(sm, xf, k0, w_fin, p.eps, tid);
-        float hreg[4][8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) hreg[i][e] = sm.h[8 * lane + 256 * i + e] * s_fin;
+        float hmaxf;
+        const float s_fin = norm_into_h(sm, xf, k0, w_fin, p.eps, tid, hmaxf);
         float best = -INFINITY;
         int bidx = 0x7FFFFFFF;
         const int nv = w.v1 - w.v0;
-        for (int r0 = 0; r0 < nv; r0 += ROWS_PER_STAGE) {
-            const int n = min(ROWS_PER_STAGE, nv - r0);
-            const uint8_t* st = cs.stage_wait(ok);
-            if (ok) {
-                for (int rr = cw; rr < n; rr += NCW) {
-                    const uint4* row = (const uint4*)(st + rr * ROW_B);
-                    float a = 0.f;
+        if constexpr (Q8) {
+            // int8 rows, 32 per stage: warp cw takes rows 4 cw .. 4 cw + 3; dp2a on the activations
+            // rounded to int16, then a transposed butterfly leaves row j in lanes 8 j .. 8 j + 7
+            const float hinv = hmaxf > 0.f ? 32767.0f / hmaxf : 0.f, hstep = hmaxf / 32767.0f * s_fin;
+            int hq[16];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        float f[8];
-                        unpack8(row[lane + 32 * i], f);
+            for (int i = 0; i < 2; ++i)
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) a = fmaf(hreg[i][e], f[e], a);
+                for (int m4 = 0; m4 < 4; ++m4) {
+                    const float4 a = *(const float4*)&sm.h[16 * lane + 512 * i + 4 * m4];
+                    hq[8 * i + 2 * m4] = pack_i16(a.x * hinv, a.y * hinv);
+                    hq[8 * i + 2 * m4 + 1] = pack_i16(a.z * hinv, a.w * hinv);
+                }
+            constexpr int RPS8 = rows_per_stage<true>();
+            for (int r0 = 0; r0 < nv; r0 += RPS8) {
+                const int n = min(RPS8, nv - r0);
+                const int my = 4 * cw + (lane >> 3);   // the row this lane reports after the reduction
+                const float sc = my < n ? __ldg(p.s_E + w.v0 + r0 + my) : 0.f;
+                const uint8_t* st = cs.stage_wait(ok);
+                float v[4] = {0.f, 0.f, 0.f, 0.f};
+                if (ok) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int rr = 4 * cw + j;
+                        if (rr < n) {
+                            int a = 0;
+#pragma unroll
+                            for (int i = 0; i < 2; ++i) {
+                                const uint4 wv = *(const uint4*)(st + rr * D + 16 * lane + 512 * i);
+                                a = dp2a_lo(hq[8 * i + 0], wv.x, a);
+                                a = dp2a_hi(hq[8 * i + 1], wv.x, a);
+                                a = dp2a_lo(hq[8 * i + 2], wv.y, a);
+                                a = dp2a_hi(hq[8 * i + 3], wv.y, a);
+                                a = dp2a_lo(hq[8 * i + 4], wv.z, a);
+                                a = dp2a_hi(hq[8 * i + 5], wv.z, a);
+                                a = dp2a_lo(hq[8 * i + 6], wv.w, a);
+                                a = dp2a_hi(hq[8 * i + 7], wv.w, a);
+                            }
+                            v[j] = (float)a;
+                        }
                     }
-                    a = warp_sum(a);
-                    const int v = w.v0 + r0 + rr;
-                    if (lane == 0) p.logits[v] = a;
-                    if (a > best || (a == best && v < bidx)) {
+                }
+                cs.stage_release();
+                const float a = warp_reduce_n<4>(v) * hstep * sc;
+                const int vid = w.v0 + r0 + my;
+                if ((lane & 7) == 0 && my < n) {
+                    p.logits[vid] = a;
+                    if (a > best || (a == best && vid < bidx)) {
                         best = a;
-                        bidx = v;
+                        bidx = vid;
                     }
                 }
             }
-            cs.stage_release();
+            // lanes 0, 8, 16, 24 hold the warp's candidates
+#pragma unroll
+            for (int o = 8; o < 32; o <<= 1) {
+                const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+                if (ob > best || (ob == best && oi < bidx)) {
+                    best = ob;
+                    bidx = oi;
+                }
+            }
+        } else {
+            float hreg[4][8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) hreg[i][e] = sm.h[8 * lane + 256 * i + e] * s_fin;
+            constexpr int RPS16 = rows_per_stage<false>();
+            for (int r0 = 0; r0 < nv; r0 += RPS16) {
+                const int n = min(RPS16, nv - r0);
+                const uint8_t* st = cs.stage_wait(ok);
+                if (ok) {
+                    for (int rr = cw; rr < n; rr += NCW) {
+                        const uint4* row = (const uint4*)(st + rr * 2 * D);
+                        float a = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            float f[8];
+                            unpack8(row[lane + 32 * i], f);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) a = fmaf(hreg[i][e], f[e], a);
+                        }
+                        a = warp_sum(a);
+                        const int v = w.v0 + r0 + rr;
+                        if (lane == 0) p.logits[v] = a;
+                        if (a > best || (a == best && v < bidx)) {
+                            best = a;
+                            bidx = v;
+                        }
+                    }
+                }
+                cs.stage_release();
+            }
         }
         if (lane == 0) {
             sm.lm_val[cw] = best;
@@ -1153,9 +1400,10 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
     cluster_sync_all();   // no peer pushes into this CTA's shared memory after it exits
 }
 
-// Wt[j][i] = W[i][j] for a [rows][cols] bf16 matrix.
-__global__ void transpose_bf16_kernel(const uint16_t* __restrict__ W, uint16_t* __restrict__ Wt, int rows, int cols) {
-    __shared__ uint16_t tile[32][33];
+// Wt[j][i] = W[i][j] for a [rows][cols] matrix of bf16 (uint16_t) or int8 codes.
+template <typename T>
+__global__ void transpose_kernel(const T* __restrict__ W, T* __restrict__ Wt, int rows, int cols) {
+    __shared__ T tile[32][33];
     const int bx = blockIdx.x * 32, by = blockIdx.y * 32;
     for (int y = threadIdx.y; y < 32; y += 8) {
         const int r = by + y, cc = bx + threadIdx.x;
@@ -1176,7 +1424,9 @@ struct FusedDecode {
     float eps = 0.f;
     uint8_t* buf = nullptr;
     fused::LayerPtrs* d_layers = nullptr;
-    const uint16_t* E = nullptr;
+    bool q8 = false;             // weight-only int8 rows (else bf16)
+    const uint8_t* E = nullptr;
+    const float* sE = nullptr;
     const float* final_norm = nullptr;
     const float* inv_freq = nullptr;
     float *oslot = nullptr, *dslot = nullptr, *lm_part = nullptr;
@@ -1196,8 +1446,9 @@ FusedDecode* fused_create(const FusedWeights& fw, int n_layers, int V, float eps
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
     if (!coop) return nullptr;
-    if (cudaFuncSetAttribute(fused_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-        cudaSuccess)
+    const bool q8 = fw.q8;
+    auto kern = q8 ? fused_decode_kernel<true> : fused_decode_kernel<false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
         return nullptr;
     // as many clusters of 8 as can be resident at once (15 on a 152-SM GB300); 8 own the KV groups
     int max_clusters = 0;
@@ -1206,20 +1457,22 @@ FusedDecode* fused_create(const FusedWeights& fw, int n_layers, int V, float eps
         cfg.gridDim = dim3(CL);
         cfg.blockDim = dim3(THREADS);
         cfg.dynamicSmemBytes = SMEM_BYTES;
-        if (cudaOccupancyMaxActiveClusters(&max_clusters, fused_decode_kernel, &cfg) != cudaSuccess) return nullptr;
+        if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess) return nullptr;
     }
     const int nc = max_clusters < MAX_CLUSTERS ? max_clusters : MAX_CLUSTERS;
     if (nc < HKV) return nullptr;
     const int G = CL * nc;
-    // dot_rows takes at most 4 stages, scaled_rows at most 2
-    if (2 * ((INTER + G - 1) / G) > 4 * ROWS_PER_STAGE || ODIMS > 2 * ROWS_PER_STAGE) return nullptr;
+    // a GEMV phase takes at most 64 rows (4 bf16 or 2 int8 stages), a scaled-row phase at most 32
+    if (2 * ((INTER + G - 1) / G) > 64 || (INTER + G - 1) / G > 32 || ODIMS > 32) return nullptr;
     FusedDecode* f = new FusedDecode();
     f->G = G;
     f->n_clusters = nc;
     f->n_layers = n_layers;
     f->V = V;
     f->eps = eps;
-    f->E = fw.E;
+    f->q8 = q8;
+    f->E = q8 ? (const uint8_t*)fw.Eq : (const uint8_t*)fw.E;
+    f->sE = q8 ? fw.sE : nullptr;
     f->final_norm = fw.final_norm;
     f->inv_freq = fw.inv_freq;
     const size_t woT = (size_t)AD * D, wdT = (size_t)INTER * D;
@@ -1229,7 +1482,8 @@ FusedDecode* fused_create(const FusedWeights& fw, int n_layers, int V, float eps
         off = (off + b + 1023) / 1024 * 1024;
         return o;
     };
-    const size_t o_w = take((woT + wdT) * 2 * n_layers);
+    const size_t esz = q8 ? 1 : 2;   // bytes per weight element
+    const size_t o_w = take((woT + wdT) * esz * n_layers);
     const size_t o_layers = take(sizeof(LayerPtrs) * n_layers);
     const size_t o_state = take(sizeof(float) * 2 * (HKV + MAX_CLUSTERS) * D);
     const size_t o_lm = take(sizeof(float) * 2 * G + 64);
@@ -1239,15 +1493,33 @@ FusedDecode* fused_create(const FusedWeights& fw, int n_layers, int V, float eps
         delete f;
         return nullptr;
     }
-    uint16_t* wt = (uint16_t*)(f->buf + o_w);
     std::vector<LayerPtrs> lp(n_layers);
     for (int l = 0; l < n_layers; ++l) {
-        uint16_t* woT_l = wt + (size_t)l * (woT + wdT);
-        uint16_t* wdT_l = woT_l + woT;
-        transpose_bf16_kernel<<<dim3(AD / 32, D / 32), dim3(32, 8)>>>(fw.wo[l], woT_l, D, AD);
-        transpose_bf16_kernel<<<dim3(INTER / 32, D / 32), dim3(32, 8)>>>(fw.wd[l], wdT_l, D, INTER);
-        lp[l] = LayerPtrs{fw.wqkv[l], woT_l, fw.wgu[l], wdT_l, fw.in_norm[l], fw.post_norm[l], fw.q_norm[l],
-                          fw.k_norm[l]};
+        uint8_t* woT_l = f->buf + o_w + (size_t)l * (woT + wdT) * esz;
+        uint8_t* wdT_l = woT_l + woT * esz;
+        LayerPtrs& L = lp[l];
+        L.in_norm = fw.in_norm[l];
+        L.post_norm = fw.post_norm[l];
+        L.q_norm = fw.q_norm[l];
+        L.k_norm = fw.k_norm[l];
+        L.woT = woT_l;
+        L.wdT = wdT_l;
+        if (q8) {
+            transpose_kernel<int8_t><<<dim3(AD / 32, D / 32), dim3(32, 8)>>>(fw.wo_q[l], (int8_t*)woT_l, D, AD);
+            transpose_kernel<int8_t><<<dim3(INTER / 32, D / 32), dim3(32, 8)>>>(fw.wd_q[l], (int8_t*)wdT_l, D, INTER);
+            L.wqkv = (const uint8_t*)fw.wqkv_q[l];
+            L.wgu = (const uint8_t*)fw.wgu_q[l];
+            L.s_qkv = fw.s_qkv[l];
+            L.s_o = fw.s_o[l];
+            L.s_gu = fw.s_gu[l];
+            L.s_d = fw.s_d[l];
+        } else {
+            transpose_kernel<uint16_t><<<dim3(AD / 32, D / 32), dim3(32, 8)>>>(fw.wo[l], (uint16_t*)woT_l, D, AD);
+            transpose_kernel<uint16_t><<<dim3(INTER / 32, D / 32), dim3(32, 8)>>>(fw.wd[l], (uint16_t*)wdT_l, D, INTER);
+            L.wqkv = (const uint8_t*)fw.wqkv[l];
+            L.wgu = (const uint8_t*)fw.wgu[l];
+            L.s_qkv = L.s_o = L.s_gu = L.s_d = nullptr;
+        }
     }
     f->d_layers = (LayerPtrs*)(f->buf + o_layers);
     f->oslot = (float*)(f->buf + o_state);
@@ -1284,6 +1556,7 @@ int fused_decode(FusedDecode* f, const int* tokens, const int* positions, int ba
     p.layers = f->d_layers;
     p.n_layers = f->n_layers;
     p.E = f->E;
+    p.s_E = f->sE;
     p.final_norm = f->final_norm;
     p.inv_freq = f->inv_freq;
     p.V = f->V;
@@ -1318,7 +1591,8 @@ int fused_decode(FusedDecode* f, const int* tokens, const int* positions, int ba
     cfg.stream = st;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, fused_decode_kernel, p);
+    const cudaError_t e = f->q8 ? cudaLaunchKernelEx(&cfg, fused_decode_kernel<true>, p)
+                                : cudaLaunchKernelEx(&cfg, fused_decode_kernel<false>, p);
     count_launches(1);
     return e == cudaSuccess ? QW_OK : QW_ECUDA;
 }

@@ -16,6 +16,14 @@ struct FusedWeights {
     const float* inv_freq;
     std::vector<const uint16_t*> wqkv, wo, wgu, wd;   // wo: [hidden][n_heads*128], wd: [hidden][intermediate]
     std::vector<const float*> in_norm, post_norm, q_norm, k_norm;
+    // Weight-only int8 (q8): the same matrices as int8 codes in the same layouts, with one fp32
+    // scale per output channel (row of E, wqkv, wo, wgu, wd); the bf16 matrices above then hold
+    // the dequantised values.
+    bool q8 = false;
+    const int8_t* Eq = nullptr;
+    const float* sE = nullptr;
+    std::vector<const int8_t*> wqkv_q, wo_q, wgu_q, wd_q;
+    std::vector<const float*> s_qkv, s_o, s_gu, s_d;
 };
 
 // nullptr when the shape or the device does not fit the fused kernel.

@@ -112,5 +112,8 @@ int launch_sample(const float* logits, int batch, int vocab, const qw_sample_par
                   int32_t* out_ids, const float2* tile_part, int n_part, const int* argmax_hint, int* err,
                   cudaStream_t st);
 int launch_bf16_to_f32(const uint16_t* src, float* dst, int n, cudaStream_t st);
+// Per-row int8 codes Q [rows][cols] (dense) and fp32 scales S [rows] of the bf16 matrix W (row
+// stride ldw); W is overwritten with the dequantised bf16 values.
+int launch_quantize_rows(uint16_t* W, int rows, int cols, int ldw, int8_t* Q, float* S, cudaStream_t st);
 
 }  // namespace qw

@@ -655,4 +655,43 @@ int launch_bf16_to_f32(const uint16_t* src, float* dst, int n, cudaStream_t st) 
     return check_launch();
 }
 
+// Weight-only int8 per output channel, one warp per row r of a bf16 matrix W (row stride ldw):
+// S[r] = the smallest power of two >= max_c |W[r][c]| / 127 (that quotient in IEEE float32) and
+// Q[r][c] = W[r][c] / S[r] rounded half to even (exact: a division by a power of two), within
+// +-127; a zero row gets S = 0 and codes 0.  W[r][c] is replaced by bf16(Q[r][c] * S[r]), which
+// is exact (seven magnitude bits times a power of two), so the paths that stream bf16 compute
+// with exactly the weights the int8 path streams.
+QW_DEV float pow2_ceil(float t) {
+    const uint32_t b = __float_as_uint(t);
+    if (!(t > 0.f)) return 0.f;
+    if (b >= 0x00800000u) return (b & 0x007FFFFFu) ? __uint_as_float((b & 0x7F800000u) + 0x00800000u) : t;
+    // subnormal: the next power of two of the integer significand, on the same 2^-149 grid
+    return (b & (b - 1)) ? __uint_as_float(1u << (32 - __clz(b))) : t;
+}
+
+__global__ void quantize_rows_kernel(uint16_t* __restrict__ W, int rows, int cols, int ldw, int8_t* __restrict__ Q,
+                                     float* __restrict__ S) {
+    const int r = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5), lane = threadIdx.x & 31;
+    if (r >= rows) return;
+    uint16_t* w = W + (size_t)r * ldw;
+    float m = 0.f;
+    for (int c = lane; c < cols; c += 32) m = fmaxf(m, fabsf(__uint_as_float((uint32_t)w[c] << 16)));
+    m = warp_max(m);
+    const float sc = pow2_ceil(__fdiv_rn(m, 127.0f));
+    if (lane == 0) S[r] = sc;
+    int8_t* q = Q + (size_t)r * cols;
+    for (int c = lane; c < cols; c += 32) {
+        int v = 0;
+        if (sc > 0.f) v = max(-127, min(127, __float2int_rn(__fdiv_rn(__uint_as_float((uint32_t)w[c] << 16), sc))));
+        q[c] = (int8_t)v;
+        w[c] = f2bf((float)v * sc);
+    }
+}
+
+int launch_quantize_rows(uint16_t* W, int rows, int cols, int ldw, int8_t* Q, float* S, cudaStream_t st) {
+    if (rows <= 0) return QW_OK;
+    quantize_rows_kernel<<<(unsigned)(((size_t)rows * 32 + 255) / 256), 256, 0, st>>>(W, rows, cols, ldw, Q, S);
+    return check_launch();
+}
+
 }  // namespace qw
