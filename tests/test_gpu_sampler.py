@@ -121,3 +121,20 @@ def test_invalid_parameters_are_reported(model):
     assert m.check_code() == bd.QW_EINVAL
     m.sample(bd.sample_params([(1.0, 0, 0.9, 0)]), 0, out, logits=logits)
     assert m.check_code() == bd.QW_OK and 0 <= int(out) < V
+
+
+def test_topk_rows_and_their_hand_over(model):
+    """Rows capped by top_k <= 1024 take the one-CTA top-k kernel; a row whose bound bucket holds
+    more than its candidate buffer (3000 tied maxima) or a constant row is handed to the
+    general kernel.  Every row must still match the oracle."""
+    bd, m = model
+    g = torch.Generator().manual_seed(99)
+    logits = torch.randn(8, V, generator=g) * 2.0
+    logits[5, :] = torch.randn(V, generator=g) * 0.5
+    logits[5, torch.randperm(V, generator=g)[:3000]] = 6.0     # 3000 tied maxima
+    logits[6, :] = 1.5                                           # constant row
+    rows = [(0.7, 50, 0.9, 1), (1.0, 1024, 0.95, 2), (1.0, 7, 1.0, 3), (0.3, 1, 0.5, 4), (2.0, 300, 0.99, 5),
+            (1.0, 100, 0.9, 6), (1.0, 10, 1.0, 7), (0.7, 1000, 0.999, 8)]
+    for counter in (0, 3, 2**40 + 5):
+        got = _check_rows(bd, m, logits, rows, counter, min_strict=4)
+        assert got[6] < 10                                       # uniform over the 10 lowest ids

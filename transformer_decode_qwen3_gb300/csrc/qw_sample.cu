@@ -36,6 +36,24 @@ QW_DEV uint32_t order_key(float v) {
 }
 QW_DEV float key_value(uint32_t k) { return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k); }
 
+constexpr int FT = 1024, FNW = FT / 32, FNB = 2048, FCAP = 2048, FKMAX = 1024;
+
+struct FShared {
+    uint32_t hist[FNB];
+    unsigned long long cand[FCAP];
+    float e[FKMAX];
+    float fred[FNW];
+    float fred2[FNW];
+    uint32_t ured[FNW];
+    uint32_t ncand, bstar, cnt_star;
+    int pick;
+};
+
+QW_DEV bool topk_row(const qw_sample_params& P, int vocab) {
+    return P.temperature > 0.f && P.top_k >= 1 && P.top_k <= FKMAX && P.top_k < vocab && P.top_p > 0.f &&
+           P.top_p <= 1.f;
+}
+
 struct Shared {
     uint32_t wcnt[NW][2][NB];     // per-warp counts of both searches
     float wmass[NW][NB];          // per-warp mass of the mass search
@@ -185,6 +203,8 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS)
     const float* lg = logits + (size_t)row * vocab;
     const qw_sample_params P = params[row];
     const bool greedy = !(P.temperature > 0.f);
+    // rows the top-k kernel (launched just before) sampled: it wrote an id; -1 hands the row over
+    if (topk_row(P, vocab) && out[row] >= 0) return;
     // this CTA's ids [j_lo, j_hi): whole float4s, the last CTA takes the ragged end
     const int span = ((vocab + CL - 1) / CL + 3) & ~3;
     const int j_lo = min(vocab, rank * span), j_hi = min(vocab, j_lo + span);
@@ -369,12 +389,197 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS)
     cluster_sync();   // no peer reads this CTA's shared memory after it exits
 }
 
+// ---------------------------------------------------------------- top-k rows (1 <= top_k <= 1024)
+// A row whose kept set is capped by a small top_k needs only its top_k best entries, plus the
+// full-vocabulary normaliser Z of the article's softmax.  One CTA of 1024 threads per row:
+//   pass 1  max, min and Z = sum of 2^((l - max) c) (online, c = log2(e) / T)
+//   pass 2  histogram of 2048 equal-width buckets of (max - l) over [0, max - min]; the first
+//           bucket where the count from the top reaches top_k bounds the k-th entry from below
+//   pass 3  gather every entry at or above that bucket (at most FCAP, else the row is handed to
+//           the general kernel by writing -1) as (order key, ~id), bitonic sort descending
+// then, over the sorted candidates: p_i = e_i / Z, cutoff = min(top_k, 1 + #(cumsum < top_p)),
+// the draw is the first kept entry whose cumulative e exceeds u * (kept e), u from Philox as in
+// the general kernel.  Rows this kernel does not take (greedy, top_k outside [1, 1024], invalid
+// parameters) are left untouched for the general kernel that runs after it.
+__global__ void __launch_bounds__(FT, 1)
+    sample_topk_kernel(const float* __restrict__ logits, int vocab, const qw_sample_params* __restrict__ params,
+                       uint64_t rng_counter, int32_t* __restrict__ out) {
+    __shared__ FShared sh;
+    pdl_wait();
+    pdl_trigger();
+    const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const qw_sample_params P = params[row];
+    if (!topk_row(P, vocab)) return;
+    const float* lg = logits + (size_t)row * vocab;
+    const float c = 1.4426950408889634f / P.temperature;
+    const int k = P.top_k;
+    const int n4 = vocab / 4;   // vocab is a multiple of 32: rows are whole float4s
+
+    // ---- pass 1: max, min, Z
+    float m = -INFINITY, mn = INFINITY, z = 0.f;
+    for (int i = tid; i < n4; i += FT) {
+        const float4 q = __ldg((const float4*)lg + i);
+        const float v[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            if (v[t] > m) {
+                z = z * exp2f((m - v[t]) * c) + 1.f;
+                m = v[t];
+            } else {
+                z += exp2f((v[t] - m) * c);
+            }
+            mn = fminf(mn, v[t]);
+        }
+    }
+    const float M = warp_max(m);
+    float zr = m == -INFINITY ? 0.f : z * exp2f((m - M) * c);
+    zr = warp_sum(zr);
+    const float mnw = -warp_max(-mn);
+    if (lane == 0) {
+        sh.fred[warp] = M;
+        sh.fred2[warp] = mnw;
+    }
+    __syncthreads();
+    float gM = -INFINITY, gmn = INFINITY;
+#pragma unroll 4
+    for (int w = 0; w < FNW; ++w) {
+        gM = fmaxf(gM, sh.fred[w]);
+        gmn = fminf(gmn, sh.fred2[w]);
+    }
+    __syncthreads();
+    if (lane == 0) sh.fred[warp] = zr * exp2f((M - gM) * c);
+    for (int b = tid; b < FNB; b += FT) sh.hist[b] = 0;
+    if (tid == 0) sh.ncand = 0;
+    __syncthreads();
+    float Z = 0.f;
+#pragma unroll 4
+    for (int w = 0; w < FNW; ++w) Z += sh.fred[w];
+    if (!(gM > gmn) || !(Z > 0.f)) {   // a constant row (ties everywhere) or non-finite values
+        if (tid == 0) out[row] = -1;
+        return;
+    }
+    // ---- pass 2: bucket histogram
+    const float inv_w = (float)FNB / (gM - gmn);
+    auto bucket = [&](float v) {   // monotone in v; NaN lands in the last bucket
+        const float d = (gM - v) * inv_w;
+        return d < (float)(FNB - 1) ? (int)d : FNB - 1;
+    };
+    for (int i = tid; i < n4; i += FT) {
+        const float4 q = __ldg((const float4*)lg + i);
+        atomicAdd(&sh.hist[bucket(q.x)], 1u);
+        atomicAdd(&sh.hist[bucket(q.y)], 1u);
+        atomicAdd(&sh.hist[bucket(q.z)], 1u);
+        atomicAdd(&sh.hist[bucket(q.w)], 1u);
+    }
+    __syncthreads();
+    // inclusive prefix counts over the buckets (2 per thread): the first bucket reaching k
+    {
+        const uint32_t h0 = sh.hist[2 * tid], h1 = sh.hist[2 * tid + 1];
+        uint32_t incl = h0 + h1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) sh.ured[warp] = incl;
+        __syncthreads();
+        uint32_t base = 0;
+        for (int w = 0; w < warp; ++w) base += sh.ured[w];
+        const uint32_t before = base + incl - (h0 + h1);
+        if (before < (uint32_t)k && before + h0 >= (uint32_t)k) {
+            sh.bstar = 2 * tid;
+            sh.cnt_star = before + h0;
+        } else if (before + h0 < (uint32_t)k && before + h0 + h1 >= (uint32_t)k) {
+            sh.bstar = 2 * tid + 1;
+            sh.cnt_star = before + h0 + h1;
+        }
+    }
+    __syncthreads();
+    const int bstar = (int)sh.bstar;
+    const uint32_t ncand = sh.cnt_star;
+    if (ncand > FCAP) {   // too many entries at the bound: the general kernel takes the row
+        if (tid == 0) out[row] = -1;
+        return;
+    }
+    // ---- pass 3: gather the candidates, sort them by (logit desc, id asc)
+    for (int i = tid; i < n4; i += FT) {
+        const float4 q = __ldg((const float4*)lg + i);
+        const float v[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+            if (bucket(v[t]) <= bstar) {
+                const uint32_t slot = atomicAdd(&sh.ncand, 1u);
+                if (slot < FCAP)
+                    sh.cand[slot] = ((unsigned long long)order_key(v[t]) << 32) | (0xFFFFFFFFu - (uint32_t)(4 * i + t));
+            }
+    }
+    __syncthreads();
+    int np2 = 1;
+    while (np2 < (int)ncand) np2 <<= 1;
+    for (int i = (int)ncand + tid; i < np2; i += FT) sh.cand[i] = 0ull;   // below every entry
+    __syncthreads();
+    for (int size = 2; size <= np2; size <<= 1)
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int i = tid; i < np2; i += FT) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const unsigned long long a = sh.cand[i], b = sh.cand[j];
+                    const bool desc = (i & size) == 0;   // descending runs, merged into one descending order
+                    if (desc ? a < b : a > b) {
+                        sh.cand[i] = b;
+                        sh.cand[j] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    // ---- top-k, top-p and the draw over the first k candidates (k <= FT)
+    const bool mine = tid < k;
+    const float ei = mine ? exp2f((key_value((uint32_t)(sh.cand[tid] >> 32)) - gM) * c) : 0.f;
+    // inclusive prefix sum of e over the first k entries
+    float incl = ei;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+    }
+    if (lane == 31) sh.fred[warp] = incl;
+    __syncthreads();
+    float base = 0.f;
+    for (int w = 0; w < warp; ++w) base += sh.fred[w];
+    const float cum = base + incl;
+    if (mine) sh.e[tid] = cum;
+    // cutoff = min(k, 1 + #(cumsum of p < top_p))
+    const bool below = mine && cum / Z < P.top_p;
+    const uint32_t nb = __popc(__ballot_sync(0xffffffffu, below));
+    if (lane == 0) sh.ured[warp] = nb;
+    if (tid == 0) sh.pick = k;
+    __syncthreads();
+    uint32_t nbelow = 0;
+    for (int w = 0; w < FNW; ++w) nbelow += sh.ured[w];
+    const int cutoff = min(k, (int)nbelow + 1);
+    const float kept = sh.e[cutoff - 1];
+    uint32_t c4[4] = {(uint32_t)rng_counter, (uint32_t)(rng_counter >> 32), 0u, 0u};
+    philox4x32_10(c4, (uint32_t)P.seed, (uint32_t)(P.seed >> 32));
+    const float u = (float)(c4[0] >> 8) * (1.0f / 16777216.0f);
+    if (tid < cutoff && cum > u * kept) atomicMin(&sh.pick, tid);
+    __syncthreads();
+    if (tid == 0) {
+        const int i = min(sh.pick, cutoff - 1);   // rounding past the kept prefix: its last entry
+        out[row] = (int32_t)(0xFFFFFFFFu - (uint32_t)(sh.cand[i] & 0xFFFFFFFFull));
+    }
+}
+
 }  // namespace smp
 
 int launch_sample(const float* logits, int batch, int vocab, const qw_sample_params* params, uint64_t rng_counter,
                   int32_t* out_ids, const float2* tile_part, int n_part, const int* argmax_hint, int* err,
                   cudaStream_t st) {
     if (batch <= 0) return QW_OK;
+    if (pdl_launch(smp::sample_topk_kernel, dim3(batch), dim3(smp::FT), 0, st, logits, vocab, params, rng_counter,
+                   out_ids) != cudaSuccess)
+        return QW_ECUDA;
+    count_launches(1);
     const cudaError_t e = pdl_launch(smp::sample_kernel, dim3(batch * smp::CL), dim3(smp::THREADS), 0, st, logits, vocab,
                                      params, rng_counter, out_ids, tile_part, n_part, argmax_hint, err);
     count_launches(1);
