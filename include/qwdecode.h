@@ -70,7 +70,8 @@ typedef struct qw_config {
     int32_t n_layers;
     int32_t hidden;        /* multiple of 256, at most 4096 */
     int32_t n_heads;       /* query heads; n_heads * head_dim is a multiple of 256 */
-    int32_t n_kv_heads;    /* n_heads / 2: the kernels implement groups of two query heads per KV head */
+    int32_t n_kv_heads;    /* n_heads / G with G = 1 (MHA), 2, 4, 8 or 16 query heads per KV head (GQA; MQA
+                            * when n_kv_heads = 1): Qwen3-0.6B and 1.7B have G = 2, 4B and 8B have G = 4 */
     int32_t head_dim;      /* must be QW_HEAD_DIM */
     int32_t intermediate;  /* multiple of 128 */
     int32_t vocab;         /* multiple of 32 */
@@ -235,7 +236,7 @@ int qw_attn_decode(qw_ctx* ctx, const float* q, const int32_t* positions, int32_
  *   kv_layer   DEVICE bf16 pages of one layer, [n_pages][2][n_kv_heads][16][128]
  *              (qw_kv_layout's base plus layer * layer_stride for a qw_kv pool).
  *   q, positions, block_tables, bt_stride, out: as in qw_attn_decode; n_heads must be
- *              2 * n_kv_heads.
+ *              n_kv_heads times 1, 2, 4, 8 or 16.
  * Limits: batch * n_heads * 130 <= QW_NOALLOC_SCRATCH_FLOATS (batch * n_heads <= 8065),
  * else QW_EINVAL with nothing launched.  Page ids outside [0, n_pages) are skipped but,
  * with no context, not reported.

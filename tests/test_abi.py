@@ -66,10 +66,12 @@ def test_init_rejects_bad_config_without_touching_the_gpu(lib, field, value):
 
 
 @pytest.mark.parametrize("shape", [dict(hidden=2560, n_heads=32, n_kv_heads=8, intermediate=9728),    # 4B
-                                   dict(hidden=4096, n_heads=32, n_kv_heads=8, intermediate=12288)])  # 8B
-def test_init_names_the_unsupported_group_size(lib, shape):
-    """Qwen3 sizes with four query heads per KV head are refused with a message (the attention
-    kernels implement groups of two: 0.6B and 1.7B)."""
+                                   dict(hidden=4096, n_heads=32, n_kv_heads=8, intermediate=12288),   # 8B
+                                   dict(n_heads=16, n_kv_heads=16),                                   # MHA
+                                   dict(n_heads=16, n_kv_heads=1)])                                   # MQA
+def test_init_takes_other_group_sizes(lib, shape):
+    """Qwen3 sizes with four query heads per KV head, MHA and MQA pass the configuration check
+    (qw_init then stops at the null weights, before any device work)."""
     from transformer_decode_qwen3_gb300 import binding
     cfg = binding.QwConfig()
     lib.qw_config_default(ctypes.byref(cfg))
@@ -77,7 +79,19 @@ def test_init_names_the_unsupported_group_size(lib, shape):
         setattr(cfg, k, v)
     h = ctypes.c_void_p()
     assert lib.qw_init(ctypes.byref(cfg), ctypes.byref(binding.QwWeights()), ctypes.byref(h)) == binding.QW_EINVAL
-    assert b"n_heads == 2 * n_kv_heads" in lib.qw_last_error_message()
+    assert b"null weight pointer" in lib.qw_last_error_message()
+
+
+@pytest.mark.parametrize("heads", [(24, 8), (32, 1), (12, 8)])
+def test_init_names_an_unsupported_group_size(lib, heads):
+    """Group sizes other than 1, 2, 4, 8, 16 (or n_heads not a multiple of n_kv_heads) are refused."""
+    from transformer_decode_qwen3_gb300 import binding
+    cfg = binding.QwConfig()
+    lib.qw_config_default(ctypes.byref(cfg))
+    cfg.n_heads, cfg.n_kv_heads = heads
+    h = ctypes.c_void_p()
+    assert lib.qw_init(ctypes.byref(cfg), ctypes.byref(binding.QwWeights()), ctypes.byref(h)) == binding.QW_EINVAL
+    assert b"query heads per KV head" in lib.qw_last_error_message()
 
 
 def test_generate_rejects_bad_arguments(lib):

@@ -1,7 +1,13 @@
-"""Another Qwen3 dense size the kernels implement (groups of two query heads per KV head,
-head_dim 128): the 1.7B shape (hidden 2048, 16 query / 8 KV heads, intermediate 6144), with
-2 layers and a reduced vocabulary so the oracle stays fast.  Ragged prefill, then a batched and
-a batch-1 decode step, against the oracle."""
+"""Other Qwen3 dense sizes and attention layouts (the article, Step 5: "From MHA to MQA to GQA"),
+head_dim 128, each with 2 layers and a reduced vocabulary so the oracle stays fast:
+
+  1.7B  hidden 2048, 16 query / 8 KV heads (2 per group), intermediate 6144
+  4B    hidden 2560, 32 / 8 (4 per group), intermediate 9728
+  8B    hidden 4096, 32 / 8 (4 per group), intermediate 12288
+  MHA   hidden 1024, 8 / 8 (1 per group);  G8: 16 / 2;  MQA: 16 / 1 (one KV head)
+
+Ragged prefill (query tiles of 128 / G positions), then a batched and a batch-1 decode step,
+against the oracle."""
 import numpy as np
 import pytest
 import torch
@@ -11,12 +17,20 @@ from transformer_decode_qwen3_gb300 import synth
 from tests import qwtest as Q
 
 pytestmark = pytest.mark.gpu
-S = synth.ModelShape(n_layers=2, hidden=2048, n_heads=16, n_kv_heads=8, head_dim=128, intermediate=6144,
-                     vocab=8192)
+SHAPES = {
+    "1.7B": dict(hidden=2048, n_heads=16, n_kv_heads=8, intermediate=6144),
+    "4B": dict(hidden=2560, n_heads=32, n_kv_heads=8, intermediate=9728),
+    "8B": dict(hidden=4096, n_heads=32, n_kv_heads=8, intermediate=12288),
+    "MHA": dict(hidden=1024, n_heads=8, n_kv_heads=8, intermediate=3072),
+    "G8": dict(hidden=1024, n_heads=16, n_kv_heads=2, intermediate=3072),
+    "MQA": dict(hidden=1024, n_heads=16, n_kv_heads=1, intermediate=3072),
+}
 
 
-def test_qwen3_1_7b_shape_prefill_and_decode():
+@pytest.mark.parametrize("name", list(SHAPES))
+def test_other_sizes_and_layouts_prefill_and_decode(name):
     from transformer_decode_qwen3_gb300 import binding as bd
+    S = synth.ModelShape(n_layers=2, head_dim=128, vocab=8192, **SHAPES[name])
     w = synth.make_weights(S, seed=5)
     model = bd.Model(w, S, max_batch=4, max_tokens=512)
     orc = R.Qwen3Oracle(w, S)

@@ -154,8 +154,8 @@ static int validate_config(const qw_config* c) {
     if (c->hidden < 256 || c->hidden % 256 || c->hidden > 4096)
         return fail(QW_EINVAL, "hidden must be a multiple of 256 in [256, 4096]");
     if (c->head_dim != QW_HEAD_DIM) return fail(QW_EINVAL, "head_dim must be 128");
-    if (c->n_kv_heads < 1 || c->n_heads != 2 * c->n_kv_heads)
-        return fail(QW_EINVAL, "the attention kernels implement n_heads == 2 * n_kv_heads");
+    if (!group_size_ok(c->n_heads, c->n_kv_heads))
+        return fail(QW_EINVAL, "n_heads must be n_kv_heads times 1, 2, 4, 8 or 16 (query heads per KV head)");
     if ((c->n_heads * c->head_dim) % 256) return fail(QW_EINVAL, "n_heads * head_dim must be a multiple of 256");
     if (c->intermediate < 128 || c->intermediate % 128) return fail(QW_EINVAL, "intermediate must be a multiple of 128");
     if (c->vocab < 32 || c->vocab % 32) return fail(QW_EINVAL, "vocab must be a positive multiple of 32");
@@ -606,11 +606,14 @@ int qw_prefill(qw_ctx* ctx, const int32_t* ids, const int32_t* positions, const 
     cudaStream_t st = (cudaStream_t)stream;
     std::vector<int> tok_seq(n), last(n_seqs);
     std::vector<int4> tiles;
+    // query tiles: 128 / G positions (G query heads per KV head fill the 128 MMA rows of the
+    // tcgen05 kernel); the mma.sync comparison kernel takes 64 positions of two heads
+    const int tile = ctx->prefill_attn == 0 ? 128 / (ctx->cfg.n_heads / ctx->cfg.n_kv_heads) : 64;
     for (int s = 0; s < n_seqs; ++s) {
         const int len = cu[s + 1] - cu[s];
         for (int t = cu[s]; t < cu[s + 1]; ++t) tok_seq[t] = s;
         last[s] = cu[s + 1] - 1;
-        for (int q0 = 0; q0 < len; q0 += 64) tiles.push_back(make_int4(s, cu[s] + q0, std::min(64, len - q0), q0));
+        for (int q0 = 0; q0 < len; q0 += tile) tiles.push_back(make_int4(s, cu[s] + q0, std::min(tile, len - q0), q0));
     }
     // longest causal rows first, so the heaviest tiles start in the first wave
     std::stable_sort(tiles.begin(), tiles.end(), [](const int4& a, const int4& b) { return a.w > b.w; });

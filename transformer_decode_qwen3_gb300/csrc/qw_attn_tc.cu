@@ -1,8 +1,9 @@
 // Causal prefill attention of the article's Step 5 on the 5th-generation tensor core.
 //
-// One CTA takes 64 consecutive query positions of one sequence and one KV head g:
-// its 128 MMA rows are those positions for query head 2g (rows 0..63) and 2g+1
-// (rows 64..127), which share the KV head (grouped-query attention).  Keys and
+// One CTA takes 128 / G consecutive query positions of one sequence and one KV head g,
+// G = Hq / Hkv query heads per KV head (1, 2, 4, 8 or 16): its 128 MMA rows are those
+// positions for each query head G g + hh of the group (rows hh * 128 / G ..), which share the
+// KV head (grouped-query attention; G = 2 for Qwen3-0.6B: 64 positions x 2 heads).  Keys and
 // values stream from the paged cache in tiles of 64 positions (4 pages), loaded by
 // TMA through a 4-D view of the pool ([page][K/V, head][slot][dim], 16-slot boxes,
 // 128-byte swizzle) into a 2-deep ring; two CTAs share an SM so that one's softmax
@@ -74,7 +75,8 @@ __global__ void __launch_bounds__(THREADS, 2)
     attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmKV,
                            const int* __restrict__ positions, const int4* __restrict__ tiles,
                            const int* __restrict__ block_tables, int bt_stride, int n_pages, int Hq, int Hkv,
-                           uint16_t* __restrict__ out, float scale_log2, int split, int* err) {
+                           int lg, uint16_t* __restrict__ out, float scale_log2, int split, int* err) {
+    // lg = log2(G): the tile holds 128 >> lg positions of each of the group's G query heads
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw;
     // 128-byte-swizzled tiles need 1024-byte aligned shared memory
@@ -145,12 +147,12 @@ __global__ void __launch_bounds__(THREADS, 2)
                 return page;
             };
             if (lane == 0) {
-                // Q: rows 0..63 = head 2g, rows 64..127 = head 2g+1, two 64-dim blocks each
+                // Q: rows hh * (128 >> lg) .. = head (g << lg) + hh, two 64-dim blocks each
                 mbar_arrive_expect_tx(q_full, Q_BYTES);
-                for (int hh = 0; hh < 2; ++hh)
+                for (int hh = 0; hh < (1 << lg); ++hh)
                     for (int c = 0; c < 2; ++c)
-                        tma_load_2d(sQ + c * CHUNK + hh * (CHUNK / 2), &tmQ, (2 * g + hh) * HD + 64 * c, row0,
-                                    q_full);
+                        tma_load_2d(sQ + c * CHUNK + hh * ((128 >> lg) * 128), &tmQ, ((g << lg) + hh) * HD + 64 * c,
+                                    row0, q_full);
             }
             // issue order K_0, then K_{j+1}, V_j for j = 0, 1, ...: K runs one tile ahead of V
             auto issue = [&](int j, int page_lane, bool is_v) -> bool {
@@ -239,7 +241,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     } else {
         // softmax warps 2..5: TMEM lane group (warp % 4), thread = row
         const int r = 32 * (warp & 3) + lane;
-        const int hh = r >> 6, ri = r & 63;
+        const int hh = r >> (7 - lg), ri = r & ((128 >> lg) - 1);
         const int qp = ri < nrows ? positions[row0 + ri] : -1;
         const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
         float m = -INFINITY, l = 0.f;
@@ -328,7 +330,7 @@ __global__ void __launch_bounds__(THREADS, 2)
             tc_fence_after();
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const size_t ld = (size_t)Hq * HD;
-            const int h = 2 * g + hh;
+            const int h = (g << lg) + hh;
 #pragma unroll 1
             for (int c = 0; c < HD / 32; ++c) {
                 float o[32];
@@ -386,7 +388,8 @@ static int encode(CUtensorMap* map, void* base, int rank, const cuuint64_t* dims
 int launch_attn_prefill_tc(const uint16_t* q_bf16, int n_tok, const int* positions, const int4* tiles, int n_tiles,
                            int Hq, int Hkv, const KvView& kv, uint16_t* out, int split, int* err, cudaStream_t st) {
     if (n_tiles <= 0) return QW_OK;
-    if (Hq != 2 * Hkv) return QW_EINVAL;
+    if (!group_size_ok(Hq, Hkv)) return QW_EINVAL;
+    const int G = Hq / Hkv, lg = 31 - __builtin_clz((unsigned)G);
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(fa::attn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, fa::SMEM) !=
@@ -395,10 +398,10 @@ int launch_attn_prefill_tc(const uint16_t* q_bf16, int n_tok, const int* positio
         attr = true;
     }
     CUtensorMap tq, tkv;
-    {   // q as [tokens][Hq * 128] bf16, boxes of 64 dims x 64 tokens
+    {   // q as [tokens][Hq * 128] bf16, boxes of 64 dims x (128 / G) tokens
         cuuint64_t dims[2] = {(cuuint64_t)Hq * 128, (cuuint64_t)n_tok};
         cuuint64_t strides[1] = {(cuuint64_t)Hq * 128 * 2};
-        cuuint32_t box[2] = {64, 64};
+        cuuint32_t box[2] = {64, (cuuint32_t)(128 / G)};
         if (encode(&tq, const_cast<uint16_t*>(q_bf16), 2, dims, strides, box)) return QW_ECUDA;
     }
     {   // this layer's pool as [page][K/V x head][slot][dim], boxes of 64 dims x 16 slots
@@ -409,7 +412,7 @@ int launch_attn_prefill_tc(const uint16_t* q_bf16, int n_tok, const int* positio
     }
     const float scale_log2 = 1.4426950408889634f / sqrtf(128.f);
     fa::attn_prefill_tc_kernel<<<dim3(n_tiles, Hkv), fa::THREADS, fa::SMEM, st>>>(
-        tq, tkv, positions, tiles, kv.block_tables, kv.bt_stride, kv.n_pages, Hq, Hkv, out, scale_log2, split, err);
+        tq, tkv, positions, tiles, kv.block_tables, kv.bt_stride, kv.n_pages, Hq, Hkv, lg, out, scale_log2, split, err);
     count_launches(1);
     return cudaGetLastError() == cudaSuccess ? QW_OK : QW_ECUDA;
 }

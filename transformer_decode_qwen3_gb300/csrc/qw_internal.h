@@ -28,6 +28,14 @@ cudaError_t pdl_launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
 }
 
+// Query heads per KV head (grouped-query attention of Step 5) the attention kernels take:
+// 1 (MHA), 2, 4, 8 or 16 (MQA for 16 heads), with n_heads a multiple of n_kv_heads.
+inline bool group_size_ok(int Hq, int Hkv) {
+    if (Hkv < 1 || Hq < Hkv || Hq % Hkv) return false;
+    const int G = Hq / Hkv;
+    return G == 1 || G == 2 || G == 4 || G == 8 || G == 16;
+}
+
 // Record `msg` for qw_last_error_message() on this thread and return `code`.
 int report_error(int code, const char* msg);
 

@@ -420,11 +420,13 @@ int launch_attn_prefill(const float* q, const int* positions, const int4* tiles,
 }
 
 // ---------------------------------------------- Step 5: decode attention, split over the cache
-// One CTA per (split of the cached positions, KV head, sequence): both query heads
-// of the group against up to chunk_pages pages.  Each warp walks pages; lane l
-// covers keys (l >> 4) + 2i of the page and dims 8 (l & 15) .. +8.  The CTA writes
-// an unnormalised partial (o[128], running max m in log2 units, sum l) per query
-// head; attn_combine_kernel merges the splits.
+// One CTA per (split of the cached positions, slice of HPC query heads of one KV group,
+// sequence): those query heads against up to chunk_pages pages of the group's KV head g
+// (grouped-query sharing of Step 5: query head h reads KV head h / (Hq / Hkv)).  A group of
+// G = Hq / Hkv heads is one slice when G <= 4, else G / 4 slices of 4 (each reads the group's
+// pages).  Each warp walks pages; lane l covers keys (l >> 4) + 2i of the page and dims
+// 8 (l & 15) .. +8.  The CTA writes an unnormalised partial (o[128], running max m in log2
+// units, sum l) per query head; attn_combine_kernel merges the splits.
 constexpr int AD_WARPS = 4;
 constexpr int AD_PART = QW_HEAD_DIM + 2;
 
@@ -440,6 +442,7 @@ QW_DEV float dot8(const float (&q)[8], uint4 k) {
            q[4] * bf16_lo(k.z) + q[5] * bf16_hi(k.z) + q[6] * bf16_lo(k.w) + q[7] * bf16_hi(k.w);
 }
 
+template <int HPC>
 __global__ void __launch_bounds__(AD_WARPS * 32) attn_decode_kernel(const float* __restrict__ q,
                                                                     const int* __restrict__ positions, int Hq,
                                                                     int Hkv, KvView kv, int chunk_pages,
@@ -447,41 +450,42 @@ __global__ void __launch_bounds__(AD_WARPS * 32) attn_decode_kernel(const float*
                                                                     float scale_log2, int* err) {
     pdl_wait();   // launched with pdl_launch: earlier kernels may still be running
     pdl_trigger();
-    const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int G = Hq / Hkv, slices = G / HPC;
+    const int split = blockIdx.x, g = blockIdx.y / slices, b = blockIdx.z;
+    const int h0 = g * G + (blockIdx.y % slices) * HPC;   // first query head of this CTA
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int half = lane >> 4, dc = lane & 15;
     const int pos = positions[b];
     int L = pos + 1;
     if (pos < 0 || pos >= kv.bt_stride * QW_PAGE_SIZE) {
-        if (threadIdx.x == 0 && split == 0 && g == 0) set_error(err, QW_ERANGE);
+        if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) set_error(err, QW_ERANGE);
         L = 0;
     }
     const int np = (L + QW_PAGE_SIZE - 1) / QW_PAGE_SIZE;
     const int p_lo = split * chunk_pages, p_hi = min(np, p_lo + chunk_pages);
-    float* pa = part + (((size_t)b * Hq + 2 * g) * n_splits + split) * AD_PART;
-    float* pb = pa + (size_t)n_splits * AD_PART;
+    float* pbase = part + (((size_t)b * Hq + h0) * n_splits + split) * AD_PART;   // head hh: + hh * n_splits * AD_PART
     if (p_lo >= p_hi) {
-        if (threadIdx.x == 0) {
-            pa[QW_HEAD_DIM] = -INFINITY;
-            pa[QW_HEAD_DIM + 1] = 0.f;
-            pb[QW_HEAD_DIM] = -INFINITY;
-            pb[QW_HEAD_DIM + 1] = 0.f;
+        if (threadIdx.x < HPC) {
+            pbase[(size_t)threadIdx.x * n_splits * AD_PART + QW_HEAD_DIM] = -INFINITY;
+            pbase[(size_t)threadIdx.x * n_splits * AD_PART + QW_HEAD_DIM + 1] = 0.f;
         }
         return;
     }
-    float qa[8], qb[8];
-    {
-        const float* q0 = q + ((size_t)b * Hq + 2 * g) * QW_HEAD_DIM + dc * 8;
+    float qh[HPC][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            qa[i] = q0[i] * scale_log2;
-            qb[i] = q0[QW_HEAD_DIM + i] * scale_log2;
-        }
+    for (int hh = 0; hh < HPC; ++hh) {
+        const float* q0 = q + ((size_t)b * Hq + h0 + hh) * QW_HEAD_DIM + dc * 8;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) qh[hh][i] = q0[i] * scale_log2;
     }
-    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-    float oa[8], ob[8];
+    float m[HPC], l[HPC], o[HPC][8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) oa[i] = ob[i] = 0.f;
+    for (int hh = 0; hh < HPC; ++hh) {
+        m[hh] = -INFINITY;
+        l[hh] = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[hh][i] = 0.f;
+    }
     const int* bt = kv.block_tables + (size_t)b * kv.bt_stride;
     const int64_t v_off = (int64_t)Hkv * QW_PAGE_SIZE * QW_HEAD_DIM;
 
@@ -500,82 +504,68 @@ __global__ void __launch_bounds__(AD_WARPS * 32) attn_decode_kernel(const float*
         for (int i = 0; i < 8; ++i) kr[i] = ldg_stream(kp + i * 2 * QW_HEAD_DIM);
 #pragma unroll
         for (int i = 0; i < 8; ++i) vr[i] = ldg_stream(kp + v_off + i * 2 * QW_HEAD_DIM);
-        float sa[8], sb[8];
+        float sc[HPC][8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            sa[i] = dot8(qa, kr[i]);
-            sb[i] = dot8(qb, kr[i]);
-        }
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) {
+            for (int hh = 0; hh < HPC; ++hh) sc[hh][i] = dot8(qh[hh], kr[i]);
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1)
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int hh = 0; hh < HPC; ++hh) sc[hh][i] += __shfl_xor_sync(0xffffffffu, sc[hh][i], off);
+        float nm[HPC];
+#pragma unroll
+        for (int hh = 0; hh < HPC; ++hh) {
+            float mx = -INFINITY;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                sa[i] += __shfl_xor_sync(0xffffffffu, sa[i], o);
-                sb[i] += __shfl_xor_sync(0xffffffffu, sb[i], o);
+                if (pi * QW_PAGE_SIZE + half + 2 * i >= L) sc[hh][i] = -INFINITY;
+                mx = fmaxf(mx, sc[hh][i]);
             }
-        }
-        float mxa = -INFINITY, mxb = -INFINITY;
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            nm[hh] = fmaxf(m[hh], mx);   // finite: key pi*16 is always visible
+            const float al = exp2f(m[hh] - nm[hh]);
+            m[hh] = nm[hh];
+            l[hh] *= al;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int kpos = pi * QW_PAGE_SIZE + half + 2 * i;
-            if (kpos >= L) sa[i] = sb[i] = -INFINITY;
-            mxa = fmaxf(mxa, sa[i]);
-            mxb = fmaxf(mxb, sb[i]);
-        }
-        mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 16));
-        mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 16));
-        const float na = fmaxf(m_a, mxa), nb = fmaxf(m_b, mxb);  // finite: key pi*16 is always visible
-        const float ala = exp2f(m_a - na), alb = exp2f(m_b - nb);
-        m_a = na;
-        m_b = nb;
-        l_a *= ala;
-        l_b *= alb;
-#pragma unroll
-        for (int d = 0; d < 8; ++d) {
-            oa[d] *= ala;
-            ob[d] *= alb;
+            for (int d = 0; d < 8; ++d) o[hh][d] *= al;
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float ea = exp2f(sa[i] - na), eb = exp2f(sb[i] - nb);
-            l_a += ea;
-            l_b += eb;
             const float v[8] = {bf16_lo(vr[i].x), bf16_hi(vr[i].x), bf16_lo(vr[i].y), bf16_hi(vr[i].y),
                                 bf16_lo(vr[i].z), bf16_hi(vr[i].z), bf16_lo(vr[i].w), bf16_hi(vr[i].w)};
 #pragma unroll
-            for (int d = 0; d < 8; ++d) {
-                oa[d] += ea * v[d];
-                ob[d] += eb * v[d];
+            for (int hh = 0; hh < HPC; ++hh) {
+                const float e = exp2f(sc[hh][i] - nm[hh]);
+                l[hh] += e;
+#pragma unroll
+                for (int d = 0; d < 8; ++d) o[hh][d] += e * v[d];
             }
         }
     }
     // the two key halves of a warp share m: add them
-    l_a += __shfl_xor_sync(0xffffffffu, l_a, 16);
-    l_b += __shfl_xor_sync(0xffffffffu, l_b, 16);
+    __shared__ float s_o[AD_WARPS][HPC][QW_HEAD_DIM];
+    __shared__ float s_m[AD_WARPS][HPC], s_l[AD_WARPS][HPC];
 #pragma unroll
-    for (int d = 0; d < 8; ++d) {
-        oa[d] += __shfl_xor_sync(0xffffffffu, oa[d], 16);
-        ob[d] += __shfl_xor_sync(0xffffffffu, ob[d], 16);
-    }
-    __shared__ float s_o[AD_WARPS][2][QW_HEAD_DIM];
-    __shared__ float s_m[AD_WARPS][2], s_l[AD_WARPS][2];
-    if (half == 0) {
+    for (int hh = 0; hh < HPC; ++hh) {
+        l[hh] += __shfl_xor_sync(0xffffffffu, l[hh], 16);
 #pragma unroll
-        for (int d = 0; d < 8; ++d) {
-            s_o[warp][0][dc * 8 + d] = oa[d];
-            s_o[warp][1][dc * 8 + d] = ob[d];
+        for (int d = 0; d < 8; ++d) o[hh][d] += __shfl_xor_sync(0xffffffffu, o[hh][d], 16);
+        if (half == 0) {
+#pragma unroll
+            for (int d = 0; d < 8; ++d) s_o[warp][hh][dc * 8 + d] = o[hh][d];
         }
-    }
-    if (lane == 0) {
-        s_m[warp][0] = m_a;
-        s_m[warp][1] = m_b;
-        s_l[warp][0] = l_a;
-        s_l[warp][1] = l_b;
+        if (lane == 0) {
+            s_m[warp][hh] = m[hh];
+            s_l[warp][hh] = l[hh];
+        }
     }
     __syncthreads();
     const int d = threadIdx.x;  // 128 threads = head_dim
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
+    for (int hh = 0; hh < HPC; ++hh) {
         float M = -INFINITY;
         for (int w = 0; w < AD_WARPS; ++w)
             if (s_l[w][hh] > 0.f) M = fmaxf(M, s_m[w][hh]);
@@ -587,7 +577,7 @@ __global__ void __launch_bounds__(AD_WARPS * 32) attn_decode_kernel(const float*
                 O += s_o[w][hh][d] * sc;
             }
         }
-        float* dst = hh ? pb : pa;
+        float* dst = pbase + (size_t)hh * n_splits * AD_PART;
         dst[d] = O;
         if (d == 0) {
             dst[QW_HEAD_DIM] = M;
@@ -622,9 +612,10 @@ __global__ void attn_combine_kernel(const float* __restrict__ part, int n_splits
 int launch_attn_decode(const float* q, const int* positions, int batch, int Hq, int Hkv, const KvView& kv,
                        float* part, int max_splits, uint16_t* out, int split, int* err, int n_sm, cudaStream_t st) {
     if (batch <= 0) return QW_OK;
-    if (Hq != 2 * Hkv) return QW_EINVAL;
+    if (!group_size_ok(Hq, Hkv)) return QW_EINVAL;
+    const int G = Hq / Hkv, hpc = G < 4 ? G : 4, slices = G / hpc;
     // pages per split: aim for ~8 CTAs per SM when every sequence is at full capacity
-    long want = ((long)kv.bt_stride * batch * Hkv + 8L * n_sm - 1) / (8L * n_sm);
+    long want = ((long)kv.bt_stride * batch * Hkv * slices + 8L * n_sm - 1) / (8L * n_sm);
     int chunk = 2;
     while (chunk < want && chunk < 32) chunk <<= 1;
     int n_splits = (kv.bt_stride + chunk - 1) / chunk;
@@ -633,9 +624,12 @@ int launch_attn_decode(const float* q, const int* positions, int batch, int Hq, 
         n_splits = (kv.bt_stride + chunk - 1) / chunk;
     }
     const float scale_log2 = 1.4426950408889634f / sqrtf((float)QW_HEAD_DIM);
-    if (pdl_launch(attn_decode_kernel, dim3(n_splits, Hkv, batch), dim3(AD_WARPS * 32), 0, st, q, positions, Hq, Hkv,
-                   kv, chunk, n_splits, part, scale_log2, err) != cudaSuccess)
-        return QW_ECUDA;
+    const dim3 grid(n_splits, Hkv * slices, batch), block(AD_WARPS * 32);
+    cudaError_t e;
+    if (hpc == 1) e = pdl_launch(attn_decode_kernel<1>, grid, block, 0, st, q, positions, Hq, Hkv, kv, chunk, n_splits, part, scale_log2, err);
+    else if (hpc == 2) e = pdl_launch(attn_decode_kernel<2>, grid, block, 0, st, q, positions, Hq, Hkv, kv, chunk, n_splits, part, scale_log2, err);
+    else e = pdl_launch(attn_decode_kernel<4>, grid, block, 0, st, q, positions, Hq, Hkv, kv, chunk, n_splits, part, scale_log2, err);
+    if (e != cudaSuccess) return QW_ECUDA;
     if (check_launch()) return QW_ECUDA;
     if (pdl_launch(attn_combine_kernel, dim3(Hq, batch), dim3(QW_HEAD_DIM / 2), 0, st, part, n_splits, Hq, out, split) !=
         cudaSuccess)

@@ -29,8 +29,9 @@ extern "C" int qw_attn_decode_noalloc(const float* q, const int32_t* positions, 
                                       const int32_t* block_tables, int32_t bt_stride, uint16_t* out, void* stream) {
     if (!q || !positions || !kv_layer || !block_tables || !out)
         return qw::report_error(QW_EINVAL, "qw_attn_decode_noalloc: null argument");
-    if (batch < 1 || n_kv_heads < 1 || n_heads != 2 * n_kv_heads || n_pages < 1 || bt_stride < 1)
-        return qw::report_error(QW_EINVAL, "qw_attn_decode_noalloc: bad size (n_heads must be 2 * n_kv_heads)");
+    if (batch < 1 || !qw::group_size_ok(n_heads, n_kv_heads) || n_pages < 1 || bt_stride < 1)
+        return qw::report_error(QW_EINVAL,
+                                "qw_attn_decode_noalloc: bad size (n_heads must be n_kv_heads times 1, 2, 4, 8 or 16)");
     const long per_split = (long)batch * n_heads * (QW_HEAD_DIM + 2);
     const long max_splits = QW_NOALLOC_SCRATCH_FLOATS / per_split;
     if (max_splits < 1)
