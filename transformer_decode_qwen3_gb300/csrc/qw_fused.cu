@@ -273,9 +273,6 @@ QW_DEV void signal_add(unsigned* ptr, unsigned v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
 }
 
-// sin and cos of a rotation angle (full-range sincosf; one out-of-line copy keeps the code small)
-__device__ __noinline__ void rope_sincos(float ang, float& sn, float& cs) { sincosf(ang, &sn, &cs); }
-
 QW_DEV void unpack8(uint4 w, float (&f)[8]) {
     f[0] = bf16_lo(w.x); f[1] = bf16_hi(w.x); f[2] = bf16_lo(w.y); f[3] = bf16_hi(w.y);
     f[4] = bf16_lo(w.z); f[5] = bf16_hi(w.z); f[6] = bf16_lo(w.w); f[7] = bf16_hi(w.w);
@@ -930,8 +927,11 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
         if (c == 0 && tid == 0 && !(tok >= 0 && tok < p.V)) set_error(p.err, QW_ERANGE);
     }
 
-    // RoPE inverse frequencies of this lane's two rotation pairs (the same for every layer)
-    const float invf0 = p.inv_freq[lane], invf1 = p.inv_freq[lane + 32];
+    // RoPE rotation of this lane's two pairs (dims lane + 32 j and + 64) at this step's
+    // position: the same in every layer, so computed once per step
+    float rs[2], rc[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) sincosf(__fmul_rn((float)pos, p.inv_freq[lane + 32 * j]), &rs[j], &rc[j]);
     for (int l = 0; l < p.n_layers; ++l) {
         // this layer's small vectors, loaded before the waits so their latency hides behind them
         const LayerPtrs L = p.layers[l];
@@ -1005,9 +1005,7 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
                     for (int i = 0; i < 4; ++i) y[i] = y[i] * sc * w_qk[i];
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
-                        const float ang = __fmul_rn((float)pos, j ? invf1 : invf0);
-                        float sn, cs_;
-                        rope_sincos(ang, sn, cs_);
+                        const float sn = rs[j], cs_ = rc[j];
                         const float a = y[j], b = y[j + 2];
                         y[j] = a * cs_ - b * sn;
                         y[j + 2] = a * sn + b * cs_;
