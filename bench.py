@@ -86,14 +86,18 @@ def config_of(name: str, K: int) -> dict:
             "global_batch": LONG_B, "cache_start": LONG_L, "cache_end": LONG_L + K, "page": PAGE, "l2": l2}
 
 
-# DRAM bytes (read + write) per launch of each workload's roofline kernel, from one ncu
-# capture summarised under profiles/; reported only while the kernel's source file is the
-# one that was captured (its sha256 below), else null.
+# DRAM bytes (read + write) of each workload's roofline kernel, from one ncu capture summarised
+# under profiles/ (per launch of the fused kernel; per step for the 28 attention launches of a
+# decode batch, like the algorithmic bytes they are compared with); reported only while the
+# kernel's source file is the one that was captured (its sha256 below), else null.
 NCU_TRAFFIC = {
     "decode_bs1": ("transformer_decode_qwen3_gb300/csrc/qw_fused.cu",
-                   "221b54e4d04fc1a5462d056882278a7913ff6eedbca007d92db2ce57b28af590", 1.253211e9 + 4.761856e6),
+                   "542dbfda0ea0cbeecc0879d7e05dfbeb1f3c9d3849aea3f5583e5f1e1122ff26", 1.263674e9 + 5.513216e6),
+    "decode_bs1_int8": ("transformer_decode_qwen3_gb300/csrc/qw_fused.cu",
+                        "542dbfda0ea0cbeecc0879d7e05dfbeb1f3c9d3849aea3f5583e5f1e1122ff26", 671.76e6),
+    # all 28 layers of a step: split-KV attention (552.41 MB) + merge (3.02 MB) per layer
     "decode_bs64": ("transformer_decode_qwen3_gb300/csrc/qw_kernels.cu",
-                    "115eff790f8dd54e9f6cec1876bd424e7e359315496e49d14195ae057d64775a", 552.48e6 + 3.01e6),
+                    "9802f1b4fabf1b2e6302f2fce2bd189570c40b04cdcda5c7e94c74070000ad3d", 28 * (552.41e6 + 3.02e6)),
 }
 
 

@@ -285,8 +285,8 @@ int qw_debug_gemm(const uint16_t* A, const uint16_t* B, void* C, int32_t M, int3
  * input; attention CTAs: 2 q|k|v rows done, 3 q|k|v exchange complete, 4 keys done,
  * 5 attention partials exchanged, 6 o_proj rows done, 7 o_proj reduced in the cluster,
  * 8 group slot published; every CTA: 9/10 before/after the wait for the attention output,
- * 11 gate/up rows done, 12 down_proj rows done, 13 reduced in the cluster, 14 cluster slot
- * published, 15 the producer has issued the layer's weights, 17 feed-forward input normalised,
+ * 11 gate/up rows and SwiGLU done, 12 down_proj rows done, 13 reduced in the cluster, 14 cluster
+ * slot published, 17 feed-forward input normalised,
  * 18 (attention CTAs) queries and the new key/value ready; layer n_layers: LM head wait
  * begin/end (0/1) and rows done (2); unused slots hold 0.  *n_needed receives the buffer
  * length.  Synchronous. */
