@@ -523,7 +523,6 @@ struct Consumer {
     int* err;
     int cw, lane;   // consumer warp 0..7, lane
     unsigned it = 0;
-    unsigned pending = 0;   // stages done with but not yet handed back
 
     // One lane of the warp waits for the stage (256 threads polling one mbarrier serialise on
     // it); __syncwarp then orders the other lanes' reads of the stage after that acquire.
@@ -555,20 +554,11 @@ struct Consumer {
         }
         return ring + (it % NS) * STAGE;
     }
-    // Done with the current stage.  The slot is handed back to the producer at once, or, when
-    // `hold`, at the next flush(): the producer's refill writes 32 KB into shared memory, and
-    // while the consumers are still reading other stages those writes compete with their reads
-    // for the shared-memory port, so short phases hand their stages back when they end.
-    QW_DEV void stage_release(bool hold = false) {
-        ++it;
-        ++pending;
-        if (!hold) flush();
-    }
-    QW_DEV void flush() {
+    // Done with the current stage: hand its slot back to the producer.
+    QW_DEV void stage_release() {
         __syncwarp();
-        if (lane == 0)
-            for (unsigned k = pending; k > 0; --k) mbar_arrive(&sm->empty[(it - k) % NS]);
-        pending = 0;
+        if (lane == 0) mbar_arrive(&sm->empty[it % NS]);
+        ++it;
     }
     // Dot products of `nrows` (at most 64, so at most 4 stages) streamed rows with sm->h.  Warp cw
     // takes rows 2 cw and 2 cw + 1 of every stage; lane l keeps one packed fp32 partial per row over

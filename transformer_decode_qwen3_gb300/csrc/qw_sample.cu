@@ -36,10 +36,12 @@ QW_DEV uint32_t order_key(float v) {
 }
 QW_DEV float key_value(uint32_t k) { return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k); }
 
-constexpr int FT = 1024, FNW = FT / 32, FNB = 2048, FCAP = 2048, FKMAX = 1024;
+constexpr int FT = 1024, FNW = FT / 32, FNB = 2048, FCAP = 2048, FKMAX = 1024, FCL = 4;
+constexpr int FUN = 4;   // float4 loads each thread keeps in flight in a pass over its part
 
 struct FShared {
     uint32_t hist[FNB];
+    float stats[3];   // this CTA's (max, min, Z relative to its max), read by the peers
     unsigned long long cand[FCAP];
     float e[FKMAX];
     float fred[FNW];
@@ -391,34 +393,73 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS)
 
 // ---------------------------------------------------------------- top-k rows (1 <= top_k <= 1024)
 // A row whose kept set is capped by a small top_k needs only its top_k best entries, plus the
-// full-vocabulary normaliser Z of the article's softmax.  One CTA of 1024 threads per row:
-//   pass 1  max, min and Z = sum of 2^((l - max) c) (online, c = log2(e) / T)
-//   pass 2  histogram of 2048 equal-width buckets of (max - l) over [0, max - min]; the first
-//           bucket where the count from the top reaches top_k bounds the k-th entry from below
-//   pass 3  gather every entry at or above that bucket (at most FCAP, else the row is handed to
-//           the general kernel by writing -1) as (order key, ~id), bitonic sort descending
+// full-vocabulary normaliser Z of the article's softmax.  One cluster of FCL CTAs (1024 threads
+// each) per row, CTA r streaming the r-th part of the row (one SM alone pulls a 608 KB row too
+// slowly); the CTAs exchange through distributed shared memory:
+//   pass 1  max, min and Z = sum of 2^((l - max) c) (online, c = log2(e) / T), merged
+//   pass 2  histogram of 2048 equal-width buckets of (max - l) over [0, max - min], summed over
+//           the cluster; the first bucket where the count from the top reaches top_k bounds the
+//           k-th entry from below
+//   pass 3  every entry at or above that bucket (at most FCAP, else the row is handed to the
+//           general kernel by writing -1) goes to rank 0 as (order key, ~id), which sorts them
+//           (bitonic, descending)
 // then, over the sorted candidates: p_i = e_i / Z, cutoff = min(top_k, 1 + #(cumsum < top_p)),
 // the draw is the first kept entry whose cumulative e exceeds u * (kept e), u from Philox as in
 // the general kernel.  Rows this kernel does not take (greedy, top_k outside [1, 1024], invalid
-// parameters) are left untouched for the general kernel that runs after it.
-__global__ void __launch_bounds__(FT, 1)
+// parameters) are left untouched for the general kernel that runs after it.  Every decision to
+// end early is taken from cluster-wide values, so all CTAs of a row take it together.
+QW_DEV void st_peer_u64(unsigned long long* local, int rank, unsigned long long v) {
+    uint32_t a;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+QW_DEV uint32_t atom_add_peer(uint32_t* local, int rank, uint32_t v) {
+    uint32_t a, old;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(a), "r"(v) : "memory");
+    return old;
+}
+QW_DEV uint32_t ld_peer_u32(const uint32_t* local, int rank) {
+    uint32_t a, v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
+
+// two CTAs per SM (at most 32 registers a thread), so the 64 clusters of a 64-row batch are
+// resident at once
+__global__ void __cluster_dims__(FCL, 1, 1) __launch_bounds__(FT, 2)
     sample_topk_kernel(const float* __restrict__ logits, int vocab, const qw_sample_params* __restrict__ params,
                        uint64_t rng_counter, int32_t* __restrict__ out) {
     __shared__ FShared sh;
     pdl_wait();
     pdl_trigger();
-    const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int row = blockIdx.x / FCL, rank = (int)cluster_rank(), tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const qw_sample_params P = params[row];
-    if (!topk_row(P, vocab)) return;
+    if (!topk_row(P, vocab)) return;   // the same for every CTA of the row
     const float* lg = logits + (size_t)row * vocab;
     const float c = 1.4426950408889634f / P.temperature;
     const int k = P.top_k;
-    const int n4 = vocab / 4;   // vocab is a multiple of 32: rows are whole float4s
+    const int n4 = vocab / 4;   // vocab is a multiple of 32: whole float4s, and n4 a multiple of FCL
+    const int i_lo = rank * (n4 / FCL), i_hi = (rank + 1) * (n4 / FCL);
+    // a pass over the part: f(i, float4 i) for i = i_lo + tid (mod FT), FUN loads in flight
+    auto sweep = [&](auto&& f) {
+        for (int i0 = i_lo + tid; i0 < i_hi; i0 += FUN * FT) {
+            float4 qs[FUN];
+#pragma unroll
+            for (int j = 0; j < FUN; ++j)
+                if (i0 + j * FT < i_hi) qs[j] = __ldg((const float4*)lg + i0 + j * FT);
+#pragma unroll
+            for (int j = 0; j < FUN; ++j)
+                if (i0 + j * FT < i_hi) f(i0 + j * FT, qs[j]);
+        }
+    };
+    for (int b = tid; b < FNB; b += FT) sh.hist[b] = 0;
+    if (tid == 0) sh.ncand = 0;
 
-    // ---- pass 1: max, min, Z
+    // ---- pass 1: max, min, Z of this CTA's part, then of the row
     float m = -INFINITY, mn = INFINITY, z = 0.f;
-    for (int i = tid; i < n4; i += FT) {
-        const float4 q = __ldg((const float4*)lg + i);
+    sweep([&](int, float4 q) {
         const float v[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
@@ -430,7 +471,7 @@ __global__ void __launch_bounds__(FT, 1)
             }
             mn = fminf(mn, v[t]);
         }
-    }
+    });
     const float M = warp_max(m);
     float zr = m == -INFINITY ? 0.f : z * exp2f((m - M) * c);
     zr = warp_sum(zr);
@@ -440,41 +481,59 @@ __global__ void __launch_bounds__(FT, 1)
         sh.fred2[warp] = mnw;
     }
     __syncthreads();
-    float gM = -INFINITY, gmn = INFINITY;
+    float cM = -INFINITY, cmn = INFINITY;
 #pragma unroll 4
     for (int w = 0; w < FNW; ++w) {
-        gM = fmaxf(gM, sh.fred[w]);
-        gmn = fminf(gmn, sh.fred2[w]);
+        cM = fmaxf(cM, sh.fred[w]);
+        cmn = fminf(cmn, sh.fred2[w]);
     }
     __syncthreads();
-    if (lane == 0) sh.fred[warp] = zr * exp2f((M - gM) * c);
-    for (int b = tid; b < FNB; b += FT) sh.hist[b] = 0;
-    if (tid == 0) sh.ncand = 0;
+    if (lane == 0) sh.fred[warp] = M == -INFINITY ? 0.f : zr * exp2f((M - cM) * c);
     __syncthreads();
+    if (tid == 0) {
+        float cz = 0.f;
+        for (int w = 0; w < FNW; ++w) cz += sh.fred[w];
+        sh.stats[0] = cM;
+        sh.stats[1] = cmn;
+        sh.stats[2] = cz;
+    }
+    cluster_sync();   // every CTA's stats, cleared histogram and candidate count are in place
+    float gM = -INFINITY, gmn = INFINITY;
+    float pm[FCL], pz[FCL];
+#pragma unroll
+    for (int r = 0; r < FCL; ++r) {
+        pm[r] = ld_peer(&sh.stats[0], r);
+        gmn = fminf(gmn, ld_peer(&sh.stats[1], r));
+        pz[r] = ld_peer(&sh.stats[2], r);
+        gM = fmaxf(gM, pm[r]);
+    }
     float Z = 0.f;
-#pragma unroll 4
-    for (int w = 0; w < FNW; ++w) Z += sh.fred[w];
-    if (!(gM > gmn) || !(Z > 0.f)) {   // a constant row (ties everywhere) or non-finite values
-        if (tid == 0) out[row] = -1;
-        return;
-    }
-    // ---- pass 2: bucket histogram
-    const float inv_w = (float)FNB / (gM - gmn);
+#pragma unroll
+    for (int r = 0; r < FCL; ++r) Z += pm[r] == -INFINITY ? 0.f : pz[r] * exp2f((pm[r] - gM) * c);
+    const bool degenerate = !(gM > gmn) || !(Z > 0.f);   // a constant row (ties everywhere) or non-finite values
+    // ---- pass 2: bucket histogram of this CTA's part
+    const float inv_w = degenerate ? 0.f : (float)FNB / (gM - gmn);
     auto bucket = [&](float v) {   // monotone in v; NaN lands in the last bucket
         const float d = (gM - v) * inv_w;
         return d < (float)(FNB - 1) ? (int)d : FNB - 1;
     };
-    for (int i = tid; i < n4; i += FT) {
-        const float4 q = __ldg((const float4*)lg + i);
-        atomicAdd(&sh.hist[bucket(q.x)], 1u);
-        atomicAdd(&sh.hist[bucket(q.y)], 1u);
-        atomicAdd(&sh.hist[bucket(q.z)], 1u);
-        atomicAdd(&sh.hist[bucket(q.w)], 1u);
-    }
-    __syncthreads();
-    // inclusive prefix counts over the buckets (2 per thread): the first bucket reaching k
+    if (!degenerate)
+        sweep([&](int, float4 q) {
+            atomicAdd(&sh.hist[bucket(q.x)], 1u);
+            atomicAdd(&sh.hist[bucket(q.y)], 1u);
+            atomicAdd(&sh.hist[bucket(q.z)], 1u);
+            atomicAdd(&sh.hist[bucket(q.w)], 1u);
+        });
+    cluster_sync();   // every part's histogram is complete
+    // the row's counts of buckets 2 tid, 2 tid + 1, and an inclusive prefix over the buckets: the
+    // first bucket reaching k (every CTA of the cluster finds the same one)
     {
-        const uint32_t h0 = sh.hist[2 * tid], h1 = sh.hist[2 * tid + 1];
+        uint32_t h0 = 0, h1 = 0;
+#pragma unroll
+        for (int r = 0; r < FCL; ++r) {
+            h0 += ld_peer_u32(&sh.hist[2 * tid], r);
+            h1 += ld_peer_u32(&sh.hist[2 * tid + 1], r);
+        }
         uint32_t incl = h0 + h1;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -497,23 +556,25 @@ __global__ void __launch_bounds__(FT, 1)
     __syncthreads();
     const int bstar = (int)sh.bstar;
     const uint32_t ncand = sh.cnt_star;
-    if (ncand > FCAP) {   // too many entries at the bound: the general kernel takes the row
-        if (tid == 0) out[row] = -1;
+    if (degenerate || ncand > FCAP) {   // the general kernel takes the row
+        cluster_sync();   // the peers have read this CTA's histogram
+        if (rank == 0 && tid == 0) out[row] = -1;
         return;
     }
-    // ---- pass 3: gather the candidates, sort them by (logit desc, id asc)
-    for (int i = tid; i < n4; i += FT) {
-        const float4 q = __ldg((const float4*)lg + i);
+    // ---- pass 3: the candidates of this part into rank 0's buffer
+    sweep([&](int i, float4 q) {
         const float v[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
         for (int t = 0; t < 4; ++t)
             if (bucket(v[t]) <= bstar) {
-                const uint32_t slot = atomicAdd(&sh.ncand, 1u);
+                const uint32_t slot = atom_add_peer(&sh.ncand, 0, 1u);
                 if (slot < FCAP)
-                    sh.cand[slot] = ((unsigned long long)order_key(v[t]) << 32) | (0xFFFFFFFFu - (uint32_t)(4 * i + t));
+                    st_peer_u64(&sh.cand[slot], 0,
+                                ((unsigned long long)order_key(v[t]) << 32) | (0xFFFFFFFFu - (uint32_t)(4 * i + t)));
             }
-    }
-    __syncthreads();
+    });
+    cluster_sync();   // rank 0 holds every candidate, and the peers are done with every exchange
+    if (rank != 0) return;
     int np2 = 1;
     while (np2 < (int)ncand) np2 <<= 1;
     for (int i = (int)ncand + tid; i < np2; i += FT) sh.cand[i] = 0ull;   // below every entry
@@ -536,7 +597,6 @@ __global__ void __launch_bounds__(FT, 1)
     // ---- top-k, top-p and the draw over the first k candidates (k <= FT)
     const bool mine = tid < k;
     const float ei = mine ? exp2f((key_value((uint32_t)(sh.cand[tid] >> 32)) - gM) * c) : 0.f;
-    // inclusive prefix sum of e over the first k entries
     float incl = ei;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -576,8 +636,8 @@ int launch_sample(const float* logits, int batch, int vocab, const qw_sample_par
                   int32_t* out_ids, const float2* tile_part, int n_part, const int* argmax_hint, int* err,
                   cudaStream_t st) {
     if (batch <= 0) return QW_OK;
-    if (pdl_launch(smp::sample_topk_kernel, dim3(batch), dim3(smp::FT), 0, st, logits, vocab, params, rng_counter,
-                   out_ids) != cudaSuccess)
+    if (pdl_launch(smp::sample_topk_kernel, dim3(batch * smp::FCL), dim3(smp::FT), 0, st, logits, vocab, params,
+                   rng_counter, out_ids) != cudaSuccess)
         return QW_ECUDA;
     count_launches(1);
     const cudaError_t e = pdl_launch(smp::sample_kernel, dim3(batch * smp::CL), dim3(smp::THREADS), 0, st, logits, vocab,
