@@ -161,3 +161,22 @@ def test_generate_agrees_with_numpy_oracle_and_recompute(tiny_shape):
         # decode position T + i - 1: each row equals the last row of a full recompute
         ref = c.forward(prompt + ids[:4], np.arange(8), c.new_cache(8))[-1]
         np.testing.assert_allclose(rows[4], ref, rtol=2e-5, atol=1e-6)
+
+
+def test_int8_weights_agree_with_numpy_oracle(tiny_shape):
+    """The C oracle run on the int8-dequantised weights (exact bf16 values, as the benchmark's
+    CPU baseline builds them) agrees with the numpy oracle's own weight_bits = 8 mode."""
+    import torch
+    w = synth.make_weights(tiny_shape, seed=4)
+    w8 = dict(w)
+    for name in w:
+        if name == "model.embed_tokens.weight" or name.endswith(R.QUANTISED_SUFFIXES):
+            deq = R.dequantize_rows_int8(*R.quantize_rows_int8(w[name]))
+            assert np.array_equal(R.round_to_bf16(deq), deq)            # exact in bf16
+            w8[name] = torch.from_numpy(deq.astype(np.float32)).to(torch.bfloat16)
+    c = C.COracle(w8, tiny_shape)
+    r = R.Qwen3Oracle(w, tiny_shape, weight_bits=8)
+    ids = [11, 200, 3, 3, 42, 255, 0, 17]
+    got = c.forward(ids, np.arange(8), c.new_cache(8))
+    ref = r.forward(ids, np.arange(8), r.new_cache())
+    assert _rel(got, ref) < 2e-6
