@@ -92,9 +92,9 @@ def config_of(name: str, K: int) -> dict:
 # kernel's source file is the one that was captured (its sha256 below), else null.
 NCU_TRAFFIC = {
     "decode_bs1": ("transformer_decode_qwen3_gb300/csrc/qw_fused.cu",
-                   "542dbfda0ea0cbeecc0879d7e05dfbeb1f3c9d3849aea3f5583e5f1e1122ff26", 1.263674e9 + 5.513216e6),
+                   "e047940d99d899b9655e3453bb302dd4075cca37f1fc51e23c44f3a003890325", 1265.92e6),
     "decode_bs1_int8": ("transformer_decode_qwen3_gb300/csrc/qw_fused.cu",
-                        "542dbfda0ea0cbeecc0879d7e05dfbeb1f3c9d3849aea3f5583e5f1e1122ff26", 671.76e6),
+                        "e047940d99d899b9655e3453bb302dd4075cca37f1fc51e23c44f3a003890325", 671.71e6),
     # all 28 layers of a step: split-KV attention (552.41 MB) + merge (3.02 MB) per layer
     "decode_bs64": ("transformer_decode_qwen3_gb300/csrc/qw_kernels.cu",
                     "9802f1b4fabf1b2e6302f2fce2bd189570c40b04cdcda5c7e94c74070000ad3d", 28 * (552.41e6 + 3.02e6)),
