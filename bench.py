@@ -92,7 +92,7 @@ def config_of(name: str, K: int) -> dict:
 # kernel's source file is the one that was captured (its sha256 below), else null.
 NCU_TRAFFIC = {
     "decode_bs1": ("transformer_decode_qwen3_gb300/csrc/qw_fused.cu",
-                   "e047940d99d899b9655e3453bb302dd4075cca37f1fc51e23c44f3a003890325", 1265.92e6),
+                   "a83d5ec64dd7d9023de2bdccd5f24dd80b1e1c80d177932f8f4d7700ea76845c", 1266.07e6),
     "decode_bs1_int8": ("transformer_decode_qwen3_gb300/csrc/qw_fused.cu",
                         "e047940d99d899b9655e3453bb302dd4075cca37f1fc51e23c44f3a003890325", 671.71e6),
     # all 28 layers of a step: split-KV attention (552.41 MB) + merge (3.02 MB) per layer

@@ -1037,7 +1037,9 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
             // merge once after it.  Scores: one key per 4-lane group (kg = lane >> 2); lane
             // dq = lane & 3 takes the 16-byte chunks u = 4 c' + dq, c' = c ^ (kg & 1), of the key
             // row (the xor puts the 8 lanes of each shared-memory phase on 8 different bank
-            // groups).  P.V: lane takes dims 4 lane .. 4 lane + 3 of both heads.
+            // groups).  P.V: lane takes dims 4 lane .. 4 lane + 3 of both heads.  The running sum
+            // is kept per key group (the rescaling factor is the same in every lane) and summed
+            // over the warp once, after the loop.
             const int kg = lane >> 2, dq = lane & 3;
             float mrun[2] = {-INFINITY, -INFINITY}, lrun[2] = {0.f, 0.f};
             float orun[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -1046,11 +1048,19 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
                 const uint8_t* st = cs.stage_wait(ok);
                 const int pi = cw >> 1, slot0 = 8 * (cw & 1);
                 const bool page_ok = ok && pi < n && sm.spg[cs.slot()][pi] >= 0;
-                const int kpos = (pg0 + pi) * QW_PAGE_SIZE + slot0 + kg;
+                const int kbase = (pg0 + pi) * QW_PAGE_SIZE + slot0;   // position of the warp's key 0
+                const int kpos = kbase + kg;
                 const bool vis = page_ok && kpos <= pos;
                 const uint8_t* page = st + (pi < n ? pi : 0) * 2 * PAGE_B;
                 // the new token's key and value come from the bf16 copies made above, not the stage
                 const uint8_t* krow = kpos == pos ? (const uint8_t*)sm.kn_b : page + (slot0 + kg) * HD * 2;
+                // this lane's dims of the 8 keys' values, read before the scores need them (rows of
+                // invisible keys hold whatever the ring slot held; they are masked below)
+                uint2 vv[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    vv[k] = kbase + k == pos ? *(const uint2*)((const uint8_t*)sm.vn_b + 8 * lane)
+                                             : *(const uint2*)(page + PAGE_B + (slot0 + k) * HD * 2 + 8 * lane);
                 float sc[2] = {0.f, 0.f};
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
@@ -1076,36 +1086,39 @@ __global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(THREADS, 1) fused_d
                     const float mnew = fmaxf(mrun[hh], mw);
                     const float alpha = mrun[hh] == -INFINITY ? 0.f : exp2f(mrun[hh] - mnew);
                     pe[hh] = vis ? exp2f(sc[hh] - mnew) : 0.f;
-                    float ps = pe[hh];
-#pragma unroll
-                    for (int o = 4; o < 32; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-                    lrun[hh] = lrun[hh] * alpha + ps;
+                    lrun[hh] = lrun[hh] * alpha + pe[hh];
                     mrun[hh] = mnew;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) orun[hh][e] *= alpha;
                 }
-                if (page_ok) {
+                // weights of the 8 keys first, then the products without branches: a key whose
+                // weights are both 0 (invisible, or not in the stage) contributes a zero value
+                float p0[8], p1[8];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const float p0 = __shfl_sync(0xffffffffu, pe[0], 4 * k);
-                        const float p1 = __shfl_sync(0xffffffffu, pe[1], 4 * k);
-                        if (p0 == 0.f && p1 == 0.f) continue;   // invisible key (warp-uniform)
-                        const int kp = (pg0 + pi) * QW_PAGE_SIZE + slot0 + k;
-                        const uint2 v = kp == pos ? *(const uint2*)((const uint8_t*)sm.vn_b + 8 * lane)
-                                                  : *(const uint2*)(page + PAGE_B + (slot0 + k) * HD * 2 + 8 * lane);
-                        const float v0 = bf16_lo(v.x), v1 = bf16_hi(v.x), v2 = bf16_lo(v.y), v3 = bf16_hi(v.y);
-                        orun[0][0] = fmaf(p0, v0, orun[0][0]);
-                        orun[0][1] = fmaf(p0, v1, orun[0][1]);
-                        orun[0][2] = fmaf(p0, v2, orun[0][2]);
-                        orun[0][3] = fmaf(p0, v3, orun[0][3]);
-                        orun[1][0] = fmaf(p1, v0, orun[1][0]);
-                        orun[1][1] = fmaf(p1, v1, orun[1][1]);
-                        orun[1][2] = fmaf(p1, v2, orun[1][2]);
-                        orun[1][3] = fmaf(p1, v3, orun[1][3]);
-                    }
+                for (int k = 0; k < 8; ++k) {
+                    p0[k] = __shfl_sync(0xffffffffu, pe[0], 4 * k);
+                    p1[k] = __shfl_sync(0xffffffffu, pe[1], 4 * k);
+                }
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const bool used = p0[k] != 0.f || p1[k] != 0.f;
+                    const uint2 v = used ? vv[k] : make_uint2(0u, 0u);
+                    const float v0 = bf16_lo(v.x), v1 = bf16_hi(v.x), v2 = bf16_lo(v.y), v3 = bf16_hi(v.y);
+                    orun[0][0] = fmaf(p0[k], v0, orun[0][0]);
+                    orun[0][1] = fmaf(p0[k], v1, orun[0][1]);
+                    orun[0][2] = fmaf(p0[k], v2, orun[0][2]);
+                    orun[0][3] = fmaf(p0[k], v3, orun[0][3]);
+                    orun[1][0] = fmaf(p1[k], v0, orun[1][0]);
+                    orun[1][1] = fmaf(p1[k], v1, orun[1][1]);
+                    orun[1][2] = fmaf(p1[k], v2, orun[1][2]);
+                    orun[1][3] = fmaf(p1[k], v3, orun[1][3]);
                 }
                 cs.stage_release();
             }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) lrun[hh] += __shfl_xor_sync(0xffffffffu, lrun[hh], o);
             if (tid == 0) stamp(p, l, 4);
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
