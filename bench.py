@@ -94,7 +94,7 @@ NCU_TRAFFIC = {
     "decode_bs1": ("transformer_decode_qwen3_gb300/csrc/qw_fused.cu",
                    "a83d5ec64dd7d9023de2bdccd5f24dd80b1e1c80d177932f8f4d7700ea76845c", 1266.07e6),
     "decode_bs1_int8": ("transformer_decode_qwen3_gb300/csrc/qw_fused.cu",
-                        "e047940d99d899b9655e3453bb302dd4075cca37f1fc51e23c44f3a003890325", 671.71e6),
+                        "a83d5ec64dd7d9023de2bdccd5f24dd80b1e1c80d177932f8f4d7700ea76845c", 667.93e6),
     # all 28 layers of a step: split-KV attention (552.41 MB) + merge (3.02 MB) per layer
     "decode_bs64": ("transformer_decode_qwen3_gb300/csrc/qw_kernels.cu",
                     "9802f1b4fabf1b2e6302f2fce2bd189570c40b04cdcda5c7e94c74070000ad3d", 28 * (552.41e6 + 3.02e6)),
