@@ -27,7 +27,7 @@ def full_int8():
 
 
 def test_int8_prompt5_greedy8_fused(full_int8):
-    """Configs[0]'s workload through the fused kernel streaming int8 codes."""
+    """A five-token prompt and eight greedy steps through the fused kernel streaming int8 codes."""
     _prompt_then_greedy(full_int8, 5, 8, call=0, path=2, min_checked=0.25)
 
 
