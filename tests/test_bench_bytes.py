@@ -53,3 +53,19 @@ def test_step_bytes_average_the_cache_over_the_timed_positions():
     want = bench.WEIGHT_BYTES + sum((bench.PROMPT + i + 1) for i in range(K)) / K * bench.KV_BYTES_PER_POS
     got = bench.DecodeBs1.bytes_per_step(None, K)
     assert abs(got - want) < 1e-6 * want
+
+
+def test_prefill_flops():
+    # projections: 2 FLOP per weight per token, every layer matrix (q, k, v, o, gate, up, down)
+    T, B = bench.PREFILL_T, bench.PREFILL_B
+    per_token = 2 * sum(math.prod(shp) for name, shp in _shapes().items() if name.endswith(R.QUANTISED_SUFFIXES))
+    linear, attn, head = bench.Prefill.flops(None)
+    assert linear == per_token * T * B
+    assert abs(linear - 14.43e12) < 0.01e12        # the 14.43 TFLOP per prefill the profiles quote
+    # attention: q.k and p.v, 2 * head_dim FLOP each per head and visible (query, key) pair; a
+    # causal prompt of T tokens has T (T + 1) / 2 pairs.  The bench counts T^2 / 2 (0.05% fewer).
+    pairs = sum(p + 1 for p in range(T))
+    exact = 4 * S.head_dim * S.n_heads * pairs * S.n_layers * B
+    assert abs(attn - exact) <= exact / T
+    # the LM head runs on the last token of each sequence only
+    assert head == 2 * S.hidden * S.vocab * B
