@@ -154,7 +154,11 @@ int qw_kv_layout(const qw_kv* kv, void** base, int64_t* layer_stride, int64_t* p
  * the cached positions 0 .. p of its sequence (the causal mask of Step 5).
  * Sequences are independent, so one call may mix fresh prompts, prompt chunks appended
  * to cached prefixes and decode tokens (a sequence of one token at the position after its
- * cache): each gets the logits of its last token. */
+ * cache): each gets the logits of its last token.
+ * Errors: QW_EINVAL (null pointer, kv of another context, n_seqs or bt_stride < 1,
+ * cu_seqlens[0] != 0, an empty sequence, n_tok > max_tokens, more than max_batch sequences
+ * with last_logits NULL), QW_ECUDA (launch failure); bad ids, positions or page ids on the
+ * device: QW_ERANGE from qw_check. */
 int qw_prefill(qw_ctx* ctx, const int32_t* ids, const int32_t* positions, const int32_t* cu_seqlens,
                int32_t n_seqs, qw_kv* kv, const int32_t* block_tables, int32_t bt_stride,
                float* last_logits, void* stream);
@@ -165,7 +169,11 @@ int qw_prefill(qw_ctx* ctx, const int32_t* ids, const int32_t* positions, const 
  *   block_tables       DEVICE int32[batch][bt_stride].
  *   logits             DEVICE float[batch][vocab], or NULL to keep them in the context
  *                      (qw_sample with logits == NULL then reads them).
- * 1 <= batch <= max_batch. */
+ * 1 <= batch <= max_batch.
+ * Errors: QW_EINVAL (null pointer, kv of another context, batch outside [1, max_batch],
+ * bt_stride < 1, or the fused path forced for a call it cannot take), QW_ECUDA (launch
+ * failure); bad ids, positions or page ids on the device: QW_ERANGE from qw_check, a
+ * bounded wait that gave up: QW_ETIMEOUT from qw_check. */
 int qw_decode_step(qw_ctx* ctx, const int32_t* tokens, const int32_t* positions, int32_t batch,
                    qw_kv* kv, const int32_t* block_tables, int32_t bt_stride, float* logits,
                    void* stream);
@@ -187,7 +195,9 @@ int qw_decode_step(qw_ctx* ctx, const int32_t* tokens, const int32_t* positions,
  * cuts are found without sorting (radix searches over the logits by count and by mass), so
  * a draw whose cumulative sum lies within fp32 rounding of a cut may differ from an exact
  * sorted evaluation.  Invalid parameters (top_k < 0, top_p outside (0, 1]) record QW_EINVAL
- * for qw_check and are clamped. */
+ * for qw_check and are clamped.
+ * Errors: QW_EINVAL (null params or out_ids, batch outside [1, max_batch], logits NULL while
+ * the context holds fewer than batch rows), QW_ECUDA (launch failure). */
 int qw_sample(qw_ctx* ctx, const float* logits, int32_t batch, const qw_sample_params* params,
               uint64_t rng_counter, int32_t* out_ids, void* stream);
 
